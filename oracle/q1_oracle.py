@@ -1,0 +1,225 @@
+"""CPU oracle for the 1-bit affine group-quantized (g128) linear layer.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, the package's smoke entry point and
+the benchmark's CPU-baseline leg may import this module.  The product path (the
+CUDA library and its Python binding) never calls it, and this module never
+imports the product: the two share no code.  The only shared module is the
+seeded input generator (bit_affine_quantized_g128_gb300/synth.py), which holds
+none of the method's arithmetic.
+
+It is a plain, slow, obviously correct restatement of what the method computes,
+written from the definitions on the pages:
+
+* "Support Bonsai-27B affine Q1" (higgs PR #212), section "What": every affine
+  1-bit weight is w = scale * q + bias with q in {0, 1}; symmetric tensors have
+  bias = -scale / 2, derived from the scale instead of stored.  Section
+  "Limitations / non-goals": forwards wider than the narrow threshold
+  dequantize to the input dtype and run a dense matmul.
+* "1-bit affine weight support" (rMLX issue #207), section "The good news -
+  packing is standard": 32 weights per uint32, fp16 scales and biases per group
+  of 128, bit 0 maps to the negative value and bit 1 to the positive one.
+* "Bonsai masked gemv" (cactus PR #775): the packed layout is the linear
+  LSB-first layout (weight k of a 32-weight run sits at bit k).
+
+Precision: dequantized values are formed in fp32 (one rounding for s + b), and
+every dot product is accumulated in fp64.  A library matmul in fp64 serves as
+the dot-product step.  Where a result is rounded to bf16/fp16 (dequantize,
+gather), torch's CPU round-to-nearest-even conversion does it.
+
+Every function here is pinned by tests/test_oracle_pins.py against facts that
+do not come from this module (hand-built words, closed forms, exact rational
+brute force, invariants).
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+GROUP_SIZE = 128
+WORD_BITS = 32
+
+_TORCH_DTYPES = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}
+
+
+# ---------------------------------------------------------------------------
+# Packing (rMLX issue, "packing is standard"; cactus PR, "linear LSB layout")
+# ---------------------------------------------------------------------------
+def unpack(words: np.ndarray, K: int) -> np.ndarray:
+    """Packed uint32 [N, K/32] -> bits uint8 [N, K].
+
+    q(n, k) = (words[n][k // 32] >> (k % 32)) & 1: the lowest bit of a word is
+    the first of its 32 weights.
+    """
+    words = np.asarray(words, dtype=np.uint32)
+    N = words.shape[0]
+    out = np.empty((N, K), dtype=np.uint8)
+    for j in range(WORD_BITS):
+        # weights k = 32*c + j for every word c
+        out[:, j::WORD_BITS] = ((words >> np.uint32(j)) & np.uint32(1)).astype(np.uint8)
+    return out
+
+
+def pack(bits: np.ndarray) -> np.ndarray:
+    """bits uint8 [N, K] (values 0/1) -> packed uint32 [N, K/32], LSB first."""
+    bits = np.asarray(bits)
+    N, K = bits.shape
+    if K % WORD_BITS:
+        raise ValueError("K must be a multiple of 32")
+    words = np.zeros((N, K // WORD_BITS), dtype=np.uint32)
+    for j in range(WORD_BITS):
+        words |= (bits[:, j::WORD_BITS].astype(np.uint32) & np.uint32(1)) << np.uint32(j)
+    return words
+
+
+# ---------------------------------------------------------------------------
+# Metadata ("Support Bonsai-27B affine Q1", section "What": bias = -scale/2)
+# ---------------------------------------------------------------------------
+def resolve_metadata(scales: np.ndarray, biases: np.ndarray | None):
+    """fp16 scales/biases [N, G] -> (s, b) in fp32.
+
+    Affine: b = fp32(bias).  Symmetric (biases is None): b = -0.5 * s in fp32,
+    which is exact (halving an fp16 value in fp32 never rounds).
+    """
+    s = np.asarray(scales, dtype=np.float16).astype(np.float32)
+    if biases is None:
+        b = np.float32(-0.5) * s
+    else:
+        b = np.asarray(biases, dtype=np.float16).astype(np.float32)
+    return s, b
+
+
+def is_symmetric(scales: np.ndarray, biases: np.ndarray) -> bool:
+    """True iff every stored bias equals -scale/2 exactly (compared in fp32).
+
+    The page's loader compacts "exact symmetric" biases only; one group that
+    differs keeps the general affine path.  +0 and -0 compare equal; a NaN
+    never equals anything, so a NaN scale or bias reads as affine.
+    """
+    s, b = resolve_metadata(scales, biases)
+    derived = np.float32(-0.5) * s
+    return bool(np.all(b == derived))
+
+
+# ---------------------------------------------------------------------------
+# Dequantization (w = scale * q + bias, q in {0, 1})
+# ---------------------------------------------------------------------------
+def dequantize_f32(words: np.ndarray, scales: np.ndarray, biases: np.ndarray | None,
+                   K: int) -> np.ndarray:
+    """Dense fp32 weights [N, K].
+
+    q = 0 gives the bias itself (bit for bit); q = 1 gives fl32(s + b), one
+    fp32 rounding.  Symmetric metadata therefore gives exactly -s/2 and +s/2.
+    """
+    q = unpack(words, K)
+    s, b = resolve_metadata(scales, biases)
+    s_k = np.repeat(s, GROUP_SIZE, axis=1)          # [N, K]
+    b_k = np.repeat(b, GROUP_SIZE, axis=1)
+    one = (s_k + b_k).astype(np.float32)            # fl32(s + b)
+    return np.where(q == 1, one, b_k).astype(np.float32)
+
+
+def round_to(values_f32: np.ndarray, dtype: str) -> torch.Tensor:
+    """fp32 array -> CPU tensor of `dtype` ('bf16', 'f16', 'f32'), one RNE."""
+    t = torch.from_numpy(np.array(values_f32, dtype=np.float32, copy=True))
+    return t.to(_TORCH_DTYPES[dtype])
+
+
+def dequantize(words, scales, biases, K: int, dtype: str = "bf16") -> torch.Tensor:
+    """Dense weights [N, K] in `dtype`: the fp32 dequantized value, rounded once."""
+    return round_to(dequantize_f32(words, scales, biases, K), dtype)
+
+
+# ---------------------------------------------------------------------------
+# Matmul (decode QMV, narrow and wide QMM all compute the same product)
+# ---------------------------------------------------------------------------
+def _x64(x) -> np.ndarray:
+    if isinstance(x, torch.Tensor):
+        return x.detach().to(torch.float64).numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+def qmm(x, words, scales, biases, K: int, rows=None) -> np.ndarray:
+    """Y[m][n] = sum_k x[m][k] * Wd[n][k], accumulated in fp64.
+
+    x: [M, K] (bf16 tensor or array; widened exactly to fp64).
+    rows: optional index array of output features n to compute (the others are
+    not evaluated); the result then has shape [M, len(rows)].
+    """
+    if rows is not None:
+        rows = np.asarray(rows)
+        words = np.asarray(words)[rows]
+        scales = np.asarray(scales)[rows]
+        biases = None if biases is None else np.asarray(biases)[rows]
+    wd = dequantize_f32(words, scales, biases, K).astype(np.float64)
+    x64 = _x64(x)
+    if x64.ndim == 1:
+        x64 = x64[None, :]
+    return x64 @ wd.T
+
+
+def silu(g: np.ndarray) -> np.ndarray:
+    """SiLU(g) = g / (1 + exp(-g)) in fp64."""
+    g = np.asarray(g, dtype=np.float64)
+    return g / (1.0 + np.exp(-g))
+
+
+def ffn(x, gate, up, down, rows=None) -> np.ndarray:
+    """Dense FFN block: y = Down . (SiLU(Gate . x) * (Up . x)).
+
+    gate/up/down are (words, scales, biases, K) tuples.  g, u and h are kept in
+    fp64 with no intermediate rounding.  rows selects output features of the
+    down projection (all when None).  Returns (y [M, D'], h [M, F]).
+    """
+    g = qmm(x, *gate)
+    u = qmm(x, *up)
+    h = silu(g) * u
+    y = qmm(h, *down, rows=rows)
+    return y, h
+
+
+# ---------------------------------------------------------------------------
+# Embedding gather ("Support Bonsai-27B affine Q1": Q1 embeddings, tied head)
+# ---------------------------------------------------------------------------
+def embed_gather(ids, words, scales, biases, K: int, dtype: str = "bf16"):
+    """out[t] = dequantized row ids[t], rounded to `dtype`.
+
+    An id outside [0, V) gives a zero row and is counted.  Returns
+    (out tensor [T, K], number of out-of-range ids).
+    """
+    ids = np.asarray(ids, dtype=np.int64)
+    V = np.asarray(words).shape[0]
+    T = ids.shape[0]
+    out = np.zeros((T, K), dtype=np.float32)
+    bad = 0
+    for t in range(T):
+        r = int(ids[t])
+        if r < 0 or r >= V:
+            bad += 1
+            continue
+        b_row = None if biases is None else np.asarray(biases)[r:r + 1]
+        out[t] = dequantize_f32(np.asarray(words)[r:r + 1], np.asarray(scales)[r:r + 1],
+                                b_row, K)[0]
+    return round_to(out, dtype), bad
+
+
+# ---------------------------------------------------------------------------
+# Storage accounting (bytes per weight of the packed format)
+# ---------------------------------------------------------------------------
+def storage_bytes(N: int, K: int, symmetric: bool) -> dict:
+    """Bytes held by one packed weight: bits, fp16 scales, fp16 biases."""
+    G = K // GROUP_SIZE
+    packed = N * K // 8
+    s = N * G * 2
+    b = 0 if symmetric else N * G * 2
+    return {"packed": packed, "scales": s, "biases": b, "total": packed + s + b}
+
+
+def tolerance_bound(x, wd_f32: np.ndarray, rel: float = 2e-2) -> np.ndarray:
+    """Per-element matmul error bound rel * ||x_m|| * ||Wd_n|| / sqrt(K) [M, N]."""
+    x64 = _x64(x)
+    if x64.ndim == 1:
+        x64 = x64[None, :]
+    K = x64.shape[1]
+    xn = np.linalg.norm(x64, axis=1)
+    wn = np.linalg.norm(np.asarray(wd_f32, dtype=np.float64), axis=1)
+    return rel * np.outer(xn, wn) / np.sqrt(K)

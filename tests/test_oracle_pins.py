@@ -1,0 +1,314 @@
+"""Pins of the CPU oracle to facts that do not come from the oracle itself.
+
+Each test checks one oracle function against hand-written fixtures
+(tests/golden/), closed forms, exact rational brute force, library routines
+that reduce to the same special case, or invariants of the definition.  The
+cases are chosen so that a plausible slip (wrong bit order, wrong sign of the
+derived bias, fma instead of select, dropped bias term, transposed operand)
+fails at least one of them.
+"""
+import math
+import os
+import struct
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import q1_oracle as O
+from bit_affine_quantized_g128_gb300 import synth
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rows(name):
+    with open(os.path.join(GOLD, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            yield [c.strip() for c in line.split("|")]
+
+
+def _f16(h):
+    return np.frombuffer(struct.pack("<H", h), dtype=np.float16)[0]
+
+
+def _bits32(v):
+    return struct.unpack("<I", np.float32(v).tobytes())[0]
+
+
+# ---------------------------------------------------------------- packing
+def test_unpack_golden_lsb_first():
+    for K, words, idx in _rows("unpack_lsb_first.txt"):
+        K = int(K)
+        w = np.array([[int(h, 16) for h in words.split()]], dtype=np.uint32)
+        want = set(int(i) for i in idx.split())
+        got = O.unpack(w, K)[0]
+        assert set(np.nonzero(got)[0].tolist()) == want, (words, idx)
+        assert got.dtype == np.uint8 and set(np.unique(got)) <= {0, 1}
+
+
+def test_pack_golden_lsb_first():
+    for K, words, idx in _rows("unpack_lsb_first.txt"):
+        K = int(K)
+        bits = np.zeros((1, K), dtype=np.uint8)
+        for i in idx.split():
+            bits[0, int(i)] = 1
+        want = np.array([[int(h, 16) for h in words.split()]], dtype=np.uint32)
+        np.testing.assert_array_equal(O.pack(bits), want)
+
+
+def test_pack_matches_numpy_packbits_little():
+    # LSB-first packing of 32 bits into a little-endian uint32 is what
+    # numpy.packbits(bitorder='little') followed by a little-endian uint32 view
+    # computes; an independent library routine for the same layout.
+    bits = synth.bits(7, 256, seed=11)
+    lib = np.packbits(bits, axis=1, bitorder="little").view("<u4")
+    np.testing.assert_array_equal(O.pack(bits), lib)
+
+
+def test_pack_unpack_roundtrip_both_directions():
+    w = synth.weight_words(9, 384, seed=5)
+    np.testing.assert_array_equal(O.pack(O.unpack(w, 384)), w)
+    b = synth.bits(9, 384, seed=6)
+    np.testing.assert_array_equal(O.unpack(O.pack(b), 384), b)
+
+
+# ---------------------------------------------------------------- dequant
+def test_dequant_golden_values():
+    for sh, bh, q, f32h, bf16h, f16h, _note in _rows("dequant_values.txt"):
+        s = np.array([[_f16(int(sh, 16))]], dtype=np.float16)
+        b = None if bh == "sym" else np.array([[_f16(int(bh, 16))]], dtype=np.float16)
+        K = 128
+        word = 0xFFFFFFFF if int(q) else 0
+        w = np.full((1, K // 32), word, dtype=np.uint32)
+        d = O.dequantize_f32(w, s, b, K)
+        assert all(_bits32(v) == int(f32h, 16) for v in d[0]), (sh, bh, q)
+        bf = O.dequantize(w, s, b, K, "bf16").view(torch.int16).numpy().astype(np.uint16)
+        hf = O.dequantize(w, s, b, K, "f16").view(torch.int16).numpy().astype(np.uint16)
+        assert np.all(bf == int(bf16h, 16)), (sh, bh, q, hex(bf[0, 0]))
+        assert np.all(hf == int(f16h, 16)), (sh, bh, q, hex(hf[0, 0]))
+
+
+def test_bf16_rounding_golden():
+    for f32h, bf16h in _rows("bf16_rounding.txt"):
+        v = np.frombuffer(struct.pack("<I", int(f32h, 16)), dtype=np.float32)
+        got = O.round_to(v, "bf16").view(torch.int16).numpy().astype(np.uint16)[0]
+        assert got == int(bf16h, 16), (f32h, hex(got))
+
+
+def test_dequant_all_zero_bits_is_bias_all_one_is_sum():
+    t = synth.q1_tensor(5, 256, seed=21, affine=True)
+    s = t.scales.astype(np.float32)
+    b = t.biases.astype(np.float32)
+    zeros = np.zeros_like(t.words)
+    ones = np.full_like(t.words, 0xFFFFFFFF)
+    d0 = O.dequantize_f32(zeros, t.scales, t.biases, 256)
+    d1 = O.dequantize_f32(ones, t.scales, t.biases, 256)
+    for g in range(2):
+        np.testing.assert_array_equal(d0[:, g * 128:(g + 1) * 128], np.repeat(b[:, g:g + 1], 128, 1))
+        np.testing.assert_array_equal(d1[:, g * 128:(g + 1) * 128],
+                                      np.repeat((s[:, g:g + 1] + b[:, g:g + 1]).astype(np.float32), 128, 1))
+
+
+def test_symmetric_values_are_plus_minus_half_scale_and_both_occur():
+    t = synth.q1_tensor(6, 512, seed=31, affine=False)
+    d = O.dequantize_f32(t.words, t.scales, None, 512)
+    bits = O.unpack(t.words, 512)
+    for n in range(6):
+        for g in range(4):
+            half = np.float32(t.scales[n, g]) / np.float32(2)
+            vals = d[n, g * 128:(g + 1) * 128]
+            q = bits[n, g * 128:(g + 1) * 128]
+            assert set(np.unique(vals).tolist()) == {float(-half), float(half)}
+            # bit 1 -> +s/2, bit 0 -> -s/2 (rMLX issue: bit0 -> negative, bit1 -> positive)
+            assert np.all(vals[q == 1] == half) and np.all(vals[q == 0] == -half)
+
+
+def test_symmetric_equals_affine_when_bias_is_exactly_minus_half_scale():
+    # scales >= 2^-13 are normal fp16 values whose half is again an fp16 value,
+    # so storing the bias -s/2 explicitly is lossless.
+    t = synth.q1_tensor(4, 256, seed=41, affine=False)
+    s = np.maximum(t.scales, np.float16(2.0 ** -13))
+    b = (-(s.astype(np.float32) / 2)).astype(np.float16)
+    assert np.all(b.astype(np.float32) == -s.astype(np.float32) / 2)
+    da = O.dequantize_f32(t.words, s, b, 256)
+    ds = O.dequantize_f32(t.words, s, None, 256)
+    np.testing.assert_array_equal(da.view(np.uint32), ds.view(np.uint32))
+
+
+# ---------------------------------------------------------------- matmul
+def _exact_qmm(x_bf16, words, scales, biases, K):
+    """Exact rational brute force: dequant with Python Fractions of the fp32
+    values (derived independently of the oracle: bit test per weight, fp32
+    add done by numpy scalar), then exact sums."""
+    xs = x_bf16.to(torch.float64).numpy()
+    M, N = xs.shape[0], words.shape[0]
+    out = [[Fraction(0)] * N for _ in range(M)]
+    for n in range(N):
+        for k in range(K):
+            q = (int(words[n, k // 32]) >> (k % 32)) & 1
+            s = np.float32(scales[n, k // 128])
+            b = np.float32(biases[n, k // 128]) if biases is not None else np.float32(-0.5) * s
+            w = np.float32(s + b) if q else b
+            fw = Fraction(float(w))
+            for m in range(M):
+                out[m][n] += Fraction(float(xs[m, k])) * fw
+    return out
+
+
+@pytest.mark.parametrize("affine", [False, True])
+def test_qmm_brute_force_tiny(affine):
+    K, N, M = 128, 4, 3
+    t = synth.q1_tensor(N, K, seed=51 + affine, affine=affine)
+    x = synth.activations(M, K, seed=61)
+    want = _exact_qmm(x, t.words, t.scales, t.biases, K)
+    got = O.qmm(x, t.words, t.scales, t.biases, K)
+    for m in range(M):
+        for n in range(N):
+            exact = float(want[m][n])
+            assert abs(got[m, n] - exact) <= 1e-12 * max(1.0, abs(exact)), (m, n)
+
+
+def test_qmm_one_hot_selects_a_column():
+    K, N = 256, 6
+    t = synth.q1_tensor(N, K, seed=71, affine=True)
+    wd = O.dequantize_f32(t.words, t.scales, t.biases, K)
+    for k in (0, 1, 31, 32, 127, 128, 200, 255):
+        x = torch.zeros(1, K, dtype=torch.bfloat16)
+        x[0, k] = 1.0
+        y = O.qmm(x, t.words, t.scales, t.biases, K)
+        np.testing.assert_array_equal(y[0], wd[:, k].astype(np.float64))
+
+
+@pytest.mark.parametrize("affine", [False, True])
+def test_qmm_all_ones_closed_form(affine):
+    # x = 1 everywhere: Y[n] = sum_g popcount_g * fl32(s+b) + (128 - popcount_g) * b
+    K, N = 384, 5
+    t = synth.q1_tensor(N, K, seed=81, affine=affine)
+    x = torch.ones(1, K, dtype=torch.bfloat16)
+    y = O.qmm(x, t.words, t.scales, t.biases, K)[0]
+    for n in range(N):
+        tot = Fraction(0)
+        for g in range(K // 128):
+            pc = sum(bin(int(t.words[n, c])).count("1") for c in range(4 * g, 4 * g + 4))
+            s = np.float32(t.scales[n, g])
+            b = np.float32(t.biases[n, g]) if affine else np.float32(-0.5) * s
+            tot += pc * Fraction(float(np.float32(s + b))) + (128 - pc) * Fraction(float(b))
+        assert abs(y[n] - float(tot)) <= 1e-12 * max(1.0, abs(float(tot)))
+
+
+def test_symmetric_complement_negates():
+    K, N, M = 256, 7, 2
+    t = synth.q1_tensor(N, K, seed=91, affine=False)
+    x = synth.activations(M, K, seed=92)
+    y = O.qmm(x, t.words, t.scales, None, K)
+    yc = O.qmm(x, ~t.words, t.scales, None, K)
+    np.testing.assert_allclose(yc, -y, rtol=0, atol=1e-12)
+
+
+def test_qmm_linear_in_x():
+    K, N = 256, 5
+    t = synth.q1_tensor(N, K, seed=101, affine=True)
+    a = synth.activations(1, K, seed=102)
+    b = synth.activations(1, K, seed=103)
+    ya = O.qmm(a, t.words, t.scales, t.biases, K)
+    yb = O.qmm(b, t.words, t.scales, t.biases, K)
+    yab = O.qmm(a.double() * 2.0 + b.double() * -3.0, t.words, t.scales, t.biases, K)
+    np.testing.assert_allclose(yab, 2 * ya - 3 * yb, rtol=1e-12, atol=1e-12)
+
+
+def test_qmm_rows_subset_matches_full():
+    K, N = 256, 9
+    t = synth.q1_tensor(N, K, seed=111, affine=True)
+    x = synth.activations(2, K, seed=112)
+    full = O.qmm(x, t.words, t.scales, t.biases, K)
+    rows = np.array([8, 0, 3])
+    np.testing.assert_array_equal(O.qmm(x, t.words, t.scales, t.biases, K, rows=rows), full[:, rows])
+
+
+def test_affine_with_exact_minus_half_bias_close_to_symmetric():
+    K, N = 512, 4
+    t = synth.q1_tensor(N, K, seed=121, affine=False)
+    s = np.maximum(t.scales, np.float16(2.0 ** -13))
+    b = (-(s.astype(np.float32) / 2)).astype(np.float16)
+    x = synth.activations(3, K, seed=122)
+    np.testing.assert_array_equal(O.qmm(x, t.words, s, b, K), O.qmm(x, t.words, s, None, K))
+
+
+# ---------------------------------------------------------------- FFN
+def test_silu_closed_form():
+    for g in (-20.0, -1.5, 0.0, 0.25, 3.0, 30.0):
+        assert O.silu(np.array([g]))[0] == pytest.approx(g / (1 + math.exp(-g)), rel=1e-15, abs=1e-300)
+    assert O.silu(np.array([0.0]))[0] == 0.0
+
+
+def test_ffn_brute_force_tiny():
+    D, F, M = 128, 256, 2
+    gate = synth.q1_tensor(F, D, seed=131, affine=False)
+    up = synth.q1_tensor(F, D, seed=132, affine=True)
+    down = synth.q1_tensor(D, F, seed=133, affine=False)
+    x = synth.activations(M, D, seed=134)
+    g = _exact_qmm(x, gate.words, gate.scales, None, D)
+    u = _exact_qmm(x, up.words, up.scales, up.biases, D)
+    h = np.array([[float(g[m][f]) / (1 + math.exp(-float(g[m][f]))) * float(u[m][f])
+                   for f in range(F)] for m in range(M)])
+    # the down projection of h, summed with math.fsum (exactly rounded sums)
+    wd = O.dequantize_f32(down.words, down.scales, None, F)  # pinned above
+    want = np.array([[math.fsum(h[m, k] * float(wd[n, k]) for k in range(F)) for n in range(D)]
+                     for m in range(M)])
+    y, h_o = O.ffn(x, (gate.words, gate.scales, None, D), (up.words, up.scales, up.biases, D),
+                   (down.words, down.scales, None, F))
+    np.testing.assert_allclose(h_o, h, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(y, want, rtol=1e-10, atol=1e-12)
+
+
+# ---------------------------------------------------------------- gather
+def test_embed_gather_rows_and_out_of_range():
+    V, K = 10, 256
+    t = synth.q1_tensor(V, K, seed=141, affine=True)
+    ids = np.array([3, 0, 9, 10, -1, 3], dtype=np.int32)
+    out, bad = O.embed_gather(ids, t.words, t.scales, t.biases, K, "f32")
+    assert bad == 2
+    wd = O.dequantize_f32(t.words, t.scales, t.biases, K)
+    for i, r in enumerate(ids):
+        if 0 <= r < V:
+            np.testing.assert_array_equal(out[i].numpy(), wd[r])
+        else:
+            assert torch.all(out[i] == 0)
+
+
+# ---------------------------------------------------------------- symmetric check
+def test_is_symmetric_exact_and_edge_cases():
+    s = np.array([[0.5, 0.25], [1.0, 2.0 ** -13]], dtype=np.float16)
+    b = (-(s.astype(np.float32) / 2)).astype(np.float16)
+    assert O.is_symmetric(s, b)
+    b2 = b.copy()
+    b2[1, 1] = np.float16(-2.0 ** -13)  # one group differs -> affine
+    assert not O.is_symmetric(s, b2)
+    # +0 and -0: s = 0 gives derived bias -0; a stored +0 still counts as equal
+    z = np.zeros((1, 1), dtype=np.float16)
+    assert O.is_symmetric(z, np.zeros((1, 1), dtype=np.float16))
+    nan = np.array([[np.nan]], dtype=np.float16)
+    assert not O.is_symmetric(nan, nan)
+    # a scale too small for -s/2 to be an fp16 value cannot be stored exactly
+    tiny = np.array([[_f16(0x0001)]], dtype=np.float16)
+    assert not O.is_symmetric(tiny, (-(tiny.astype(np.float32) / 2)).astype(np.float16))
+
+
+# ---------------------------------------------------------------- accounting
+def test_storage_bytes_bias_is_one_sixty_fourth_byte_per_weight():
+    # "Support Bonsai-27B affine Q1", "Measured impact": 412,262,400 bytes of
+    # fp16 biases removed; at 2 bytes per 128 weights that is 26.38e9 weights,
+    # consistent with a 27B-parameter checkpoint.
+    st = O.storage_bytes(17408, 5120, symmetric=False)
+    assert st["biases"] * 64 == 17408 * 5120
+    assert st["packed"] == 17408 * 5120 // 8
+    params = 412_262_400 * 64
+    assert 26.0e9 < params < 27.0e9
+    sym = O.storage_bytes(17408, 5120, symmetric=True)
+    # 1.125 bits per weight symmetric, 1.25 affine
+    assert sym["total"] * 8 / (17408 * 5120) == pytest.approx(1.125)
+    assert st["total"] * 8 / (17408 * 5120) == pytest.approx(1.25)
