@@ -1,0 +1,488 @@
+"""Benchmark of the Q1 (1-bit affine, group size 128) linear layer on GB300.
+
+Headline workload (decode QMV, M = 1, 27B-class shapes): one decode step is one
+token through a stack of 64 layers, each with four Q1 projections
+  gate  [17408 x 5120]   up [17408 x 5120]   down [5120 x 17408]   attn [5120 x 5120]
+with symmetric metadata (bias derived, not stored) and bf16 activations ~N(0,1).
+The 64 layers hold 2.64 GB of packed weights and scales, 20x the 129 MB L2, so
+every step streams its weights from HBM (no flush needed).  A step is replayed
+as a CUDA graph of the library's public calls.
+
+  value      achieved HBM GB/s = algorithmic bytes of the step / device time
+             (packed words + fp16 metadata + x + y, each once)
+  e2e        the same metric with the step's activations copied in from pinned
+             host memory and its outputs copied back inside the timed region
+  roofline   the narrow kernel (the only kernel of the step) against the
+             measured HBM copy bandwidth
+  sub        narrow M = 2..8 GB/s, the affine variant, and prefill TFLOP/s
+
+`--impl reference` times the CPU oracle (the only reference implementation:
+the pages publish no code) on the same metric and a bounded sample.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+LAYERS = 64
+D_MODEL, D_FF = 5120, 17408
+SHAPES = (("gate", D_FF, D_MODEL), ("up", D_FF, D_MODEL), ("down", D_MODEL, D_FF),
+          ("attn", D_MODEL, D_MODEL))
+WORKLOAD = "q1 decode QMV M=1, 64 layers x {gate,up 17408x5120; down 5120x17408; attn 5120x5120}, symmetric g128"
+
+# DRAM traffic per launch of the narrow kernel on the gate shape (17408 x 5120,
+# M = 1), from ncu (dram__bytes_read.sum + dram__bytes_write.sum), and the
+# sha256 of q1_narrow.cu it was taken on; reported as null once the source differs.
+NCU_TRAFFIC = {"bytes": None, "source_sha256": None}
+
+
+def weight_bytes(N, K, affine):
+    G = K // 128
+    return N * K // 8 + N * G * 2 * (2 if affine else 1)
+
+
+def step_bytes(M, affine=False):
+    tot = 0
+    for _, N, K in SHAPES:
+        tot += weight_bytes(N, K, affine) + M * K * 2 + M * N * 2
+    return tot * LAYERS
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            p = [c.strip() for c in ln.split(",")]
+            if len(p) < 8:
+                continue
+            try:
+                sm.append(float(p[0]))
+                mx.append(float(p[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, p[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (runs in a child process pinned to one thread)
+# ---------------------------------------------------------------------------
+def cpu_worker(seconds: float):
+    import numpy as np
+    from bit_affine_quantized_g128_gb300 import synth
+    from oracle import q1_oracle as O
+    N, K = D_FF, D_MODEL
+    rows_per_chunk = 256
+    t = synth.q1_tensor(2048, K, seed=1001, affine=False)
+    x = synth.activations(1, K, seed=1006)
+    done_bytes, done_rows = 0, 0
+    t0 = time.perf_counter()
+    i = 0
+    while time.perf_counter() - t0 < seconds:
+        r0 = (i * rows_per_chunk) % 2048
+        sl = slice(r0, r0 + rows_per_chunk)
+        O.qmm(x, t.words[sl], t.scales[sl], None, K)
+        done_rows += rows_per_chunk
+        done_bytes += weight_bytes(rows_per_chunk, K, False) + K * 2 + rows_per_chunk * 2
+        i += 1
+    el = time.perf_counter() - t0
+    print(json.dumps({"bytes": done_bytes, "seconds": el, "rows": done_rows}))
+
+
+def cpu_baseline(seconds: float):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-worker", str(seconds)],
+                       capture_output=True, text=True, env=env, timeout=600)
+    if r.returncode != 0:
+        return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                "sample": f"failed: {r.stderr.strip()[-200:]}"}
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": d["bytes"] / d["seconds"] / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": (f"oracle QMV M=1 on {d['rows']} rows of a symmetric 17408x5120 gate matrix "
+                       f"(chunks of 256 rows, {d['seconds']:.1f} s, 1 thread); GB/s of the same "
+                       "algorithmic bytes per row as the GPU metric")}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def build_stack(q1, synth, torch, device, affine, seed0):
+    layers = []
+    for li in range(LAYERS):
+        ws = {}
+        for j, (name, N, K) in enumerate(SHAPES):
+            sd = seed0 + 4 * li + j
+            w = synth.device_weight_words(N, K, sd, device)
+            s = synth.device_scales(N, K, sd + 7919, device)
+            b = synth.device_biases(N, K, sd + 15485863, device) if affine else None
+            ws[name] = q1.Q1Weight(w, s, b, K)
+        layers.append(ws)
+    return layers
+
+
+def make_step(q1, torch, layers, M, device):
+    xs, ys = [], []
+    g = torch.Generator(device=device)
+    g.manual_seed(1006 + M)
+    for ws in layers:
+        for name, N, K in SHAPES:
+            xs.append(torch.randn((M, K), generator=g, device=device).to(torch.bfloat16))
+            ys.append(torch.empty((M, N), dtype=torch.bfloat16, device=device))
+
+    def step():
+        i = 0
+        for ws in layers:
+            for name, N, K in SHAPES:
+                if M == 1:
+                    q1.qmv(ws[name], xs[i], out=ys[i].view(N))
+                else:
+                    q1.qmm_narrow(ws[name], xs[i], out=ys[i])
+                i += 1
+    return step, xs, ys
+
+
+def time_graph(torch, step, warmup, steps, stream):
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    return graph
+
+
+def run_timed(torch, graph, steps, stream, dist=None):
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    return e0.elapsed_time(e1) / 1e3  # seconds
+
+
+def time_prefill(q1, synth, torch, device, M, shape, affine, reps=20):
+    name, N, K = shape
+    nl = 6  # rotate over weights + activations larger than L2
+    Ws = [q1.Q1Weight(synth.device_weight_words(N, K, 77 + i, device),
+                      synth.device_scales(N, K, 177 + i, device),
+                      synth.device_biases(N, K, 277 + i, device) if affine else None, K)
+          for i in range(nl)]
+    g = torch.Generator(device=device)
+    g.manual_seed(1004)
+    xs = [torch.randn((M, K), generator=g, device=device).to(torch.bfloat16) for _ in range(nl)]
+    ys = [torch.empty((M, N), dtype=torch.bfloat16, device=device) for _ in range(nl)]
+    for i in range(nl):
+        q1.qmm(Ws[i], xs[i], out=ys[i])
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for r in range(reps):
+        i = r % nl
+        q1.qmm(Ws[i], xs[i], out=ys[i])
+    e1.record()
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) / 1e3 / reps
+    # unfused comparator: dequantize to bf16, then a dense bf16 GEMM (cuBLAS via torch)
+    wd = [q1.dequantize(Ws[i], torch.bfloat16) for i in range(2)]
+    torch.matmul(xs[0], wd[0].T, out=ys[0])
+    torch.cuda.synchronize()
+    e0.record()
+    for r in range(reps):
+        i = r % 2
+        tmp = q1.dequantize(Ws[i], torch.bfloat16)
+        torch.matmul(xs[i], tmp.T, out=ys[i])
+    e1.record()
+    torch.cuda.synchronize()
+    t_unfused = e0.elapsed_time(e1) / 1e3 / reps
+    del Ws, xs, ys, wd
+    return 2.0 * M * N * K / t / 1e12, 2.0 * M * N * K / t_unfused / 1e12
+
+
+def gpu_arm(args):
+    import torch
+    from bit_affine_quantized_g128_gb300 import build as qbuild
+    from bit_affine_quantized_g128_gb300 import q1, synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if rank == 0:
+        qbuild.build()
+    if dist is not None:
+        dist.barrier()
+    q1.load_library()
+
+    stream = torch.cuda.Stream(device=device)
+    layers = build_stack(q1, synth, torch, device, affine=False, seed0=5000 + 1000 * rank)
+    torch.cuda.synchronize()
+
+    # ---- headline: decode M = 1
+    step, xs, ys = make_step(q1, torch, layers, 1, device)
+    graph = time_graph(torch, step, args.warmup, args.steps, stream)
+    with ClockSampler(local) as clk:
+        secs = run_timed(torch, graph, args.steps, stream, dist)
+    clocks = clk.summary()
+    t_max = secs
+    if dist is not None:
+        tt = torch.tensor([secs], dtype=torch.float64, device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_max = float(tt.item())
+    bytes_step = step_bytes(1)
+    value = bytes_step * args.steps * world / t_max / 1e9
+    launches = args.steps * LAYERS * len(SHAPES)
+
+    # ---- e2e: inputs from pinned host memory, outputs back, every step
+    x_host = torch.empty(sum(x.numel() for x in xs), dtype=torch.bfloat16).pin_memory()
+    y_host = torch.empty(sum(y.numel() for y in ys), dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(x_host, device=device)
+    y_dev = torch.empty_like(y_host, device=device)
+    # the graph's x/y buffers are views into one flat device buffer each
+    off = 0
+    for x in xs:
+        n = x.numel()
+        x_dev[off:off + n].copy_(x.reshape(-1))
+        off += n
+    x_host.copy_(x_dev.cpu())
+    x_views, y_views, off, offy = [], [], 0, 0
+    for x, y in zip(xs, ys):
+        x_views.append(x_dev[off:off + x.numel()].view(x.shape))
+        y_views.append(y_dev[offy:offy + y.numel()].view(y.shape))
+        off += x.numel()
+        offy += y.numel()
+
+    def step_e2e():
+        i = 0
+        for ws in layers:
+            for name, N, K in SHAPES:
+                q1.qmv(ws[name], x_views[i], out=y_views[i].view(N))
+                i += 1
+    g2 = time_graph(torch, step_e2e, 2, 2, stream)
+    e2e_steps = max(10, args.steps // 10)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            x_dev.copy_(x_host, non_blocking=True)
+            g2.replay()
+            y_host.copy_(y_dev, non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    t_e2e = e0.elapsed_time(e1) / 1e3
+    if dist is not None:
+        tt = torch.tensor([t_e2e], dtype=torch.float64, device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_e2e = float(tt.item())
+    e2e = {"value": bytes_step * e2e_steps * world / t_e2e / 1e9, "unit": "GB/s",
+           "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": y_host.numel() * 2,
+           "path": "q1_qmv calls captured in a CUDA graph; x copied from pinned host and y back every step"}
+    del g2, graph
+
+    sub = {}
+    if not args.quick:
+        # narrow M = 2..8 (same stack), GB/s
+        for M in (2, 4, 8):
+            stp, _, _ = make_step(q1, torch, layers, M, device)
+            gm = time_graph(torch, stp, 3, 3, stream)
+            n = max(20, args.steps // 10)
+            s_ = run_timed(torch, gm, n, stream)
+            sub[f"narrow_M{M}_GBps"] = round(step_bytes(M) * n / s_ / 1e9, 1)
+            del gm
+        del layers
+        torch.cuda.empty_cache()
+        # affine metadata (bias stored): M = 1
+        la = build_stack(q1, synth, torch, device, affine=True, seed0=9000)
+        stp, _, _ = make_step(q1, torch, la, 1, device)
+        gm = time_graph(torch, stp, 3, 3, stream)
+        n = max(20, args.steps // 10)
+        s_ = run_timed(torch, gm, n, stream)
+        sub["affine_M1_GBps"] = round(step_bytes(1, True) * n / s_ / 1e9, 1)
+        del gm, la
+        torch.cuda.empty_cache()
+        # prefill on the tensor cores
+        for M in (128, 2048):
+            for shp in (SHAPES[0], SHAPES[2]):
+                tf, tf_unf = time_prefill(q1, synth, torch, device, M, shp, affine=False)
+                sub[f"prefill_M{M}_{shp[0]}_TFLOPs"] = round(tf, 1)
+                sub[f"prefill_M{M}_{shp[0]}_unfused_TFLOPs"] = round(tf_unf, 1)
+                torch.cuda.empty_cache()
+    assert q1.device_errors() == 0, "device-side wait ran out"
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except Exception:
+        pass
+    peak = peaks.get("hbm_gbs")
+    peak_src = "measured" if peak else "fallback"
+    if not peak:
+        peak = 6800.0
+    src = os.path.join(ROOT, "bit_affine_quantized_g128_gb300", "csrc", "q1_narrow.cu")
+    with open(src, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()
+    traffic = NCU_TRAFFIC["bytes"] if NCU_TRAFFIC["source_sha256"] == sha else None
+    per_launch_bytes = bytes_step / (LAYERS * len(SHAPES))
+    per_launch_s = secs / (args.steps * LAYERS * len(SHAPES))
+    achieved = per_launch_bytes / per_launch_s / 1e9
+    line = {
+        "metric": "Q1 QMV achieved HBM GB/s (% of 8 TB/s) at M=1..8; prefill QMM TFLOP/s",
+        "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t_max / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded uniform bits, |N(0,0.02)|+1e-4 fp16 scales, N(0,1) bf16 x)",
+        "config": {"workload": WORKLOAD, "layers": LAYERS, "M": 1, "metadata": "symmetric",
+                   "bytes_per_step": bytes_step,
+                   "l2": "inputs larger than L2 (2.64 GB of weights per step, no flush)",
+                   "parallelism": f"replicas x{world}"},
+        "pct_of_8TBps": round(100 * value / world / 8000.0, 1),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 3), "traffic": traffic,
+                     "peak_source": peak_src,
+                     "kernel": "narrow_kernel<1,false> (mma.sync bf16, cluster K-split)"},
+        "clocks": clocks,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "sub": sub,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def reference_arm(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import numpy as np
+    from bit_affine_quantized_g128_gb300 import synth
+    from oracle import q1_oracle as O
+    # each step: a bounded sample of the decode workload (256 rows of the gate
+    # matrix, M = 1), timed on the host cores; GB/s of the same algorithmic bytes
+    K = D_MODEL
+    t = synth.q1_tensor(256, K, seed=1001, affine=False)
+    x = synth.activations(1, K, seed=1006)
+    for _ in range(args.warmup):
+        O.qmm(x, t.words, t.scales, None, K)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        O.qmm(x, t.words, t.scales, None, K)
+    el = time.perf_counter() - t0
+    b = (weight_bytes(256, K, False) + K * 2 + 256 * 2) * args.steps
+    v = b / el / 1e9
+    cores = os.cpu_count()
+    line = {"metric": "Q1 QMV achieved HBM GB/s (% of 8 TB/s) at M=1..8; prefill QMM TFLOP/s",
+            "value": round(v, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": WORKLOAD, "M": 1, "metadata": "symmetric"},
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": "each step: oracle QMV on 256 rows of a 17408x5120 symmetric matrix"},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--quick", action="store_true", help="headline only (no sub-measurements)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-worker", type=float, default=None, help=argparse.SUPPRESS)
+    args = ap.parse_args()
+    if args.cpu_worker is not None:
+        cpu_worker(args.cpu_worker)
+        return
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

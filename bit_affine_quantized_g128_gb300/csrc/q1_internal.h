@@ -1,0 +1,52 @@
+// Internal declarations shared by the library's translation units (host side).
+// Not part of the public ABI (include/q1.h is).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "q1.h"
+
+namespace q1 {
+
+constexpr int kGroup = 128;      // weights per scale/bias group
+constexpr int kWordBits = 32;    // weights per packed word
+constexpr int kNarrowMaxM = 8;   // token rows of one mma.sync n8 tile
+
+// Metadata pointers resolved for a launch.
+struct WeightView {
+  const uint32_t *w;
+  const uint16_t *s;
+  const uint16_t *b;  // nullptr: symmetric
+  int64_t N, K;
+};
+
+inline WeightView view(const q1_weight *W) {
+  return WeightView{W->w, W->scales, W->biases, W->N, W->K};
+}
+
+// ---- elementwise kernels (q1_elementwise.cu)
+cudaError_t launch_pack(const uint8_t *bits, int64_t N, int64_t K, uint32_t *w, cudaStream_t st);
+cudaError_t launch_unpack(const uint32_t *w, int64_t N, int64_t K, uint8_t *bits,
+                          cudaStream_t st);
+cudaError_t launch_dequantize(const WeightView &W, q1_dtype t, void *out, cudaStream_t st);
+cudaError_t launch_gather(const WeightView &E, const int32_t *ids, int64_t T, q1_dtype t,
+                          void *out, int32_t *bad, cudaStream_t st);
+cudaError_t launch_check_symmetric(const WeightView &W, int32_t *result, cudaStream_t st);
+
+// ---- narrow path (q1_narrow.cu): one launch, no scratch
+// y [M][N] bf16 = x . W^T (x [M][K] bf16).
+cudaError_t launch_narrow(const WeightView &W, const void *x, int64_t M, void *y,
+                          cudaStream_t st, bool pdl);
+// h [M][F] bf16 = SiLU(x . G^T) * (x . U^T).
+cudaError_t launch_narrow_gate_up(const WeightView &G, const WeightView &U, const void *x,
+                                  int64_t M, void *h, cudaStream_t st, bool pdl);
+
+// ---- wide path (q1_wide.cu)
+cudaError_t launch_wide(const WeightView &W, const void *x, int64_t M, void *y,
+                        cudaStream_t st);
+
+// ---- device error words (each translation unit with bounded waits owns one)
+unsigned int read_and_clear_wide_errors(cudaStream_t st, cudaError_t *err);
+
+}  // namespace q1

@@ -1,0 +1,440 @@
+// Wide (prefill) Q1 matmul on the tcgen05 tensor cores:
+//   y[M][N] = x[M][K] . bf16(Wd)^T, fp32 accumulation in tensor memory.
+//
+// The page "Support Bonsai-27B affine Q1" (higgs PR #212), section
+// "Limitations / non-goals", runs forwards wider than the narrow threshold by
+// dequantizing the whole matrix to the input dtype and calling a dense matmul,
+// which is what set its peak memory ("Measured impact": peak about 6.65 GB
+// from dense prefill temporaries).  Here the dequantization happens per tile
+// in shared memory, feeding the MMA directly: no dense temporary exists.
+// Each weight is rounded to bf16 exactly as q1_dequantize rounds it, so the
+// product equals x . q1_dequantize(W, bf16)^T up to fp32 accumulation order.
+//
+// One CTA computes a 128-token x 256-row output tile (one SM; 192 KB of shared
+// memory keeps it alone on the SM, so its 256-column TMEM allocation cannot
+// contend):
+//   warp 0        TMA producer: x tiles [128 tokens x 64 k] bf16, 128B swizzle
+//   warp 1        TMEM allocator and the single MMA-issuing thread
+//                 (tcgen05.mma.cta_group::1.kind::f16, M=128 N=256 K=16)
+//   warps 2..9    dequantizers: each thread owns one weight row, reads the
+//                 packed words of one group (uint4) and the group's
+//                 scale/bias, and writes 64 bf16 per k-step into the
+//                 128B-swizzled K-major layout the MMA reads; then the
+//                 epilogue: TMEM -> registers -> bf16 -> global.
+// Stages: 4 x (16 KB x tile + 32 KB weight tile), mbarrier hand-offs.
+// Every wait is bounded (globaltimer); one that runs out sets a device error
+// word and a CTA-wide abort flag so that the other roles stop waiting too.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "q1_internal.h"
+
+namespace q1 {
+
+__device__ unsigned int g_wide_err = 0;
+
+namespace {
+
+constexpr int BM = 128;  // tokens per tile (TMEM lanes)
+constexpr int BN = 256;  // weight rows per tile (MMA N)
+constexpr int BK = 64;   // k per stage (one 128-byte swizzle atom of bf16)
+constexpr int STAGES = 4;
+constexpr int kThreadsWide = 320;  // 10 warps
+constexpr int kDeqWarp0 = 2;
+constexpr int kDeqThreads = 256;
+constexpr uint32_t A_BYTES = BM * BK * 2;  // 16 KB
+constexpr uint32_t B_BYTES = BN * BK * 2;  // 32 KB
+constexpr uint32_t kTmemCols = 256;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+
+struct __align__(8) WideShared {
+  uint64_t full_a[STAGES];
+  uint64_t full_b[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t accum_full;
+  uint32_t tmem_base;
+  volatile int abort_flag;
+};
+
+constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + STAGES * (A_BYTES + B_BYTES) + sizeof(WideShared);
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait on the phase with the given parity.  Returns false when the
+// wait ran out or another role of this CTA already aborted.
+__device__ __noinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, WideShared *sh) {
+  const uint32_t addr = smem_u32(bar);
+  if (mbar_try(addr, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try(addr, parity)) return true;
+    if ((i & 15u) == 15u) {
+      if (sh->abort_flag) return false;
+      if (globaltimer() - t0 > kWaitLimitNs) {
+        sh->abort_flag = 1;
+        atomicOr(&g_wide_err, 1u);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar, int c0,
+                                            int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(smem_u32(dst)), "l"(map), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, 8-row groups 1024 bytes apart (stride byte offset), fixed
+// descriptor version 1 at bits 46..48, swizzle mode 2 (128B) at bits 61..63.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)1 << 16;             // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;   // stride byte offset
+  d |= (uint64_t)1 << 46;             // version
+  d |= (uint64_t)2 << 61;             // SWIZZLE_128B
+  return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, N >> 3 at bits 17..22, M >> 4 at bits 24..28.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                            ((uint32_t)(BM >> 4) << 24);
+
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// 32 weights of one word -> 16 bf16x2 in k order: out[j] = (k = 2j, 2j+1).
+// A prmt with the sign-replicate selector turns bit 7 of a source byte into a
+// 0x00/0xFF byte, so two shifted copies of the word give 16-bit masks for two
+// adjacent weights at once; one LOP3 then selects hi (bit 1) or lo (bit 0).
+__device__ __forceinline__ void expand_word(uint32_t w, uint32_t lo2, uint32_t hi2, uint32_t (&out)[16]) {
+#pragma unroll
+  for (int e = 0; e < 8; e += 2) {
+    const uint32_t A = w << (7 - e);  // byte i msb = bit 8i+e
+    const uint32_t B = w << (6 - e);  // byte i msb = bit 8i+e+1
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t s = (8u | i) | ((8u | i) << 4) | ((8u | (4 + i)) << 8) | ((8u | (4 + i)) << 12);
+      const uint32_t m = prmt(A, B, s);
+      out[4 * i + e / 2] = (m & hi2) | (~m & lo2);
+    }
+  }
+}
+
+struct GroupData {
+  uint4 w;
+  uint16_t s, b;
+};
+
+__global__ void __launch_bounds__(kThreadsWide, 1)
+wide_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint32_t *__restrict__ W,
+            const uint16_t *__restrict__ S, const uint16_t *__restrict__ Bv, int M, int N, int K,
+            __nv_bfloat16 *__restrict__ y) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char *base = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  unsigned char *sa = base;                        // STAGES x A_BYTES
+  unsigned char *sb = base + STAGES * A_BYTES;     // STAGES x B_BYTES
+  WideShared *sh = reinterpret_cast<WideShared *>(sb + STAGES * B_BYTES);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
+  const int KSTEPS = K / BK;
+
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&sh->full_a[s], 1);
+      mbar_init(&sh->full_b[s], kDeqThreads / 32);
+      mbar_init(&sh->empty[s], 1);
+    }
+    mbar_init(&sh->accum_full, 1);
+    sh->abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_x) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&sh->tmem_base)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem_d = sh->tmem_base;
+
+  if (warp == 0) {
+    // ---------------- TMA producer (x tiles)
+    if (lane == 0) {
+      for (int ks = 0; ks < KSTEPS; ++ks) {
+        const int s = ks % STAGES;
+        const uint32_t ph = (uint32_t)(ks / STAGES) & 1u;
+        if (!mbar_wait(&sh->empty[s], ph ^ 1u, sh)) break;
+        mbar_arrive_expect_tx(&sh->full_a[s], A_BYTES);
+        tma_load_2d(sa + s * A_BYTES, &tmap_x, &sh->full_a[s], ks * BK, m0);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer
+    if (lane == 0) {
+      bool ok = true;
+      for (int ks = 0; ks < KSTEPS && ok; ++ks) {
+        const int s = ks % STAGES;
+        const uint32_t ph = (uint32_t)(ks / STAGES) & 1u;
+        ok = mbar_wait(&sh->full_a[s], ph, sh) && mbar_wait(&sh->full_b[s], ph, sh);
+        if (!ok) break;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t a_addr = smem_u32(sa + s * A_BYTES), b_addr = smem_u32(sb + s * B_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          umma_bf16(tmem_d, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32),
+                    (ks > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(&sh->empty[s]);
+      }
+      umma_commit(&sh->accum_full);  // arrives once every issued MMA has completed
+    }
+  } else {
+    // ---------------- dequantizers: thread d owns weight row n0 + d
+    const int d = tid - kDeqWarp0 * 32;
+    const int n = n0 + d;
+    const bool ok_row = n < N;
+    const int wpr = K / 32, G = K / 128;
+    const uint4 *wrow = reinterpret_cast<const uint4 *>(W + (size_t)(ok_row ? n : 0) * wpr);
+    const uint16_t *srow = S + (size_t)(ok_row ? n : 0) * G;
+    const uint16_t *brow = Bv ? Bv + (size_t)(ok_row ? n : 0) * G : nullptr;
+    auto load = [&](int g, GroupData &gd) {
+      if (g < G && ok_row) {
+        gd.w = __ldg(wrow + g);
+        gd.s = srow[g];
+        gd.b = brow ? brow[g] : (uint16_t)0;
+      } else {
+        gd.w = make_uint4(0, 0, 0, 0);
+        gd.s = 0;
+        gd.b = 0;
+      }
+    };
+    bool alive = true;
+    auto process = [&](int g, const GroupData &gd) {
+      const float sc = __half2float(__ushort_as_half(gd.s));
+      const float bi = brow ? __half2float(__ushort_as_half(gd.b)) : __fmul_rn(-0.5f, sc);
+      const uint32_t lo16 = __bfloat16_as_ushort(__float2bfloat16_rn(bi));
+      const uint32_t hi16 = __bfloat16_as_ushort(__float2bfloat16_rn(__fadd_rn(sc, bi)));
+      const uint32_t lo2 = lo16 | (lo16 << 16), hi2 = hi16 | (hi16 << 16);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int ks = 2 * g + h;
+        const int s = ks % STAGES;
+        const uint32_t ph = (uint32_t)(ks / STAGES) & 1u;
+        // one lane waits, the warp follows its verdict (keeps the warp converged)
+        int okw = 0;
+        if (lane == 0) okw = alive && mbar_wait(&sh->empty[s], ph ^ 1u, sh);
+        okw = __shfl_sync(0xffffffffu, okw, 0);
+        if (!okw) {
+          alive = false;
+          return;
+        }
+        unsigned char *rowp = sb + s * B_BYTES + d * 128;
+#pragma unroll
+        for (int wi = 0; wi < 2; ++wi) {
+          const uint32_t word = h == 0 ? (wi == 0 ? gd.w.x : gd.w.y) : (wi == 0 ? gd.w.z : gd.w.w);
+          uint32_t out[16];
+          expand_word(word, lo2, hi2, out);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int c = wi * 4 + q;  // 16-byte chunk: k = 8c .. 8c+7 of this stage
+            *reinterpret_cast<uint4 *>(rowp + ((c ^ (d & 7)) << 4)) =
+                make_uint4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
+          }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->full_b[s]);
+      }
+    };
+    GroupData r0, r1, r2;
+    load(0, r0);
+    load(1, r1);
+    for (int g = 0; g < G && alive; g += 3) {
+      load(g + 2, r2);
+      process(g, r0);
+      if (g + 1 >= G || !alive) break;
+      load(g + 3, r0);
+      process(g + 1, r1);
+      if (g + 2 >= G || !alive) break;
+      load(g + 4, r1);
+      process(g + 2, r2);
+    }
+
+    // ---------------- epilogue: warp w reads TMEM lanes 32*(w%4).., columns half (w-2)/4
+    int acc_ok = 0;
+    if (lane == 0) acc_ok = mbar_wait(&sh->accum_full, 0u, sh) && !sh->abort_flag;
+    acc_ok = __shfl_sync(0xffffffffu, acc_ok, 0);
+    if (acc_ok) {
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const int quarter = warp & 3, half = (warp - kDeqWarp0) >> 2;
+      const int m = m0 + 32 * quarter + lane;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        const int col = half * 128 + cc * 32;
+        uint32_t v[32];
+        const uint32_t taddr = tmem_d + ((uint32_t)(32 * quarter) << 16) + (uint32_t)col;
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+            "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+            "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+            : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+              "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
+              "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]),
+              "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+              "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
+              "=r"(v[31])
+            : "r"(taddr)
+            : "memory");
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        if (m < M) {
+          const int n = n0 + col;
+          __nv_bfloat16 *dst = y + (size_t)m * N + n;
+          // 16-byte stores need 16-byte aligned rows: N % 8 == 0
+          if (n + 32 <= N && (N & 7) == 0) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t p[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                __nv_bfloat162 t2 = __floats2bfloat162_rn(__uint_as_float(v[8 * q + 2 * e]),
+                                                          __uint_as_float(v[8 * q + 2 * e + 1]));
+                p[e] = *reinterpret_cast<uint32_t *>(&t2);
+              }
+              reinterpret_cast<uint4 *>(dst)[q] = make_uint4(p[0], p[1], p[2], p[3]);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (n + e < N) dst[e] = __float2bfloat16_rn(__uint_as_float(v[e]));
+          }
+        }
+      }
+    }
+  }
+
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (warp == 1) {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_d), "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void *p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+}  // namespace
+
+cudaError_t launch_wide(const WeightView &W, const void *x, int64_t M, void *y,
+                        cudaStream_t st) {
+  auto encode = get_encode();
+  if (!encode) return cudaErrorNotSupported;
+  CUtensorMap map;
+  cuuint64_t gdim[2] = {(cuuint64_t)W.K, (cuuint64_t)M};
+  cuuint64_t gstride[1] = {(cuuint64_t)W.K * 2};
+  cuuint32_t box[2] = {BK, BM};
+  cuuint32_t estride[2] = {1, 1};
+  CUresult r = encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(x), gdim, gstride,
+                      box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  dim3 grid((unsigned)((W.N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM), 1);
+  wide_kernel<<<grid, kThreadsWide, kSmemBytes, st>>>(map, W.w, W.s, W.b, (int)M, (int)W.N, (int)W.K,
+                                                      static_cast<__nv_bfloat16 *>(y));
+  return cudaGetLastError();
+}
+
+unsigned int read_and_clear_wide_errors(cudaStream_t st, cudaError_t *err) {
+  unsigned int v = 0, zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_wide_err, sizeof(v), 0, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess && v)
+    e = cudaMemcpyToSymbolAsync(g_wide_err, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (err) *err = e;
+  return v;
+}
+
+}  // namespace q1

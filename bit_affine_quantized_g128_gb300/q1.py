@@ -1,0 +1,239 @@
+"""Thin Python binding of libq1 (include/q1.h) over ctypes.
+
+Argument marshalling only: every step of every call runs in the library's CUDA
+kernels.  torch tensors supply device memory and the current CUDA stream.
+There is no fallback: if the library is missing or the device is not a
+Blackwell GPU, the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libq1.so")
+
+Q1_BF16, Q1_F16, Q1_F32 = 0, 1, 2
+_DT = {torch.bfloat16: Q1_BF16, torch.float16: Q1_F16, torch.float32: Q1_F32}
+
+# every symbol include/q1.h declares
+EXPORTED = [
+    "q1_pack", "q1_unpack", "q1_dequantize", "q1_qmv",
+    "q1_qmm_narrow", "q1_qmm", "q1_set_qmm_max_rows", "q1_get_qmm_max_rows",
+    "q1_embed_gather", "q1_ffn_workspace_size", "q1_ffn_fused", "q1_check_symmetric",
+    "q1_device_errors", "q1_status_string",
+]
+
+
+class Q1Error(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn}: {msg} (status {status})")
+        self.status = status
+
+
+class _CWeight(ctypes.Structure):
+    _fields_ = [("w", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("biases", ctypes.c_void_p),
+                ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("group_size", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libq1.so (after torch, so that both share one CUDA runtime)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libq1.so not built ({path}); run __graft_entry__.build() or "
+                           "python -m bit_affine_quantized_g128_gb300.build")
+    lib = ctypes.CDLL(path)
+    P, I64, I32, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
+    W = ctypes.POINTER(_CWeight)
+    sig = {
+        "q1_pack": ([P, I64, I64, P, P], I32),
+        "q1_unpack": ([P, I64, I64, P, P], I32),
+        "q1_dequantize": ([W, I32, P, P], I32),
+        "q1_qmv": ([W, P, I32, P, P], I32),
+        "q1_qmm_narrow": ([W, P, I64, I32, P, P], I32),
+        "q1_qmm": ([W, P, I64, I32, P, P], I32),
+        "q1_set_qmm_max_rows": ([ctypes.c_int], None),
+        "q1_get_qmm_max_rows": ([], ctypes.c_int),
+        "q1_embed_gather": ([W, P, I64, I32, P, P, P], I32),
+        "q1_ffn_workspace_size": ([I64, I64, I64], SZ),
+        "q1_ffn_fused": ([W, W, W, P, I64, I32, P, P, SZ, P], I32),
+        "q1_check_symmetric": ([W, P, P], I32),
+        "q1_device_errors": ([ctypes.POINTER(ctypes.c_uint), P], I32),
+        "q1_status_string": ([I32], ctypes.c_char_p),
+    }
+    for name, (args, res) in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = res
+    _lib = lib
+    return lib
+
+
+def lib() -> ctypes.CDLL:
+    return load_library()
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise Q1Error(fn, status, lib().q1_status_string(status).decode())
+
+
+def _stream() -> int:
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+class Q1Weight:
+    """A packed Q1 weight on the GPU: words uint32 [N, K/32] (held as int32),
+    fp16 scales [N, K/128] and fp16 biases [N, K/128] or None (symmetric)."""
+
+    def __init__(self, words: torch.Tensor, scales: torch.Tensor,
+                 biases: Optional[torch.Tensor], K: int):
+        self.words = words.contiguous()
+        self.scales = scales.contiguous()
+        self.biases = None if biases is None else biases.contiguous()
+        self.N = int(words.shape[0])
+        self.K = int(K)
+        self._c = _CWeight(self.words.data_ptr(), self.scales.data_ptr(),
+                           _ptr(self.biases), self.N, self.K, 128)
+
+    @property
+    def symmetric(self) -> bool:
+        return self.biases is None
+
+    @staticmethod
+    def from_host(t, device="cuda") -> "Q1Weight":
+        """From a host bundle with numpy words/scales/biases (synth.Q1Tensor)."""
+        w = torch.from_numpy(t.words.view("<i4").copy()).to(device)
+        s = torch.from_numpy(t.scales.copy()).to(device)
+        b = None if t.biases is None else torch.from_numpy(t.biases.copy()).to(device)
+        return Q1Weight(w, s, b, t.K)
+
+    def cref(self):
+        return ctypes.byref(self._c)
+
+
+def _flat(x: torch.Tensor, K: int) -> torch.Tensor:
+    if x.shape[-1] != K:
+        raise ValueError(f"last dim {x.shape[-1]} != K {K}")
+    return x.reshape(-1, K).contiguous()
+
+
+def pack(bits: torch.Tensor) -> torch.Tensor:
+    """bits uint8 [N, K] -> words int32 [N, K/32] (LSB first)."""
+    bits = bits.contiguous()
+    N, K = bits.shape
+    w = torch.empty((N, K // 32), dtype=torch.int32, device=bits.device)
+    _check("q1_pack", lib().q1_pack(bits.data_ptr(), N, K, w.data_ptr(), _stream()))
+    return w
+
+
+def unpack(words: torch.Tensor, K: int) -> torch.Tensor:
+    words = words.contiguous()
+    N = words.shape[0]
+    out = torch.empty((N, K), dtype=torch.uint8, device=words.device)
+    _check("q1_unpack", lib().q1_unpack(words.data_ptr(), N, K, out.data_ptr(), _stream()))
+    return out
+
+
+def dequantize(W: Q1Weight, dtype=torch.bfloat16) -> torch.Tensor:
+    out = torch.empty((W.N, W.K), dtype=dtype, device=W.words.device)
+    _check("q1_dequantize", lib().q1_dequantize(W.cref(), _DT[dtype], out.data_ptr(), _stream()))
+    return out
+
+
+def qmv(W: Q1Weight, x: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """x [K] -> y [N] (M = 1 decode)."""
+    x = x.reshape(W.K).contiguous()
+    y = out if out is not None else torch.empty((W.N,), dtype=x.dtype, device=x.device)
+    _check("q1_qmv", lib().q1_qmv(W.cref(), x.data_ptr(), _DT[x.dtype], y.data_ptr(), _stream()))
+    return y
+
+
+def _qmm_call(fn: str, W: Q1Weight, x: torch.Tensor, out):
+    lead = x.shape[:-1]
+    x2 = _flat(x, W.K)
+    M = x2.shape[0]
+    y = out if out is not None else torch.empty((M, W.N), dtype=x.dtype, device=x.device)
+    _check(fn, getattr(lib(), fn)(W.cref(), x2.data_ptr(), M, _DT[x.dtype], y.data_ptr(),
+                                  _stream()))
+    return y.reshape(*lead, W.N)
+
+
+def qmm_narrow(W: Q1Weight, x: torch.Tensor, out=None) -> torch.Tensor:
+    """x [..., K] with prod(leading dims) <= 8 -> y [..., N]; weights stay packed."""
+    return _qmm_call("q1_qmm_narrow", W, x, out)
+
+
+def qmm(W: Q1Weight, x: torch.Tensor, out=None) -> torch.Tensor:
+    """x [..., K] -> y [..., N]; narrow path up to the row threshold, tcgen05 beyond."""
+    return _qmm_call("q1_qmm", W, x, out)
+
+
+def set_qmm_max_rows(rows: int):
+    lib().q1_set_qmm_max_rows(int(rows))
+
+
+def get_qmm_max_rows() -> int:
+    return int(lib().q1_get_qmm_max_rows())
+
+
+def embed_gather(E: Q1Weight, ids: torch.Tensor, dtype=torch.bfloat16):
+    """ids int32 [T] (device) -> (rows [T, K], out-of-range count int32 [1] on device)."""
+    ids = ids.to(torch.int32).contiguous()
+    T = ids.numel()
+    out = torch.empty((T, E.K), dtype=dtype, device=E.words.device)
+    bad = torch.zeros((1,), dtype=torch.int32, device=E.words.device)
+    _check("q1_embed_gather", lib().q1_embed_gather(E.cref(), ids.data_ptr(), T, _DT[dtype],
+                                                    out.data_ptr(), bad.data_ptr(), _stream()))
+    return out, bad
+
+
+def ffn_workspace(M: int, D: int, F: int, device) -> torch.Tensor:
+    n = lib().q1_ffn_workspace_size(M, D, F)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def ffn_fused(gate: Q1Weight, up: Q1Weight, down: Q1Weight, x: torch.Tensor,
+              workspace=None, out=None) -> torch.Tensor:
+    lead = x.shape[:-1]
+    x2 = _flat(x, gate.K)
+    M = x2.shape[0]
+    y = out if out is not None else torch.empty((M, down.N), dtype=x.dtype, device=x.device)
+    ws = workspace if workspace is not None else ffn_workspace(M, gate.K, gate.N, x.device)
+    _check("q1_ffn_fused", lib().q1_ffn_fused(gate.cref(), up.cref(), down.cref(), x2.data_ptr(), M,
+                                              _DT[x.dtype], y.data_ptr(), ws.data_ptr(),
+                                              ws.numel(), _stream()))
+    return y.reshape(*lead, down.N)
+
+
+def ffn_h(ws: torch.Tensor, M: int, F: int) -> torch.Tensor:
+    """The bf16 intermediate h [M, F] that the last q1_ffn_fused left in `ws`."""
+    return ws[: M * F * 2].view(torch.bfloat16).reshape(M, F)
+
+
+def check_symmetric(W: Q1Weight) -> torch.Tensor:
+    """Device int32 [1]: 1 iff every stored bias is exactly -scale/2."""
+    r = torch.empty((1,), dtype=torch.int32, device=W.words.device)
+    _check("q1_check_symmetric", lib().q1_check_symmetric(W.cref(), r.data_ptr(), _stream()))
+    return r
+
+
+def device_errors() -> int:
+    """Synchronizes the current stream; returns and clears the device error flags."""
+    v = ctypes.c_uint(0)
+    st = lib().q1_device_errors(ctypes.byref(v), _stream())
+    if st not in (0, 8):
+        _check("q1_device_errors", st)
+    return int(v.value)

@@ -1,0 +1,153 @@
+/*
+ * q1.h - C ABI of libq1: the 1-bit affine group-quantized (group size 128)
+ * linear layer on NVIDIA GB300 (sm_103a).
+ *
+ * Format ("1-bit affine weight support", rMLX issue #207, section "The good
+ * news - packing is standard"; "Bonsai masked gemv", cactus PR #775, "linear
+ * LSB layout"):
+ *   w       uint32 [N][K/32]  weight (n, k) is bit (k % 32) of word [n][k / 32]
+ *   scales  fp16   [N][K/128] one per row and group of 128 along K
+ *   biases  fp16   [N][K/128] or NULL
+ * Value ("Support Bonsai-27B affine Q1", higgs PR #212, section "What"):
+ *   w(n,k) = scale * q + bias, q in {0,1}.  With biases == NULL the tensor is
+ *   symmetric: bias = -scale/2, derived in fp32 and never stored.  So bit 0
+ *   gives the negative value and bit 1 the positive one.
+ *   The dequantized value is fp32: q = 0 -> bias, q = 1 -> fl32(scale + bias).
+ *
+ * Conventions for every call:
+ *   - Pointers named d_* or documented as "device" are device pointers
+ *     allocated by the caller (the library never allocates or frees device
+ *     memory).  Arrays are row-major and contiguous.
+ *   - Work is enqueued on `stream` (NULL = the legacy default stream) and the
+ *     call returns without waiting, unless stated otherwise.
+ *   - Arguments are validated on the host before anything is launched; an
+ *     invalid argument returns an error status and launches nothing.  A failed
+ *     launch returns Q1_ERR_CUDA.  No exception crosses the ABI.
+ *   - Activations/outputs of the matmul calls are bf16 (Q1_BF16); other dtypes
+ *     return Q1_ERR_DTYPE.
+ *   - The one call that needs scratch (q1_ffn_fused, for its intermediate
+ *     activations) takes a caller-owned device workspace and its size;
+ *     q1_ffn_workspace_size returns the bytes needed.  The workspace must be
+ *     256-byte aligned and must not be used by another call that may run
+ *     concurrently.
+ *   - Device-side waits in the kernels are bounded; one that runs out sets a
+ *     device error word that q1_device_errors() reads (Q1_ERR_TIMEOUT).
+ *   - The narrow matmul and FFN kernels are launched with programmatic
+ *     dependent launch: they may start streaming the packed weights and
+ *     metadata while the preceding kernel on the stream is still running, if
+ *     that kernel signalled programmatic completion early; they read x (and
+ *     write y) only after the preceding kernel has completed.  Weights must
+ *     therefore not be produced by a kernel that signals early.
+ */
+#ifndef Q1_H_
+#define Q1_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream. */
+typedef struct CUstream_st *q1_stream;
+
+typedef enum {
+  Q1_OK = 0,
+  Q1_ERR_NULL = 1,       /* a required pointer is NULL                          */
+  Q1_ERR_SHAPE = 2,      /* N < 1, K < 128, K % 128 != 0, M out of range, ...   */
+  Q1_ERR_ALIGN = 3,      /* a pointer is not aligned as documented              */
+  Q1_ERR_DTYPE = 4,      /* unsupported dtype for this call                     */
+  Q1_ERR_GROUP = 5,      /* group_size != 128                                   */
+  Q1_ERR_WORKSPACE = 6,  /* workspace missing, too small or misaligned          */
+  Q1_ERR_CUDA = 7,       /* a CUDA runtime call or launch failed                */
+  Q1_ERR_TIMEOUT = 8,    /* a bounded device-side wait ran out                  */
+  Q1_ERR_DEVICE = 9      /* current device is not a compute capability 10.x GPU */
+} q1_status;
+
+typedef enum { Q1_BF16 = 0, Q1_F16 = 1, Q1_F32 = 2 } q1_dtype;
+
+/* One packed Q1 weight.  All pointers are device pointers owned by the caller.
+ *   w: 16-byte aligned.  scales/biases: 2-byte aligned.
+ *   N >= 1, K >= 128, K % 128 == 0, group_size == 128. */
+typedef struct {
+  const uint32_t *w;
+  const uint16_t *scales;
+  const uint16_t *biases; /* NULL => symmetric metadata */
+  int64_t N;
+  int64_t K;
+  int32_t group_size;
+} q1_weight;
+
+/* ---- pack / unpack (rMLX issue #207, "packing is standard") ------------- */
+/* bits uint8 [N][K] (bit 0 of every byte is the weight; other bits ignored)
+ * -> w uint32 [N][K/32], LSB first.  K % 32 == 0.  Both 16-byte aligned. */
+q1_status q1_pack(const uint8_t *bits, int64_t N, int64_t K, uint32_t *w, q1_stream stream);
+/* w uint32 [N][K/32] -> bits uint8 [N][K] of 0/1 values.  Both 16-byte aligned. */
+q1_status q1_unpack(const uint32_t *w, int64_t N, int64_t K, uint8_t *bits, q1_stream stream);
+
+/* ---- dequantize (higgs PR #212, "What"; rMLX issue #207, the missing
+ * affine_dequantize kernel) ---------------------------------------------- */
+/* out [N][K] in out_t (bf16 / f16 / f32): the fp32 dequantized value rounded
+ * once to nearest-even.  out 16-byte aligned.  Bit-exact. */
+q1_status q1_dequantize(const q1_weight *W, q1_dtype out_t, void *out, q1_stream stream);
+
+/* ---- matmul: y[M][N] = x[M][K] . Wd^T ------------------------------------
+ * fp32 accumulation, bf16 in and out.  x and y 16-byte aligned.
+ * q1_qmv: the M = 1 decode product (higgs PR #212, "What": the Q1 decode tile).
+ * q1_qmm_narrow: 1 <= M <= 8 (speculative-verifier windows) with the weights
+ *   kept packed and no dense temporary (higgs PR #212, "What": narrow Q1
+ *   matrix multiplies of up to 8 flattened rows).  Leading dimensions are
+ *   flattened by the caller: x [B][T][K] is passed as M = B*T.
+ * q1_qmm: any M >= 1.  M <= q1_get_qmm_max_rows() runs the narrow path;
+ *   wider M runs the prefill path, which dequantizes tiles to bf16 in shared
+ *   memory and multiplies them on the tcgen05 tensor cores (no dense
+ *   temporary in global memory either). */
+q1_status q1_qmv(const q1_weight *W, const void *x, q1_dtype dtype, void *y, q1_stream stream);
+q1_status q1_qmm_narrow(const q1_weight *W, const void *x, int64_t M, q1_dtype dtype,
+                        void *y, q1_stream stream);
+q1_status q1_qmm(const q1_weight *W, const void *x, int64_t M, q1_dtype dtype, void *y,
+                 q1_stream stream);
+/* Narrow/wide threshold (higgs PR #212, "Limitations": HIGGS_BONSAI_QMM_MAX_ROWS,
+ * default 8).  Values are clamped to [0, 8].  The environment variable
+ * Q1_QMM_MAX_ROWS, if set, gives the initial value when the library loads. */
+void q1_set_qmm_max_rows(int rows);
+int q1_get_qmm_max_rows(void);
+
+/* ---- embedding gather (higgs PR #212, "What": Q1 embeddings) --------------
+ * out[t][:] = dequant(E row ids[t]) in out_t, bit-exact like q1_dequantize.
+ * ids: device int32 [T].  An id outside [0, E->N) gives a zero row and, when
+ * d_bad_count is not NULL, adds 1 to *d_bad_count (device int32).  T >= 0
+ * (T == 0 launches nothing).  out 16-byte aligned. */
+q1_status q1_embed_gather(const q1_weight *E, const int32_t *ids, int64_t T, q1_dtype out_t,
+                          void *out, int32_t *d_bad_count, q1_stream stream);
+
+/* ---- fused dense FFN (higgs PR #212, "What": fused dense-FFN operations) ---
+ * y[M][D] = Down . (SiLU(Gate . x) * (Up . x)) with SiLU(g) = g / (1 + e^-g).
+ * gate, up: [F][D]; down: [D][F].  1 <= M <= 8.  x [M][D], y [M][D] bf16.
+ * The intermediate h [M][F] is kept in bf16 at the start of the workspace
+ * (q1_ffn_workspace_size(M, D, F) bytes, 256-byte aligned); it is still
+ * there when the call's work completes. */
+size_t q1_ffn_workspace_size(int64_t M, int64_t D, int64_t F);
+q1_status q1_ffn_fused(const q1_weight *gate, const q1_weight *up, const q1_weight *down,
+                       const void *x, int64_t M, q1_dtype dtype, void *y, void *workspace,
+                       size_t workspace_bytes, q1_stream stream);
+
+/* ---- symmetric check (higgs PR #212, walkthrough: symmetric bias
+ * compaction and validation) -------------------------------------------------
+ * Writes 1 to *d_is_symmetric (device int32) iff every stored bias equals
+ * -scale/2 exactly in fp32 (+0 == -0; NaN never equal), else 0.
+ * W->biases must not be NULL. */
+q1_status q1_check_symmetric(const q1_weight *W, int32_t *d_is_symmetric, q1_stream stream);
+
+/* ---- diagnostics ------------------------------------------------------------ */
+/* Synchronizes `stream`, then reads and clears the device error words of the
+ * library's kernels.  *flags (may be NULL) receives their OR; returns
+ * Q1_ERR_TIMEOUT if any bounded wait ran out since the last call. */
+q1_status q1_device_errors(unsigned int *flags, q1_stream stream);
+const char *q1_status_string(q1_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* Q1_H_ */

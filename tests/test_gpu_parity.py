@@ -1,0 +1,250 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Bit-exact: pack, unpack, dequantize (bf16/f16/f32), embedding gather.
+Matmuls: the per-element and Frobenius bars of tests/tolerance.py.
+Inputs are the seeded synthetic workloads (bit_affine_quantized_g128_gb300/synth.py).
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import q1_oracle as O
+from bit_affine_quantized_g128_gb300 import synth
+from tests.tolerance import check_matmul
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def q1():
+    from bit_affine_quantized_g128_gb300 import q1 as mod
+    mod.load_library()
+    return mod
+
+
+def _u16(t):
+    return t.view(torch.int16).cpu().numpy().astype(np.uint16)
+
+
+# ------------------------------------------------------------------ pack / unpack
+@pytest.mark.parametrize("N,K", [(1, 32), (7, 96), (33, 1024), (1024, 1024)])
+def test_pack_unpack_bit_exact(q1, N, K):
+    bits = synth.bits(N, K, seed=1000 + N)
+    w = q1.pack(torch.from_numpy(bits).to(DEV))
+    want = O.pack(bits)
+    np.testing.assert_array_equal(w.cpu().numpy().view(np.uint32), want)
+    words = synth.weight_words(N, K, seed=2000 + N)
+    b = q1.unpack(torch.from_numpy(words.view(np.int32)).to(DEV), K)
+    np.testing.assert_array_equal(b.cpu().numpy(), O.unpack(words, K))
+    # round trip on the device
+    np.testing.assert_array_equal(q1.pack(b).cpu().numpy().view(np.uint32), words)
+
+
+def test_pack_ignores_high_bits_of_bytes(q1):
+    bits = synth.bits(4, 64, seed=3)
+    noisy = bits | (np.random.default_rng(4).integers(0, 128, bits.shape, dtype=np.uint8) << 1)
+    w = q1.pack(torch.from_numpy(noisy).to(DEV))
+    np.testing.assert_array_equal(w.cpu().numpy().view(np.uint32), O.pack(bits))
+
+
+# ------------------------------------------------------------------ dequantize
+@pytest.mark.parametrize("affine", [False, True])
+@pytest.mark.parametrize("dtype,name", [(torch.bfloat16, "bf16"), (torch.float16, "f16"),
+                                        (torch.float32, "f32")])
+@pytest.mark.parametrize("N,K", [(1024, 1024), (37, 384)])
+def test_dequantize_bit_exact(q1, affine, dtype, name, N, K):
+    t = synth.q1_tensor(N, K, seed=1000 + affine, affine=affine)
+    W = q1.Q1Weight.from_host(t)
+    got = q1.dequantize(W, dtype).cpu()
+    want = O.dequantize(t.words, t.scales, t.biases, K, name)
+    if dtype == torch.float32:
+        np.testing.assert_array_equal(got.view(torch.int32).numpy(), want.view(torch.int32).numpy())
+    else:
+        np.testing.assert_array_equal(_u16(got), _u16(want))
+
+
+def test_dequantize_edge_values(q1):
+    # tiny, zero and negative-zero metadata (the golden dequant fixture's cases)
+    K = 128
+    s = np.array([[0x0001], [0x3C01], [0x3555], [0x3555], [0x0000]], dtype=np.uint16).view(np.float16)
+    b = np.array([[0x8000], [0x0001], [0x0000], [0x8000], [0x8000]], dtype=np.uint16).view(np.float16)
+    words = np.tile(np.array([0x0000FFFF, 0xFFFF0000, 0x12345678, 0x80000001], dtype=np.uint32), (5, 1))
+    for bias in (None, b):
+        t = synth.Q1Tensor(words, s, bias, K)
+        W = q1.Q1Weight.from_host(t)
+        for dt, name in ((torch.bfloat16, "bf16"), (torch.float16, "f16")):
+            np.testing.assert_array_equal(_u16(q1.dequantize(W, dt).cpu()),
+                                          _u16(O.dequantize(words, s, bias, K, name)))
+        np.testing.assert_array_equal(q1.dequantize(W, torch.float32).cpu().view(torch.int32).numpy(),
+                                      O.dequantize(words, s, bias, K, "f32").view(torch.int32).numpy())
+
+
+# ------------------------------------------------------------------ narrow matmul
+def _case(N, K, M, affine, seed):
+    t = synth.q1_tensor(N, K, seed=seed, affine=affine)
+    x = synth.activations(M, K, seed=seed + 5)
+    return t, x
+
+
+@pytest.mark.parametrize("affine", [False, True])
+@pytest.mark.parametrize("M", list(range(1, 9)))
+def test_qmm_narrow_tiny(q1, affine, M):
+    # 1024 x 1024 (the tiny oracle check), every window size 1..8
+    t, x = _case(1024, 1024, M, affine, seed=1000 + affine)
+    W = q1.Q1Weight.from_host(t)
+    y = q1.qmm_narrow(W, x.to(DEV))
+    check_matmul(y, O.qmm(x, t.words, t.scales, t.biases, 1024), x,
+                 O.dequantize_f32(t.words, t.scales, t.biases, 1024), f"narrow M={M}")
+
+
+@pytest.mark.parametrize("N,K", [(1, 128), (17, 384), (130, 2176), (1000, 640), (333, 17408 // 4)])
+@pytest.mark.parametrize("affine", [False, True])
+def test_qmm_narrow_ragged(q1, N, K, affine):
+    for M in (1, 3, 8):
+        t, x = _case(N, K, M, affine, seed=N + K + M)
+        W = q1.Q1Weight.from_host(t)
+        y = q1.qmm_narrow(W, x.to(DEV))
+        check_matmul(y, O.qmm(x, t.words, t.scales, t.biases, K), x,
+                     O.dequantize_f32(t.words, t.scales, t.biases, K), f"narrow N={N} K={K} M={M}")
+
+
+def test_qmv_and_leading_dims(q1):
+    K = N = 1024
+    t, x = _case(N, K, 8, True, seed=1001)
+    W = q1.Q1Weight.from_host(t)
+    yo = O.qmm(x, t.words, t.scales, t.biases, K)
+    wd = O.dequantize_f32(t.words, t.scales, t.biases, K)
+    y1 = q1.qmv(W, x[0].to(DEV))
+    check_matmul(y1[None], yo[:1], x[:1], wd, "qmv")
+    # [2, 4, K] leading dimensions flatten to M = 8
+    y3 = q1.qmm(W, x.reshape(2, 4, K).to(DEV))
+    assert y3.shape == (2, 4, N)
+    check_matmul(y3.reshape(8, N), yo, x, wd, "[2,4,K]")
+
+
+def test_narrow_deterministic(q1):
+    t, x = _case(2048, 5120, 4, False, seed=7)
+    W = q1.Q1Weight.from_host(t)
+    xd = x.to(DEV)
+    a = q1.qmm_narrow(W, xd)
+    b = q1.qmm_narrow(W, xd)
+    assert torch.equal(a, b)
+
+
+def test_symmetric_complement_negates_on_gpu(q1):
+    K, N = 1024, 256
+    t, x = _case(N, K, 2, False, seed=11)
+    W = q1.Q1Weight.from_host(t)
+    Wc = q1.Q1Weight.from_host(synth.Q1Tensor(~t.words, t.scales, None, K))
+    y = q1.qmm_narrow(W, x.to(DEV)).float()
+    yc = q1.qmm_narrow(Wc, x.to(DEV)).float()
+    # negation holds in exact arithmetic; allow the bar's rounding on both
+    wd = O.dequantize_f32(t.words, t.scales, None, K)
+    check_matmul(-yc, O.qmm(x, t.words, t.scales, None, K), x, wd, "complement")
+    assert torch.allclose(y, -yc, rtol=0, atol=float(np.abs(wd).max()) * 2)
+
+
+# ------------------------------------------------------------------ dispatch / wide
+@pytest.mark.parametrize("affine", [False, True])
+@pytest.mark.parametrize("M,N,K", [(9, 512, 1024), (128, 256, 1024), (130, 300, 640),
+                                   (256, 1024, 1024), (200, 256, 128)])
+def test_qmm_wide(q1, affine, M, N, K):
+    t, x = _case(N, K, M, affine, seed=M + N + K + affine)
+    W = q1.Q1Weight.from_host(t)
+    y = q1.qmm(W, x.to(DEV))
+    check_matmul(y, O.qmm(x, t.words, t.scales, t.biases, K), x,
+                 O.dequantize_f32(t.words, t.scales, t.biases, K), f"wide M={M} N={N} K={K}")
+
+
+def test_wide_equals_dense_bf16_product(q1):
+    # the prefill path multiplies exactly the bf16 weights q1_dequantize returns
+    M, N, K = 256, 512, 2048
+    t, x = _case(N, K, M, True, seed=99)
+    W = q1.Q1Weight.from_host(t)
+    xd = x.to(DEV)
+    y = q1.qmm(W, xd).float()
+    ref = (xd.float() @ q1.dequantize(W, torch.bfloat16).float().T)
+    assert torch.allclose(y, ref, rtol=1e-2, atol=1e-2 * float(ref.abs().mean()))
+
+
+def test_threshold_dispatch(q1):
+    K, N = 1024, 512
+    t, x = _case(N, K, 9, False, seed=5)
+    W = q1.Q1Weight.from_host(t)
+    yo = O.qmm(x, t.words, t.scales, None, K)
+    wd = O.dequantize_f32(t.words, t.scales, None, K)
+    old = q1.get_qmm_max_rows()
+    try:
+        for rows in (0, 4, 8):
+            q1.set_qmm_max_rows(rows)
+            for M in (1, 4, 5, 8, 9):
+                y = q1.qmm(W, x[:M].to(DEV))
+                check_matmul(y, yo[:M], x[:M], wd, f"threshold={rows} M={M}")
+    finally:
+        q1.set_qmm_max_rows(old)
+    with pytest.raises(q1.Q1Error):
+        q1.qmm_narrow(W, x.to(DEV))  # M = 9 is not narrow
+
+
+# ------------------------------------------------------------------ gather / head
+@pytest.mark.parametrize("affine", [False, True])
+def test_embed_gather_bit_exact(q1, affine):
+    V, K = 3000, 640
+    t = synth.q1_tensor(V, K, seed=1003 + affine, affine=affine)
+    E = q1.Q1Weight.from_host(t)
+    ids = synth.token_ids(64, V, seed=1003)
+    ids[5], ids[9] = -1, V  # out of range -> zero rows, counted
+    for dt, name in ((torch.bfloat16, "bf16"), (torch.float32, "f32"), (torch.float16, "f16")):
+        out, bad = q1.embed_gather(E, torch.from_numpy(ids).to(DEV), dt)
+        want, nbad = O.embed_gather(ids, t.words, t.scales, t.biases, K, name)
+        assert int(bad.item()) == nbad == 2
+        g, w_ = out.cpu(), want
+        if dt == torch.float32:
+            np.testing.assert_array_equal(g.view(torch.int32).numpy(), w_.view(torch.int32).numpy())
+        else:
+            np.testing.assert_array_equal(_u16(g), _u16(w_))
+
+
+def test_embed_gather_empty(q1):
+    t = synth.q1_tensor(10, 128, seed=1, affine=False)
+    E = q1.Q1Weight.from_host(t)
+    out, bad = q1.embed_gather(E, torch.zeros(0, dtype=torch.int32, device=DEV))
+    assert out.shape == (0, 128) and int(bad.item()) == 0
+
+
+# ------------------------------------------------------------------ fused FFN
+@pytest.mark.parametrize("M", [1, 4, 8])
+def test_ffn_fused(q1, M):
+    D, F = 512, 1408
+    gate = synth.q1_tensor(F, D, seed=301, affine=False)
+    up = synth.q1_tensor(F, D, seed=302, affine=(M == 4))  # mixed metadata once
+    down = synth.q1_tensor(D, F, seed=303, affine=False)
+    x = synth.activations(M, D, seed=304)
+    G, U, Dn = (q1.Q1Weight.from_host(w) for w in (gate, up, down))
+    ws = q1.ffn_workspace(M, D, F, DEV)
+    y = q1.ffn_fused(G, U, Dn, x.to(DEV), workspace=ws)
+    yo, ho = O.ffn(x, (gate.words, gate.scales, None, D), (up.words, up.scales, up.biases, D),
+                   (down.words, down.scales, None, F))
+    # h against the oracle's fp64 h (bf16-rounded on the GPU)
+    h = q1.ffn_h(ws, M, F).float().cpu().double().numpy()
+    assert np.linalg.norm(h - ho) / np.linalg.norm(ho) < 5e-3
+    check_matmul(y, yo, ho, O.dequantize_f32(down.words, down.scales, None, F), f"ffn M={M}")
+
+
+# ------------------------------------------------------------------ symmetric check
+def test_check_symmetric(q1):
+    t = synth.q1_tensor(64, 256, seed=9, affine=False)
+    s = np.maximum(t.scales, np.float16(2.0 ** -13))
+    b = (-(s.astype(np.float32) / 2)).astype(np.float16)
+    W = q1.Q1Weight.from_host(synth.Q1Tensor(t.words, s, b, 256))
+    assert int(q1.check_symmetric(W).item()) == 1 == int(O.is_symmetric(s, b))
+    b2 = b.copy()
+    b2[63, 1] = np.float16(0.25)
+    W2 = q1.Q1Weight.from_host(synth.Q1Tensor(t.words, s, b2, 256))
+    assert int(q1.check_symmetric(W2).item()) == 0 == int(O.is_symmetric(s, b2))
+
+
+def test_no_device_errors_after_suite(q1):
+    assert q1.device_errors() == 0
