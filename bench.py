@@ -236,14 +236,15 @@ def time_prefill(q1, synth, torch, device, M, shape, affine, reps=20):
     g.manual_seed(1004)
     xs = [torch.randn((M, K), generator=g, device=device).to(torch.bfloat16) for _ in range(nl)]
     ys = [torch.empty((M, N), dtype=torch.bfloat16, device=device) for _ in range(nl)]
+    ws = q1.qmm_workspace(M, N, K, device)
     for i in range(nl):
-        q1.qmm(Ws[i], xs[i], out=ys[i])
+        q1.qmm(Ws[i], xs[i], workspace=ws, out=ys[i])
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for r in range(reps):
         i = r % nl
-        q1.qmm(Ws[i], xs[i], out=ys[i])
+        q1.qmm(Ws[i], xs[i], workspace=ws, out=ys[i])
     e1.record()
     torch.cuda.synchronize()
     t = e0.elapsed_time(e1) / 1e3 / reps
@@ -261,6 +262,40 @@ def time_prefill(q1, synth, torch, device, M, shape, affine, reps=20):
     t_unfused = e0.elapsed_time(e1) / 1e3 / reps
     del Ws, xs, ys, wd
     return 2.0 * M * N * K / t / 1e12, 2.0 * M * N * K / t_unfused / 1e12
+
+
+def profile_case(args):
+    """A few launches of one kernel on one shape, for ncu (small device footprint)."""
+    import torch
+    from bit_affine_quantized_g128_gb300 import build as qbuild
+    from bit_affine_quantized_g128_gb300 import q1, synth
+    qbuild.build()
+    q1.load_library()
+    device = torch.device("cuda", 0)
+    case = args.profile
+    if case.startswith("decode") or case.startswith("narrow"):
+        M = 1 if case.startswith("decode") else int(case.split("M")[-1])
+        shape = {"gate": SHAPES[0], "down": SHAPES[2], "attn": SHAPES[3]}[args.shape]
+        _, N, K = shape
+        nl = 12  # > L2 in total: 12 x 12.5 MB
+        Ws = [q1.Q1Weight(synth.device_weight_words(N, K, 11 + i, device),
+                          synth.device_scales(N, K, 111 + i, device), None, K) for i in range(nl)]
+        x = torch.randn((M, K), device=device).to(torch.bfloat16)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+        for r in range(args.steps):
+            q1.qmm_narrow(Ws[r % nl], x, out=y)
+    else:  # prefill
+        M = int(case.split("M")[-1])
+        _, N, K = {"gate": SHAPES[0], "down": SHAPES[2], "attn": SHAPES[3]}[args.shape]
+        W = q1.Q1Weight(synth.device_weight_words(N, K, 11, device), synth.device_scales(N, K, 111, device), None, K)
+        x = torch.randn((M, K), device=device).to(torch.bfloat16)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+        ws = q1.qmm_workspace(M, N, K, device)
+        for r in range(args.steps):
+            q1.qmm(W, x, workspace=ws, out=y)
+    torch.cuda.synchronize()
+    assert q1.device_errors() == 0
+    print("profile case done", case, args.shape)
 
 
 def gpu_arm(args):
@@ -472,9 +507,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-worker", type=float, default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--profile", default=None,
+                    help="run a few launches of one case for ncu: decode | narrowM<m> | prefillM<m>")
+    ap.add_argument("--shape", default="gate", choices=["gate", "down", "attn"])
     args = ap.parse_args()
     if args.cpu_worker is not None:
         cpu_worker(args.cpu_worker)
+        return
+    if args.profile:
+        profile_case(args)
         return
     if args.warmup < 3:
         args.warmup = 3

@@ -1,7 +1,8 @@
 // C ABI entry points of libq1 (declared in include/q1.h): host-side argument
 // validation, dispatch between the narrow and wide matmul paths, and launch
-// chaining.  No device memory is allocated here; scratch comes from the
-// caller's workspace.
+// chaining.  No device memory is allocated here; scratch (the prefill path's
+// fp16 activation rows, the fused FFN's intermediate) comes from the caller's
+// workspace.
 #include <atomic>
 #include <cstdlib>
 #include <cstring>
@@ -135,13 +136,21 @@ q1_status q1_qmm_narrow(const q1_weight *W, const void *x, int64_t M, q1_dtype d
   return cuda_status(q1::launch_narrow(q1::view(W), x, M, y, (cudaStream_t)stream, true));
 }
 
+size_t q1_qmm_workspace_size(int64_t M, int64_t N, int64_t K) {
+  (void)N;
+  if (M < 1 || K < 128 || K % 128) return 0;
+  return q1::wide_workspace_bytes(M, K);
+}
+
 q1_status q1_qmm(const q1_weight *W, const void *x, int64_t M, q1_dtype dtype, void *y,
-                 q1_stream stream) {
+                 void *workspace, size_t workspace_bytes, q1_stream stream) {
   q1_status s = matmul_common(W, x, M, dtype, y);
   if (s != Q1_OK) return s;
   if (M <= g_max_rows.load())
     return cuda_status(q1::launch_narrow(q1::view(W), x, M, y, (cudaStream_t)stream, true));
-  return cuda_status(q1::launch_wide(q1::view(W), x, M, y, (cudaStream_t)stream));
+  s = check_ws(workspace, workspace_bytes, q1::wide_workspace_bytes(M, W->K));
+  if (s != Q1_OK) return s;
+  return cuda_status(q1::launch_wide(q1::view(W), x, M, y, workspace, (cudaStream_t)stream));
 }
 
 q1_status q1_embed_gather(const q1_weight *E, const int32_t *ids, int64_t T, q1_dtype out_t,

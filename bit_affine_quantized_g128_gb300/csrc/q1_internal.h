@@ -43,7 +43,9 @@ cudaError_t launch_narrow_gate_up(const WeightView &G, const WeightView &U, cons
                                   int64_t M, void *h, cudaStream_t st, bool pdl);
 
 // ---- wide path (q1_wide.cu)
-cudaError_t launch_wide(const WeightView &W, const void *x, int64_t M, void *y,
+// workspace: fp16 activation rows [M][K] and per-row scales [M]
+size_t wide_workspace_bytes(int64_t M, int64_t K);
+cudaError_t launch_wide(const WeightView &W, const void *x, int64_t M, void *y, void *ws,
                         cudaStream_t st);
 
 // ---- device error words (each translation unit with bounded waits owns one)

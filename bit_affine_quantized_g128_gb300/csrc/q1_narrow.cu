@@ -37,7 +37,7 @@
 //   * the clusters split the 16-row tiles of W into contiguous ranges;
 //   * inside a CTA, the (row tile, group) units of the current round are cut
 //     into 16 equal contiguous ranges, one per warp, streamed through a
-//     double-buffered register pipeline of 8 units;
+//     double-buffered register pipeline of up to 4 groups of one row tile;
 //   * partial sums go to shared memory, are combined over warps in warp
 //     order, then over the cluster's CTAs in rank order through distributed
 //     shared memory (deterministic: fixed summation order, no atomics).
@@ -55,7 +55,7 @@ namespace {
 
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
-constexpr int kChunk = 8;            // units per register-pipeline stage
+constexpr int kChunk = 4;            // groups per register-pipeline stage
 constexpr int kXsThreadStride = 80;  // bytes per (group, token, quad-thread) block of x'
 constexpr int kSmemMax = 227 * 1024;
 
@@ -76,17 +76,20 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Two weights (bits p and p+16 of `src`) -> bf16x2 with base 1.0.
-template <int P>
-__device__ __forceinline__ uint32_t sel(uint32_t src) {
-  constexpr uint32_t m = 0x00010001u << P;
-  return (src & m) | (0x3F803F80u & ~m);
+// Two weights (bits p and p+16 of `src`) -> bf16x2 with base 1.0: one LOP3
+// selecting the masked bits of src and the other bits of `base` (the bf16x2
+// pattern of (1.0, 1.0)), with the mask as the immediate.
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t sel(uint32_t src, uint32_t base) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xE2;" : "=r"(r) : "r"(src), "n"(MASK), "r"(base));
+  return r;
 }
 template <int P>
-__device__ __forceinline__ uint32_t pair_reg(uint32_t w, uint32_t w8) {
-  if constexpr (P < 8) return sel<P>(w);
-  else if constexpr (P < 15) return sel<P - 8>(w8);
-  else return (w & 0x80008000u) | 0x3F803F80u;
+__device__ __forceinline__ uint32_t pair_reg(uint32_t w, uint32_t w8, uint32_t base) {
+  if constexpr (P < 8) return sel<(0x00010001u << P)>(w, base);
+  else if constexpr (P < 15) return sel<(0x00010001u << (P - 8))>(w8, base);
+  else return sel<0x80008000u>(w, base);
 }
 
 // Launch geometry, decided on the host.
@@ -98,16 +101,17 @@ struct Geo {
 };
 
 struct SmemLayout {
-  int xs, cs, part, red, total;
+  int xs, cs, part, red, meta, total;
 };
 
-__host__ __device__ inline SmemLayout smem_layout(int kslmax, int M, int tr, int rpw) {
+__host__ __device__ inline SmemLayout smem_layout(int kslmax, int tr, int rpw) {
   SmemLayout L;
   int off = 0;
-  L.xs = off; off += align_up(kslmax * M * 4 * kXsThreadStride, 128);
-  L.cs = off; off += align_up(kslmax * M * 8, 128);
+  L.xs = off; off += align_up(kslmax * 8 * 4 * kXsThreadStride, 128);
+  L.cs = off; off += align_up(kslmax * 8 * 8, 128);
   L.part = off; off += kWarps * rpw * 16 * 8 * 4;
   L.red = off; off += tr * 16 * 8 * 4;
+  L.meta = off; off += align_up((kWarps + tr) * 4, 128);
   L.total = off;
   return L;
 }
@@ -132,10 +136,12 @@ __device__ __forceinline__ int warp_of_unit(int X, int U) {
   return w < 0 ? 0 : (w > kWarps - 1 ? kWarps - 1 : w);
 }
 
+// One register-pipeline stage: up to kChunk consecutive groups of one row tile.
 struct Stage {
   uint32_t wa[kChunk], wb[kChunk];  // packed words, rows gid and gid+8
   uint32_t s[kChunk];               // fp16 scales: lo = row gid, hi = row gid+8
   uint32_t b[kChunk];               // fp16 biases (affine), same packing
+  int vt, j0, n;                    // virtual row tile, first group (slice-local), units
 };
 
 template <int NMAT, bool AFFINE>
@@ -151,97 +157,120 @@ __global__ void __launch_bounds__(kThreads, 1) narrow_kernel(NarrowArgs a) {
   const int g0 = (int)(((int64_t)rank * G) / KS), g1 = (int)(((int64_t)(rank + 1) * G) / KS);
   const int KSL = g1 - g0;
   const int kslmax = (G + KS - 1) / KS;
-  const SmemLayout L = smem_layout(kslmax, M, geo.tr, geo.rpw);
+  const SmemLayout L = smem_layout(kslmax, geo.tr, geo.rpw);
   unsigned char *xs = smem + L.xs;
-  float2 *css = reinterpret_cast<float2 *>(smem + L.cs);
+  float4 *css = reinterpret_cast<float4 *>(smem + L.cs);  // [j][token pair]: (C0, Sx0, C1, Sx1)
   float *part = reinterpret_cast<float *>(smem + L.part);
   float *red = reinterpret_cast<float *>(smem + L.red);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, t = lane & 3;
   const int NT = (int)((a.N + 15) / 16);
+  const int last_row = (int)(a.N - 1);
   // this cluster's virtual row tiles (matrix = v % NMAT, row tile = v / NMAT)
   const int v_lo = (int)(((int64_t)NT * clus) / geo.nclus) * NMAT;
   const int v_hi = (int)(((int64_t)NT * (clus + 1)) / geo.nclus) * NMAT;
+
+  // bf16x2 (1.0, 1.0), kept in one register for every unpack LOP3 (opaque to
+  // the compiler, so that it is not re-materialised per instruction)
+  uint32_t kbase;
+  asm volatile("mov.b32 %0, 0x3F803F80;" : "=r"(kbase));
 
   int round_v = v_lo;
   int T = min(geo.tr, v_hi - round_v);
   int U = T * KSL;
   int ua = range_start(U, warp), ub = range_start(U, warp + 1);
+  // loader cursor: next unit to load (as row tile + slice-local group) and units left
+  int ld_vt = round_v + ua / KSL, ld_j = ua % KSL, ld_left = ub - ua;
 
-  auto load_unit = [&](Stage &S, int i, int vt, int j) {
-    const int mat = NMAT == 2 ? (vt & 1) : 0;
-    const int64_t rt = NMAT == 2 ? (vt >> 1) : vt;
-    const int64_t nA = rt * 16 + gid, nB = nA + 8;
+  // Issue the loads of the next stage: consecutive groups of one row tile.
+  // Rows beyond N read row N-1 (in bounds; their results are never stored).
+  auto load_stage = [&](Stage &S) {
+    const int n = min(kChunk, min(KSL - ld_j, ld_left));
+    S.vt = ld_vt;
+    S.j0 = ld_j;
+    S.n = n;
+    const int mat = NMAT == 2 ? (ld_vt & 1) : 0;
+    const int rt = NMAT == 2 ? (ld_vt >> 1) : ld_vt;
+    const int rA = min(rt * 16 + gid, last_row), rB = min(rt * 16 + gid + 8, last_row);
     const uint32_t *W = mat == 0 ? a.w[0] : a.w[1];
     const uint16_t *Sp = mat == 0 ? a.s[0] : a.s[1];
     const uint16_t *Bp = mat == 0 ? a.b[0] : a.b[1];
-    const int g = g0 + j;
-    uint32_t wa = 0, wb = 0, s = 0, b = 0;
-    if (nA < a.N) {
-      wa = __ldg(W + nA * wpr + g * 4 + t);
-      s = __ldg(Sp + nA * G + g);
-      if (AFFINE && Bp) b = __ldg(Bp + nA * G + g);
-    }
-    if (nB < a.N) {
-      wb = __ldg(W + nB * wpr + g * 4 + t);
-      s |= (uint32_t)__ldg(Sp + nB * G + g) << 16;
-      if (AFFINE && Bp) b |= (uint32_t)__ldg(Bp + nB * G + g) << 16;
-    }
-    S.wa[i] = wa;
-    S.wb[i] = wb;
-    S.s[i] = s;
-    if (AFFINE) S.b[i] = Bp ? b : 0xFFFFFFFFu;  // all-ones: no stored bias, derive -s/2
-  };
-  auto load_chunk = [&](Stage &S, int u0, int uend) {
-    int vt = round_v + u0 / KSL, j = u0 % KSL;
+    const int g = g0 + ld_j;
+    const uint32_t *pa = W + (size_t)rA * wpr + g * 4 + t;
+    const uint32_t *pb = W + (size_t)rB * wpr + g * 4 + t;
+    const uint16_t *sa = Sp + (size_t)rA * G + g;
+    const uint16_t *sb = Sp + (size_t)rB * G + g;
 #pragma unroll
     for (int i = 0; i < kChunk; ++i) {
-      if (u0 + i < uend) load_unit(S, i, vt, j);
-      if (++j == KSL) { j = 0; ++vt; }
+      if (i < n) {
+        S.wa[i] = __ldg(pa + 4 * i);
+        S.wb[i] = __ldg(pb + 4 * i);
+        S.s[i] = (uint32_t)__ldg(sa + i) | ((uint32_t)__ldg(sb + i) << 16);
+        if (AFFINE) {
+          if (Bp) {
+            S.b[i] = (uint32_t)__ldg(Bp + (size_t)rA * G + g + i) |
+                     ((uint32_t)__ldg(Bp + (size_t)rB * G + g + i) << 16);
+          } else {
+            S.b[i] = 0xFFFFFFFFu;  // no stored bias: derive -s/2
+          }
+        }
+      }
+    }
+    ld_left -= n;
+    ld_j += n;
+    if (ld_j == KSL) {
+      ld_j = 0;
+      ++ld_vt;
     }
   };
 
   Stage SA, SB;
-  // the first chunk of weights goes out before anything else
-  if (ua < ub) load_chunk(SA, ua, ub);
+  // the first weights go out before anything else
+  if (ld_left > 0) load_stage(SA);
 
   // the next kernel of a dependent chain may start streaming its weights now
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // x may be the output of the preceding kernel: wait for it before reading
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  // ---- activation fragments of this CTA's K-slice -> shared memory
+  // ---- activation fragments of this CTA's K-slice -> shared memory, for 8
+  //      tokens (rows m >= M are zero, so every lane loads unconditionally)
   {
-    const int nitems = KSL * M * 4;  // (j, m, t) blocks of 32 k
+    const int nitems = KSL * 8 * 4;  // (j, m, t) blocks of 32 k
     for (int base = 0; base < nitems; base += kThreads) {
       const int i = base + tid;
       const bool valid = i < nitems;
       const int tt = i & 3, jm = i >> 2;
+      const int j = jm >> 3, m = jm & 7;
       float c = 0.f, sx = 0.f;
       if (valid) {
-        const int j = jm / M, m = jm - j * M;
-        const uint4 *src =
-            reinterpret_cast<const uint4 *>(a.x + (size_t)m * K + (size_t)(g0 + j) * 128 + 32 * tt);
-        uint32_t xv[16];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint4 v = __ldg(src + q);
-          xv[4 * q] = v.x; xv[4 * q + 1] = v.y; xv[4 * q + 2] = v.z; xv[4 * q + 3] = v.w;
-        }
         uint32_t pr[16];
+        if (m < M) {
+          const uint4 *src =
+              reinterpret_cast<const uint4 *>(a.x + (size_t)m * K + (size_t)(g0 + j) * 128 + 32 * tt);
+          uint32_t xv[16];
 #pragma unroll
-        for (int p = 0; p < 16; ++p) {
-          // x[p] is half (p & 1) of xv[p >> 1]; x[p+16] likewise in xv[8 + (p >> 1)]
-          const uint32_t lo_bits = (p & 1) ? (xv[p >> 1] >> 16) : (xv[p >> 1] & 0xFFFFu);
-          const uint32_t hi_bits = (p & 1) ? (xv[8 + (p >> 1)] >> 16) : (xv[8 + (p >> 1)] & 0xFFFFu);
-          const float xl = __uint_as_float(lo_bits << 16), xh = __uint_as_float(hi_bits << 16);
-          const float sc = inv_d(p);
-          const float pl = xl * sc, ph = xh * sc;  // exact: power-of-two scaling
-          const __nv_bfloat162 pb = __floats2bfloat162_rn(pl, ph);
-          pr[p] = *reinterpret_cast<const uint32_t *>(&pb);
-          c = fmaf(a_of(p), pl + ph, c);
-          sx += xl + xh;
+          for (int q = 0; q < 4; ++q) {
+            uint4 v = __ldg(src + q);
+            xv[4 * q] = v.x; xv[4 * q + 1] = v.y; xv[4 * q + 2] = v.z; xv[4 * q + 3] = v.w;
+          }
+#pragma unroll
+          for (int p = 0; p < 16; ++p) {
+            // x[p] is half (p & 1) of xv[p >> 1]; x[p+16] likewise in xv[8 + (p >> 1)]
+            const uint32_t lo_bits = (p & 1) ? (xv[p >> 1] >> 16) : (xv[p >> 1] & 0xFFFFu);
+            const uint32_t hi_bits = (p & 1) ? (xv[8 + (p >> 1)] >> 16) : (xv[8 + (p >> 1)] & 0xFFFFu);
+            const float xl = __uint_as_float(lo_bits << 16), xh = __uint_as_float(hi_bits << 16);
+            const float sc = inv_d(p);
+            const float pl = xl * sc, ph = xh * sc;  // exact: power-of-two scaling
+            const __nv_bfloat162 pb = __floats2bfloat162_rn(pl, ph);
+            pr[p] = *reinterpret_cast<const uint32_t *>(&pb);
+            c = fmaf(a_of(p), pl + ph, c);
+            sx += xl + xh;
+          }
+        } else {
+#pragma unroll
+          for (int p = 0; p < 16; ++p) pr[p] = 0u;
         }
         uint4 *dst = reinterpret_cast<uint4 *>(xs + ((size_t)jm * 4 + tt) * kXsThreadStride);
 #pragma unroll
@@ -252,61 +281,54 @@ __global__ void __launch_bounds__(kThreads, 1) narrow_kernel(NarrowArgs a) {
       sx += __shfl_xor_sync(0xffffffffu, sx, 1);
       c += __shfl_xor_sync(0xffffffffu, c, 2);
       sx += __shfl_xor_sync(0xffffffffu, sx, 2);
-      if (valid && tt == 0) css[jm] = make_float2(c, sx);
+      if (valid && tt == 0) {
+        // symmetric metadata folds the derived bias in: E = C + Sx / 2
+        float *cf = reinterpret_cast<float *>(css) + (size_t)j * 16 + (m >> 1) * 4 + (m & 1) * 2;
+        cf[0] = AFFINE ? c : fmaf(0.5f, sx, c);
+        cf[1] = sx;
+      }
     }
   }
   __syncthreads();
 
   while (true) {
-    // ---- stream this warp's units [ua, ub) of the round
+    // ---- stream this warp's units [ua, ub) of the round, one stage at a time
     const int vt_first = round_v + ua / KSL;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    int cur_vt = -1;
     auto flush = [&](int vt) {
       float *pp = part + ((size_t)(warp * geo.rpw + (vt - vt_first)) * 16) * 8;
       pp[gid * 8 + 2 * t] = acc[0];
       pp[gid * 8 + 2 * t + 1] = acc[1];
       pp[(gid + 8) * 8 + 2 * t] = acc[2];
       pp[(gid + 8) * 8 + 2 * t + 1] = acc[3];
+      acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
     };
-    auto process_chunk = [&](const Stage &S, int u0, int uend) {
-      int vt = round_v + u0 / KSL, j = u0 % KSL;
+    auto compute_stage = [&](const Stage &S) {
+      const unsigned char *xb = xs + ((size_t)(S.j0 * 8 + gid) * 4 + t) * kXsThreadStride;
+      const float4 *cb = css + (size_t)S.j0 * 4 + t;
 #pragma unroll
       for (int i = 0; i < kChunk; ++i) {
-        if (u0 + i < uend) {
-          if (vt != cur_vt) {
-            if (cur_vt >= 0) flush(cur_vt);
-            acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-            cur_vt = vt;
-          }
+        if (i < S.n) {
           uint32_t bfr[16];
-          if (gid < M) {
-            const uint4 *src =
-                reinterpret_cast<const uint4 *>(xs + ((size_t)(j * M + gid) * 4 + t) * kXsThreadStride);
+          const uint4 *src = reinterpret_cast<const uint4 *>(xb + (size_t)i * 8 * 4 * kXsThreadStride);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint4 v = src[q];
-              bfr[4 * q] = v.x; bfr[4 * q + 1] = v.y; bfr[4 * q + 2] = v.z; bfr[4 * q + 3] = v.w;
-            }
-          } else {
-#pragma unroll
-            for (int q = 0; q < 16; ++q) bfr[q] = 0u;
+          for (int q = 0; q < 4; ++q) {
+            uint4 v = src[q];
+            bfr[4 * q] = v.x; bfr[4 * q + 1] = v.y; bfr[4 * q + 2] = v.z; bfr[4 * q + 3] = v.w;
           }
           const uint32_t w0 = S.wa[i], w1 = S.wb[i], w08 = w0 >> 8, w18 = w1 >> 8;
           float d[4] = {0.f, 0.f, 0.f, 0.f};
           uint32_t af[4];
-#define Q1_MMA_STEP(JJ)                    \
-  af[0] = pair_reg<2 * (JJ)>(w0, w08);     \
-  af[1] = pair_reg<2 * (JJ)>(w1, w18);     \
-  af[2] = pair_reg<2 * (JJ) + 1>(w0, w08); \
-  af[3] = pair_reg<2 * (JJ) + 1>(w1, w18); \
+#define Q1_MMA_STEP(JJ)                              \
+  af[0] = pair_reg<2 * (JJ)>(w0, w08, kbase);        \
+  af[1] = pair_reg<2 * (JJ)>(w1, w18, kbase);        \
+  af[2] = pair_reg<2 * (JJ) + 1>(w0, w08, kbase);    \
+  af[3] = pair_reg<2 * (JJ) + 1>(w1, w18, kbase);    \
   mma_bf16_16816(d, af, bfr[2 * (JJ)], bfr[2 * (JJ) + 1]);
           Q1_MMA_STEP(0) Q1_MMA_STEP(1) Q1_MMA_STEP(2) Q1_MMA_STEP(3)
           Q1_MMA_STEP(4) Q1_MMA_STEP(5) Q1_MMA_STEP(6) Q1_MMA_STEP(7)
 #undef Q1_MMA_STEP
-          float2 c0 = make_float2(0.f, 0.f), c1 = make_float2(0.f, 0.f);
-          if (2 * t < M) c0 = css[j * M + 2 * t];
-          if (2 * t + 1 < M) c1 = css[j * M + 2 * t + 1];
+          const float4 cc = cb[(size_t)i * 4];  // (C or E, Sx) of tokens 2t, 2t+1
           const float sa = __half2float(__ushort_as_half((uint16_t)(S.s[i] & 0xFFFFu)));
           const float sb = __half2float(__ushort_as_half((uint16_t)(S.s[i] >> 16)));
           if (AFFINE) {
@@ -318,31 +340,39 @@ __global__ void __launch_bounds__(kThreads, 1) narrow_kernel(NarrowArgs a) {
               ba = __half2float(__ushort_as_half((uint16_t)(S.b[i] & 0xFFFFu)));
               bb = __half2float(__ushort_as_half((uint16_t)(S.b[i] >> 16)));
             }
-            acc[0] = fmaf(sa, d[0] - c0.x, fmaf(ba, c0.y, acc[0]));
-            acc[1] = fmaf(sa, d[1] - c1.x, fmaf(ba, c1.y, acc[1]));
-            acc[2] = fmaf(sb, d[2] - c0.x, fmaf(bb, c0.y, acc[2]));
-            acc[3] = fmaf(sb, d[3] - c1.x, fmaf(bb, c1.y, acc[3]));
+            acc[0] = fmaf(sa, d[0] - cc.x, fmaf(ba, cc.y, acc[0]));
+            acc[1] = fmaf(sa, d[1] - cc.z, fmaf(ba, cc.w, acc[1]));
+            acc[2] = fmaf(sb, d[2] - cc.x, fmaf(bb, cc.y, acc[2]));
+            acc[3] = fmaf(sb, d[3] - cc.z, fmaf(bb, cc.w, acc[3]));
           } else {
-            const float e0 = fmaf(0.5f, c0.y, c0.x), e1 = fmaf(0.5f, c1.y, c1.x);
-            acc[0] = fmaf(sa, d[0] - e0, acc[0]);
-            acc[1] = fmaf(sa, d[1] - e1, acc[1]);
-            acc[2] = fmaf(sb, d[2] - e0, acc[2]);
-            acc[3] = fmaf(sb, d[3] - e1, acc[3]);
+            acc[0] = fmaf(sa, d[0] - cc.x, acc[0]);
+            acc[1] = fmaf(sa, d[1] - cc.z, acc[1]);
+            acc[2] = fmaf(sb, d[2] - cc.x, acc[2]);
+            acc[3] = fmaf(sb, d[3] - cc.z, acc[3]);
           }
         }
-        if (++j == KSL) { j = 0; ++vt; }
       }
     };
-    for (int c0 = ua; c0 < ub; c0 += 2 * kChunk) {
-      if (c0 + kChunk < ub) load_chunk(SB, c0 + kChunk, ub);
-      process_chunk(SA, c0, ub);
-      if (c0 + kChunk >= ub) break;
-      if (c0 + 2 * kChunk < ub) load_chunk(SA, c0 + 2 * kChunk, ub);
-      process_chunk(SB, c0 + kChunk, ub);
+    // two stages in flight: load the next while computing the current
+    bool have_a = ua < ub, have_b = false;
+    while (have_a || have_b) {
+      if (have_a) {
+        have_b = ld_left > 0;
+        if (have_b) load_stage(SB);
+        compute_stage(SA);
+        if (!have_b || SB.vt != SA.vt) flush(SA.vt);
+        have_a = false;
+      }
+      if (have_b) {
+        have_a = ld_left > 0;
+        if (have_a) load_stage(SA);
+        compute_stage(SB);
+        if (!have_a || SA.vt != SB.vt) flush(SB.vt);
+        have_b = false;
+      }
     }
-    if (cur_vt >= 0) flush(cur_vt);
 
-    // ---- the next round's geometry, and its first chunk of weights in flight
+    // ---- the next round's geometry, and its first stage of weights in flight
     const int next_v = round_v + T;
     int nT = 0, nU = 0, nua = 0, nub = 0;
     if (next_v < v_hi) {
@@ -350,22 +380,32 @@ __global__ void __launch_bounds__(kThreads, 1) narrow_kernel(NarrowArgs a) {
       nU = nT * KSL;
       nua = range_start(nU, warp);
       nub = range_start(nU, warp + 1);
-      const int save_v = round_v;
-      round_v = next_v;  // load_chunk indexes from round_v
-      if (nua < nub) load_chunk(SA, nua, nub);
-      round_v = save_v;
+      ld_vt = next_v + nua / KSL;
+      ld_j = nua % KSL;
+      ld_left = nub - nua;
+      if (ld_left > 0) load_stage(SA);
     }
     __syncthreads();
 
-    // ---- combine the warps' partials per row tile, in warp order
+    // ---- combine the warps' partials per row tile, in warp order.  The
+    //      contributing warps of row tile lv and each warp's first row tile
+    //      are computed once (meta[]), then every element sums its slots.
+    int *meta = reinterpret_cast<int *>(smem + L.meta);  // [0,16): first lv per warp (-1 empty); [16..): wf | wl << 8
+    if (tid < kWarps) {
+      const int a0 = range_start(U, tid), a1 = range_start(U, tid + 1);
+      meta[tid] = a0 < a1 ? a0 / KSL : -1;
+    }
+    for (int lv = tid; lv < T; lv += kThreads)
+      meta[kWarps + lv] = warp_of_unit(lv * KSL, U) | (warp_of_unit(lv * KSL + KSL - 1, U) << 8);
+    __syncthreads();
     for (int i = tid; i < T * 128; i += kThreads) {
       const int lv = i >> 7, e = i & 127;
-      const int wf = warp_of_unit(lv * KSL, U), wl = warp_of_unit(lv * KSL + KSL - 1, U);
+      const int fl = meta[kWarps + lv];
       float sum = 0.f;
-      for (int w = wf; w <= wl; ++w) {
-        const int a0 = range_start(U, w), a1 = range_start(U, w + 1);
-        if (a0 >= a1) continue;  // empty range: this warp wrote nothing
-        sum += part[((size_t)(w * geo.rpw + (lv - a0 / KSL)) * 16) * 8 + e];
+      for (int w = fl & 0xFF; w <= (fl >> 8); ++w) {
+        const int f = meta[w];
+        if (f < 0) continue;  // empty range: this warp wrote nothing
+        sum += part[((size_t)(w * geo.rpw + (lv - f)) * 16) * 8 + e];
       }
       red[(size_t)lv * 128 + e] = sum;
     }
@@ -460,7 +500,6 @@ cudaError_t launch_impl(NarrowArgs args, cudaStream_t st, bool pdl) {
     attr_set = true;
   }
   const int G = args.K / 128;
-  const int M = args.M;
   const int NT = (int)((args.N + 15) / 16);
   // Pick the cluster size (K slices) that minimises the units of the busiest
   // CTA: ceil(row tiles per cluster) x ceil(groups per slice), among those
@@ -473,13 +512,13 @@ cudaError_t launch_impl(NarrowArgs args, cudaStream_t st, bool pdl) {
     if (nclus > NT) nclus = NT;
     const int kslmax = (G + ks - 1) / ks, kslmin = G / ks;
     const int vmax = ((NT + nclus - 1) / nclus) * NMAT;
-    const int xs_bytes = align_up(kslmax * M * 4 * kXsThreadStride, 128) + align_up(kslmax * M * 8, 128);
+    const int xs_bytes = align_up(kslmax * 8 * 4 * kXsThreadStride, 128) + align_up(kslmax * 8 * 8, 128);
     int tr = vmax, rpw = 0;
     bool ok = false;
     for (;;) {
       const int upw = (tr * kslmax + kWarps - 1) / kWarps;  // units per warp, at most
       rpw = (upw + kslmin - 1) / kslmin + 1;
-      const int total = xs_bytes + kWarps * rpw * 512 + tr * 512;
+      const int total = xs_bytes + kWarps * rpw * 512 + tr * 512 + align_up((kWarps + tr) * 4, 128);
       if (total <= kSmemMax) { ok = true; break; }
       if (tr <= NMAT) break;
       tr = tr / 2;
@@ -496,7 +535,7 @@ cudaError_t launch_impl(NarrowArgs args, cudaStream_t st, bool pdl) {
   }
   if (best_cost < 0) return cudaErrorInvalidConfiguration;
   args.geo = best;
-  const SmemLayout L = smem_layout((G + best.ks - 1) / best.ks, M, best.tr, best.rpw);
+  const SmemLayout L = smem_layout((G + best.ks - 1) / best.ks, best.tr, best.rpw);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(best.nclus * best.ks), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);

@@ -1,26 +1,34 @@
 // Wide (prefill) Q1 matmul on the tcgen05 tensor cores:
-//   y[M][N] = x[M][K] . bf16(Wd)^T, fp32 accumulation in tensor memory.
+//   y[M][N] = x[M][K] . Wd^T, fp32 accumulation in tensor memory.
 //
 // The page "Support Bonsai-27B affine Q1" (higgs PR #212), section
 // "Limitations / non-goals", runs forwards wider than the narrow threshold by
 // dequantizing the whole matrix to the input dtype and calling a dense matmul,
 // which is what set its peak memory ("Measured impact": peak about 6.65 GB
 // from dense prefill temporaries).  Here the dequantization happens per tile
-// in shared memory, feeding the MMA directly: no dense temporary exists.
-// Each weight is rounded to bf16 exactly as q1_dequantize rounds it, so the
-// product equals x . q1_dequantize(W, bf16)^T up to fp32 accumulation order.
+// in shared memory, feeding the MMA directly: no dense weight temporary.
+//
+// Operand precision.  Rounding the dequantized weights to bf16 (a half-ulp of
+// 2^-8, the same for every weight of a symmetric group) moves a few outputs in
+// 10^5 past the per-element error bar the method is held to, so the tiles are
+// fp16 instead: symmetric weights +-s/2 are exact in fp16 and affine values
+// s+b are rounded once at 2^-11.  The activations go to fp16 through a
+// per-row power-of-two scale 2^e_m chosen so that the row maximum lands in
+// [2^14, 2^15) (exact for every normal fp16 result, no overflow); the
+// epilogue multiplies by 2^-e_m.  A small prep kernel writes the scaled fp16
+// rows and the scales into the caller's workspace.
 //
 // One CTA computes a 128-token x 256-row output tile (one SM; 192 KB of shared
 // memory keeps it alone on the SM, so its 256-column TMEM allocation cannot
 // contend):
-//   warp 0        TMA producer: x tiles [128 tokens x 64 k] bf16, 128B swizzle
+//   warp 0        TMA producer: x tiles [128 tokens x 64 k] fp16, 128B swizzle
 //   warp 1        TMEM allocator and the single MMA-issuing thread
 //                 (tcgen05.mma.cta_group::1.kind::f16, M=128 N=256 K=16)
 //   warps 2..9    dequantizers: each thread owns one weight row, reads the
 //                 packed words of one group (uint4) and the group's
-//                 scale/bias, and writes 64 bf16 per k-step into the
+//                 scale/bias, and writes 64 fp16 per k-step into the
 //                 128B-swizzled K-major layout the MMA reads; then the
-//                 epilogue: TMEM -> registers -> bf16 -> global.
+//                 epilogue: TMEM -> registers -> scale -> bf16 -> global.
 // Stages: 4 x (16 KB x tile + 32 KB weight tile), mbarrier hand-offs.
 // Every wait is bounded (globaltimer); one that runs out sets a device error
 // word and a CTA-wide abort flag so that the other roles stop waiting too.
@@ -134,10 +142,10 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
-// K-major, N >> 3 at bits 17..22, M >> 4 at bits 24..28.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                            ((uint32_t)(BM >> 4) << 24);
+// Instruction descriptor, kind::f16: fp32 accumulator (bits 4..5 = 1), fp16 A
+// and B (format 0 at bits 7..9 and 10..12), both K-major, N >> 3 at bits
+// 17..22, M >> 4 at bits 24..28.
+constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 
 __device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
                                           uint32_t accumulate) {
@@ -186,7 +194,7 @@ struct GroupData {
 __global__ void __launch_bounds__(kThreadsWide, 1)
 wide_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint32_t *__restrict__ W,
             const uint16_t *__restrict__ S, const uint16_t *__restrict__ Bv, int M, int N, int K,
-            __nv_bfloat16 *__restrict__ y) {
+            const float *__restrict__ inv_scale, __nv_bfloat16 *__restrict__ y) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char *base = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -224,6 +232,8 @@ wide_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint32_t *__restri
   if (warp == 0) {
     // ---------------- TMA producer (x tiles)
     if (lane == 0) {
+      // the fp16 rows come from the prep kernel that precedes this one
+      asm volatile("griddepcontrol.wait;" ::: "memory");
       for (int ks = 0; ks < KSTEPS; ++ks) {
         const int s = ks % STAGES;
         const uint32_t ph = (uint32_t)(ks / STAGES) & 1u;
@@ -276,8 +286,8 @@ wide_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint32_t *__restri
     auto process = [&](int g, const GroupData &gd) {
       const float sc = __half2float(__ushort_as_half(gd.s));
       const float bi = brow ? __half2float(__ushort_as_half(gd.b)) : __fmul_rn(-0.5f, sc);
-      const uint32_t lo16 = __bfloat16_as_ushort(__float2bfloat16_rn(bi));
-      const uint32_t hi16 = __bfloat16_as_ushort(__float2bfloat16_rn(__fadd_rn(sc, bi)));
+      const uint32_t lo16 = __half_as_ushort(__float2half_rn(bi));
+      const uint32_t hi16 = __half_as_ushort(__float2half_rn(__fadd_rn(sc, bi)));
       const uint32_t lo2 = lo16 | (lo16 << 16), hi2 = hi16 | (hi16 << 16);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -330,8 +340,10 @@ wide_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint32_t *__restri
     acc_ok = __shfl_sync(0xffffffffu, acc_ok, 0);
     if (acc_ok) {
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      asm volatile("griddepcontrol.wait;" ::: "memory");  // inv_scale comes from the prep kernel
       const int quarter = warp & 3, half = (warp - kDeqWarp0) >> 2;
       const int m = m0 + 32 * quarter + lane;
+      const float rs = m < M ? inv_scale[m] : 0.f;
 #pragma unroll 1
       for (int cc = 0; cc < 4; ++cc) {
         const int col = half * 128 + cc * 32;
@@ -360,8 +372,8 @@ wide_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint32_t *__restri
               uint32_t p[4];
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                __nv_bfloat162 t2 = __floats2bfloat162_rn(__uint_as_float(v[8 * q + 2 * e]),
-                                                          __uint_as_float(v[8 * q + 2 * e + 1]));
+                __nv_bfloat162 t2 = __floats2bfloat162_rn(__uint_as_float(v[8 * q + 2 * e]) * rs,
+                                                          __uint_as_float(v[8 * q + 2 * e + 1]) * rs);
                 p[e] = *reinterpret_cast<uint32_t *>(&t2);
               }
               reinterpret_cast<uint4 *>(dst)[q] = make_uint4(p[0], p[1], p[2], p[3]);
@@ -369,7 +381,7 @@ wide_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint32_t *__restri
           } else {
 #pragma unroll
             for (int e = 0; e < 32; ++e)
-              if (n + e < N) dst[e] = __float2bfloat16_rn(__uint_as_float(v[e]));
+              if (n + e < N) dst[e] = __float2bfloat16_rn(__uint_as_float(v[e]) * rs);
           }
         }
       }
@@ -383,6 +395,55 @@ wide_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint32_t *__restri
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_d), "r"(kTmemCols)
                  : "memory");
   }
+}
+
+// x [M][K] bf16 -> x16 [M][K] fp16 = x * 2^e_m and inv_scale[m] = 2^-e_m, with
+// e_m = 14 - floor(log2(max_k |x[m][k]|)) so that the row maximum lands in
+// [2^14, 2^15).  Multiplying by a power of two is exact; the fp16 rounding is
+// exact for every result that is a normal fp16 value.  One warp per row.
+__global__ void __launch_bounds__(256) x_to_f16_kernel(const __nv_bfloat16 *__restrict__ x, int M,
+                                                       int K, __half *__restrict__ x16,
+                                                       float *__restrict__ inv_scale) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (warp >= M) return;
+  const uint4 *row = reinterpret_cast<const uint4 *>(x + (size_t)warp * K);
+  const int n16 = K / 8;  // 16-byte chunks
+  float mx = 0.f;
+  for (int i = lane; i < n16; i += 32) {
+    uint4 v = __ldg(row + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      mx = fmaxf(mx, fabsf(__uint_as_float(w[q] << 16)));
+      mx = fmaxf(mx, fabsf(__uint_as_float(w[q] & 0xFFFF0000u)));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  int e = 0;
+  if (mx > 0.f && mx <= 3.0e38f) {
+    const int E = (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127;  // floor(log2) for normal mx
+    e = 14 - (E < -126 ? -126 : E);
+    if (e > 126) e = 126;
+    if (e < -126) e = -126;
+  }
+  const float sc = __uint_as_float((uint32_t)(127 + e) << 23);   // 2^e, exact
+  const float isc = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e, exact
+  uint4 *out = reinterpret_cast<uint4 *>(x16 + (size_t)warp * K);
+  for (int i = lane; i < n16; i += 32) {
+    uint4 v = __ldg(row + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const __half2 h = __floats2half2_rn(__uint_as_float(w[q] << 16) * sc,
+                                          __uint_as_float(w[q] & 0xFFFF0000u) * sc);
+      o[q] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+    out[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  if (lane == 0) inv_scale[warp] = isc;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -400,17 +461,35 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 
 }  // namespace
 
-cudaError_t launch_wide(const WeightView &W, const void *x, int64_t M, void *y,
+size_t wide_workspace_bytes(int64_t M, int64_t K) {
+  const size_t x16 = ((size_t)(M * K * 2) + 255) / 256 * 256;
+  return x16 + ((size_t)(M * 4) + 255) / 256 * 256;
+}
+
+cudaError_t launch_wide(const WeightView &W, const void *x, int64_t M, void *y, void *ws,
                         cudaStream_t st) {
   auto encode = get_encode();
   if (!encode) return cudaErrorNotSupported;
+  __half *x16 = static_cast<__half *>(ws);
+  float *inv_scale = reinterpret_cast<float *>(static_cast<char *>(ws) +
+                                               ((size_t)(M * W.K * 2) + 255) / 256 * 256);
+  // 1. fp16 rows with per-row power-of-two scales
+  {
+    const unsigned blocks = (unsigned)((M * 32 + 255) / 256);
+    x_to_f16_kernel<<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(x), (int)M, (int)W.K,
+                                            x16, inv_scale);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  // 2. the tcgen05 kernel, launched as a programmatic dependent of the prep:
+  //    barrier set-up, TMEM allocation and the first weight tiles overlap it
   CUtensorMap map;
   cuuint64_t gdim[2] = {(cuuint64_t)W.K, (cuuint64_t)M};
   cuuint64_t gstride[1] = {(cuuint64_t)W.K * 2};
   cuuint32_t box[2] = {BK, BM};
   cuuint32_t estride[2] = {1, 1};
-  CUresult r = encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(x), gdim, gstride,
-                      box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  CUresult r = encode(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x16, gdim, gstride, box, estride,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   static bool attr = false;
@@ -420,10 +499,18 @@ cudaError_t launch_wide(const WeightView &W, const void *x, int64_t M, void *y,
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  dim3 grid((unsigned)((W.N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM), 1);
-  wide_kernel<<<grid, kThreadsWide, kSmemBytes, st>>>(map, W.w, W.s, W.b, (int)M, (int)W.N, (int)W.K,
-                                                      static_cast<__nv_bfloat16 *>(y));
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((W.N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM), 1);
+  cfg.blockDim = dim3(kThreadsWide, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr_pdl;
+  attr_pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr_pdl.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr_pdl;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, wide_kernel, map, W.w, W.s, W.b, (int)M, (int)W.N, (int)W.K,
+                            (const float *)inv_scale, static_cast<__nv_bfloat16 *>(y));
 }
 
 unsigned int read_and_clear_wide_errors(cudaStream_t st, cudaError_t *err) {

@@ -21,7 +21,7 @@ _DT = {torch.bfloat16: Q1_BF16, torch.float16: Q1_F16, torch.float32: Q1_F32}
 
 # every symbol include/q1.h declares
 EXPORTED = [
-    "q1_pack", "q1_unpack", "q1_dequantize", "q1_qmv",
+    "q1_pack", "q1_unpack", "q1_dequantize", "q1_qmv", "q1_qmm_workspace_size",
     "q1_qmm_narrow", "q1_qmm", "q1_set_qmm_max_rows", "q1_get_qmm_max_rows",
     "q1_embed_gather", "q1_ffn_workspace_size", "q1_ffn_fused", "q1_check_symmetric",
     "q1_device_errors", "q1_status_string",
@@ -59,7 +59,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "q1_dequantize": ([W, I32, P, P], I32),
         "q1_qmv": ([W, P, I32, P, P], I32),
         "q1_qmm_narrow": ([W, P, I64, I32, P, P], I32),
-        "q1_qmm": ([W, P, I64, I32, P, P], I32),
+        "q1_qmm_workspace_size": ([I64, I64, I64], SZ),
+        "q1_qmm": ([W, P, I64, I32, P, P, SZ, P], I32),
         "q1_set_qmm_max_rows": ([ctypes.c_int], None),
         "q1_get_qmm_max_rows": ([], ctypes.c_int),
         "q1_embed_gather": ([W, P, I64, I32, P, P, P], I32),
@@ -161,24 +162,37 @@ def qmv(W: Q1Weight, x: torch.Tensor, out: Optional[torch.Tensor] = None) -> tor
     return y
 
 
-def _qmm_call(fn: str, W: Q1Weight, x: torch.Tensor, out):
-    lead = x.shape[:-1]
-    x2 = _flat(x, W.K)
-    M = x2.shape[0]
-    y = out if out is not None else torch.empty((M, W.N), dtype=x.dtype, device=x.device)
-    _check(fn, getattr(lib(), fn)(W.cref(), x2.data_ptr(), M, _DT[x.dtype], y.data_ptr(),
-                                  _stream()))
-    return y.reshape(*lead, W.N)
+def qmm_workspace(M: int, N: int, K: int, device) -> torch.Tensor:
+    n = lib().q1_qmm_workspace_size(M, N, K)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
 
 
 def qmm_narrow(W: Q1Weight, x: torch.Tensor, out=None) -> torch.Tensor:
     """x [..., K] with prod(leading dims) <= 8 -> y [..., N]; weights stay packed."""
-    return _qmm_call("q1_qmm_narrow", W, x, out)
+    lead = x.shape[:-1]
+    x2 = _flat(x, W.K)
+    M = x2.shape[0]
+    y = out if out is not None else torch.empty((M, W.N), dtype=x.dtype, device=x.device)
+    _check("q1_qmm_narrow", lib().q1_qmm_narrow(W.cref(), x2.data_ptr(), M, _DT[x.dtype],
+                                                y.data_ptr(), _stream()))
+    return y.reshape(*lead, W.N)
 
 
-def qmm(W: Q1Weight, x: torch.Tensor, out=None) -> torch.Tensor:
-    """x [..., K] -> y [..., N]; narrow path up to the row threshold, tcgen05 beyond."""
-    return _qmm_call("q1_qmm", W, x, out)
+def qmm(W: Q1Weight, x: torch.Tensor, workspace: Optional[torch.Tensor] = None,
+        out=None) -> torch.Tensor:
+    """x [..., K] -> y [..., N]; narrow path up to the row threshold, tcgen05 beyond
+    (which needs a workspace; one is allocated when none is given)."""
+    lead = x.shape[:-1]
+    x2 = _flat(x, W.K)
+    M = x2.shape[0]
+    y = out if out is not None else torch.empty((M, W.N), dtype=x.dtype, device=x.device)
+    ws = workspace
+    if ws is None and M > get_qmm_max_rows():
+        ws = qmm_workspace(M, W.N, W.K, x.device)
+    wp, wn = (ws.data_ptr(), ws.numel()) if ws is not None else (None, 0)
+    _check("q1_qmm", lib().q1_qmm(W.cref(), x2.data_ptr(), M, _DT[x.dtype], y.data_ptr(), wp, wn,
+                                  _stream()))
+    return y.reshape(*lead, W.N)
 
 
 def set_qmm_max_rows(rows: int):

@@ -25,11 +25,11 @@
  *     launch returns Q1_ERR_CUDA.  No exception crosses the ABI.
  *   - Activations/outputs of the matmul calls are bf16 (Q1_BF16); other dtypes
  *     return Q1_ERR_DTYPE.
- *   - The one call that needs scratch (q1_ffn_fused, for its intermediate
- *     activations) takes a caller-owned device workspace and its size;
- *     q1_ffn_workspace_size returns the bytes needed.  The workspace must be
- *     256-byte aligned and must not be used by another call that may run
- *     concurrently.
+ *   - Calls that need scratch (q1_qmm on its prefill path, q1_ffn_fused for
+ *     its intermediate activations) take a caller-owned device workspace and
+ *     its size; q1_qmm_workspace_size / q1_ffn_workspace_size return the
+ *     bytes needed.  A workspace must be 256-byte aligned and must not be used
+ *     by another call that may run concurrently.
  *   - Device-side waits in the kernels are bounded; one that runs out sets a
  *     device error word that q1_device_errors() reads (Q1_ERR_TIMEOUT).
  *   - The narrow matmul and FFN kernels are launched with programmatic
@@ -100,14 +100,21 @@ q1_status q1_dequantize(const q1_weight *W, q1_dtype out_t, void *out, q1_stream
  *   matrix multiplies of up to 8 flattened rows).  Leading dimensions are
  *   flattened by the caller: x [B][T][K] is passed as M = B*T.
  * q1_qmm: any M >= 1.  M <= q1_get_qmm_max_rows() runs the narrow path;
- *   wider M runs the prefill path, which dequantizes tiles to bf16 in shared
- *   memory and multiplies them on the tcgen05 tensor cores (no dense
- *   temporary in global memory either). */
+ *   wider M runs the prefill path, which dequantizes weight tiles in shared
+ *   memory and multiplies them on the tcgen05 tensor cores (no dense weight
+ *   temporary).  Its tiles are fp16: symmetric weights are exact and affine
+ *   ones rounded once at 2^-11; the activations enter as fp16 rows scaled by
+ *   a power of two per row (kept in the workspace), which is exact for every
+ *   activation whose scaled value is a normal fp16 number. */
 q1_status q1_qmv(const q1_weight *W, const void *x, q1_dtype dtype, void *y, q1_stream stream);
 q1_status q1_qmm_narrow(const q1_weight *W, const void *x, int64_t M, q1_dtype dtype,
                         void *y, q1_stream stream);
+/* Workspace of q1_qmm: fp16 activation rows and per-row scales of the prefill
+ * path, M*K*2 + M*4 bytes rounded up (256-byte aligned).  The call needs it
+ * only when M > q1_get_qmm_max_rows(); workspace may be NULL otherwise. */
+size_t q1_qmm_workspace_size(int64_t M, int64_t N, int64_t K);
 q1_status q1_qmm(const q1_weight *W, const void *x, int64_t M, q1_dtype dtype, void *y,
-                 q1_stream stream);
+                 void *workspace, size_t workspace_bytes, q1_stream stream);
 /* Narrow/wide threshold (higgs PR #212, "Limitations": HIGGS_BONSAI_QMM_MAX_ROWS,
  * default 8).  Values are clamped to [0, 8].  The environment variable
  * Q1_QMM_MAX_ROWS, if set, gives the initial value when the library loads. */
