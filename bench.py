@@ -328,13 +328,8 @@ def gpu_arm(args):
     with ClockSampler(local) as clk:
         secs = run_timed(torch, graph, args.steps, stream, dist)
     clocks = clk.summary()
-    t_max = secs
-    if dist is not None:
-        tt = torch.tensor([secs], dtype=torch.float64, device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_max = float(tt.item())
     bytes_step = step_bytes(1)
-    value = bytes_step * args.steps * world / t_max / 1e9
+    value, t_max, _ = aggregate_over_ranks(bytes_step * args.steps, secs, dist, device)
     launches = args.steps * LAYERS * len(SHAPES)
 
     # ---- e2e: inputs from pinned host memory, outputs back, every step
@@ -375,11 +370,8 @@ def gpu_arm(args):
         e1.record(stream)
     torch.cuda.synchronize()
     t_e2e = e0.elapsed_time(e1) / 1e3
-    if dist is not None:
-        tt = torch.tensor([t_e2e], dtype=torch.float64, device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_e2e = float(tt.item())
-    e2e = {"value": bytes_step * e2e_steps * world / t_e2e / 1e9, "unit": "GB/s",
+    e2e_value, _, _ = aggregate_over_ranks(bytes_step * e2e_steps, t_e2e, dist, device)
+    e2e = {"value": round(e2e_value, 1), "unit": "GB/s",
            "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": y_host.numel() * 2,
            "path": "q1_qmv calls captured in a CUDA graph; x copied from pinned host and y back every step"}
     del g2, graph
@@ -460,6 +452,22 @@ def gpu_arm(args):
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def aggregate_over_ranks(bytes_per_rank: float, secs: float, dist=None, device=None):
+    """Whole-job GB/s across ranks: total bytes of all ranks / the slowest
+    rank's time (the max over ranks), as every rank processes its own replica."""
+    world, t_max, tot = 1, secs, bytes_per_rank
+    if dist is not None and dist.is_initialized():
+        import torch
+        world = dist.get_world_size()
+        tt = torch.tensor([secs, bytes_per_rank], dtype=torch.float64, device=device)
+        t = tt[:1].clone()
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        b = tt[1:].clone()
+        dist.all_reduce(b, op=dist.ReduceOp.SUM)
+        t_max, tot = float(t.item()), float(b.item())
+    return tot / t_max / 1e9, t_max, world
 
 
 def reference_arm(args):

@@ -213,10 +213,11 @@ q1_status q1_check_symmetric(const q1_weight *W, int32_t *d_is_symmetric, q1_str
 q1_status q1_device_errors(unsigned int *flags, q1_stream stream) {
   q1_status s = check_device();
   if (s != Q1_OK) return s;
-  cudaError_t e = cudaSuccess;
-  unsigned int v = q1::read_and_clear_wide_errors((cudaStream_t)stream, &e);
+  cudaError_t e1 = cudaSuccess, e2 = cudaSuccess;
+  unsigned int v = q1::read_and_clear_wide_errors((cudaStream_t)stream, &e1);
+  v |= q1::read_and_clear_narrow_errors((cudaStream_t)stream, &e2) << 1;
   if (flags) *flags = v;
-  if (e != cudaSuccess) return Q1_ERR_CUDA;
+  if (e1 != cudaSuccess || e2 != cudaSuccess) return Q1_ERR_CUDA;
   return v ? Q1_ERR_TIMEOUT : Q1_OK;
 }
 

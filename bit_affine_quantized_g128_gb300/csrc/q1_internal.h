@@ -50,5 +50,6 @@ cudaError_t launch_wide(const WeightView &W, const void *x, int64_t M, void *y, 
 
 // ---- device error words (each translation unit with bounded waits owns one)
 unsigned int read_and_clear_wide_errors(cudaStream_t st, cudaError_t *err);
+unsigned int read_and_clear_narrow_errors(cudaStream_t st, cudaError_t *err);
 
 }  // namespace q1

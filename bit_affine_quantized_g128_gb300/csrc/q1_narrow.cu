@@ -35,14 +35,19 @@
 //     owns groups [G r / KS, G (r+1) / KS) and keeps their activation
 //     fragments in shared memory for the whole kernel);
 //   * the clusters split the 16-row tiles of W into contiguous ranges;
-//   * inside a CTA, the (row tile, group) units of the current round are cut
-//     into 16 equal contiguous ranges, one per warp, streamed through a
-//     double-buffered register pipeline of up to 4 groups of one row tile;
+//   * a tile is 16 rows x 4 groups (1 KB of packed words).  Inside a CTA the
+//     tiles of the current round are cut into 16 equal contiguous ranges, one
+//     per warp; each warp streams its tiles through its own ring of shared
+//     memory slots filled by TMA (64-byte swizzle: conflict-free reads), so
+//     several kilobytes per warp are always in flight;
 //   * partial sums go to shared memory, are combined over warps in warp
 //     order, then over the cluster's CTAs in rank order through distributed
 //     shared memory (deterministic: fixed summation order, no atomics).
 // One pair of cluster barriers per round; most shapes need a single round.
+// Every mbarrier wait is bounded: one that runs out sets a device error word.
 #include <cooperative_groups.h>
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -51,13 +56,18 @@
 namespace cg = cooperative_groups;
 
 namespace q1 {
+
+__device__ unsigned int g_narrow_err = 0;
+
 namespace {
 
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
-constexpr int kChunk = 4;            // groups per register-pipeline stage
-constexpr int kXsThreadStride = 80;  // bytes per (group, token, quad-thread) block of x'
+constexpr int kQuad = 4;              // groups per tile
+constexpr int kTileBytes = 16 * 64;   // 16 rows x 16 words
+constexpr int kXsThreadStride = 80;   // bytes per (group, token, quad-thread) block of x'
 constexpr int kSmemMax = 227 * 1024;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
 __host__ __device__ constexpr int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
@@ -69,7 +79,9 @@ __device__ __forceinline__ float a_of(int p) { return p == 7 ? 0.5f : 1.0f; }
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4],
                                                uint32_t b0, uint32_t b1) {
-  asm volatile(
+  // not volatile: no side effects, so the compiler may interleave the
+  // independent MMA chains of a tile's four groups
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
       "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -92,32 +104,85 @@ __device__ __forceinline__ uint32_t pair_reg(uint32_t w, uint32_t w8, uint32_t b
   else return sel<0x80008000u>(w, base);
 }
 
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ float4 lds128f(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ bool mbar_try(uint32_t addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait; false when it ran out (the device error word is set).
+__device__ __noinline__ bool mbar_wait_bounded(uint32_t addr, uint32_t parity) {
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try(addr, parity)) return true;
+    if ((i & 15u) == 15u && globaltimer() - t0 > kWaitLimitNs) {
+      atomicOr(&g_narrow_err, 1u);
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity) {
+  if (mbar_try(addr, parity)) return true;
+  return mbar_wait_bounded(addr, parity);
+}
+
 // Launch geometry, decided on the host.
 struct Geo {
   int ks;     // CTAs per cluster (K slices)
   int nclus;  // clusters
   int tr;     // virtual row tiles per round
   int rpw;    // partial slots per warp (row tiles one warp can touch in a round)
+  int ring;   // TMA slots per warp
 };
 
 struct SmemLayout {
-  int xs, cs, part, red, meta, total;
+  int ring, bars, xs, cs, part, red, meta, total;
 };
 
-__host__ __device__ inline SmemLayout smem_layout(int kslmax, int tr, int rpw) {
+// qmax: tiles (of 4 groups) per row tile in the widest K-slice; mst: tokens stored
+__host__ __device__ inline SmemLayout smem_layout(int qmax, int mst, int tr, int rpw, int ring) {
   SmemLayout L;
   int off = 0;
-  L.xs = off; off += align_up(kslmax * 8 * 4 * kXsThreadStride, 128);
-  L.cs = off; off += align_up(kslmax * 8 * 8, 128);
+  L.ring = off; off += kWarps * ring * kTileBytes;
+  L.bars = off; off += align_up(kWarps * ring * 8, 128);
+  // x' for qmax*4 groups x mst tokens, then one zero block (lanes with no token)
+  L.xs = off; off += align_up((qmax * kQuad * mst + 1) * 4 * kXsThreadStride, 128);
+  L.cs = off; off += align_up(qmax * kQuad * 8 * 8, 128);
   L.part = off; off += kWarps * rpw * 16 * 8 * 4;
   L.red = off; off += tr * 16 * 8 * 4;
   L.meta = off; off += align_up((kWarps + tr) * 4, 128);
-  L.total = off;
+  L.total = off + 1024;  // slack for aligning the dynamic shared memory base
   return L;
 }
 
 struct NarrowArgs {
-  const uint32_t *w[2];
   const uint16_t *s[2];
   const uint16_t *b[2];
   int64_t N;
@@ -128,40 +193,41 @@ struct NarrowArgs {
   Geo geo;
 };
 
-// Start of warp w's contiguous unit range when U units are cut into 16.
+// Start of warp w's contiguous tile range when U tiles are cut into 16.
 __host__ __device__ __forceinline__ int range_start(int U, int w) { return (U * w) / kWarps; }
-// The warp whose range holds unit X (the last warp whose range starts at or before X).
-__device__ __forceinline__ int warp_of_unit(int X, int U) {
+// The warp whose range holds tile X (the last warp whose range starts at or before X).
+__device__ __forceinline__ int warp_of_tile(int X, int U) {
   int w = (kWarps * (X + 1) + U - 1) / U - 1;
   return w < 0 ? 0 : (w > kWarps - 1 ? kWarps - 1 : w);
 }
 
-// One register-pipeline stage: up to kChunk consecutive groups of one row tile.
-struct Stage {
-  uint32_t wa[kChunk], wb[kChunk];  // packed words, rows gid and gid+8
-  uint32_t s[kChunk];               // fp16 scales: lo = row gid, hi = row gid+8
-  uint32_t b[kChunk];               // fp16 biases (affine), same packing
-  int vt, j0, n;                    // virtual row tile, first group (slice-local), units
-};
-
 template <int NMAT, bool AFFINE>
-__global__ void __launch_bounds__(kThreads, 1) narrow_kernel(NarrowArgs a) {
-  extern __shared__ __align__(128) unsigned char smem[];
+__global__ void __launch_bounds__(kThreads, 1)
+narrow_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
+              NarrowArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // TMA with the 64-byte swizzle wants 512-byte aligned slots: align the base
+  unsigned char *smem = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   cg::cluster_group cluster = cg::this_cluster();
 
-  const int M = a.M, K = a.K, G = K / 128, wpr = K / 32;
+  const int M = a.M, K = a.K, G = K / 128;
   const Geo geo = a.geo;
-  const int KS = geo.ks;
+  const int KS = geo.ks, RING = geo.ring;
   const int rank = (int)cluster.block_rank();
   const int clus = blockIdx.x / KS;
   const int g0 = (int)(((int64_t)rank * G) / KS), g1 = (int)(((int64_t)(rank + 1) * G) / KS);
   const int KSL = g1 - g0;
-  const int kslmax = (G + KS - 1) / KS;
-  const SmemLayout L = smem_layout(kslmax, geo.tr, geo.rpw);
+  const int Q = (KSL + kQuad - 1) / kQuad;  // tiles per row tile in this slice
+  const int qmax = ((G + KS - 1) / KS + kQuad - 1) / kQuad;
+  const SmemLayout L = smem_layout(qmax, M, geo.tr, geo.rpw, RING);
+  unsigned char *ring = smem + L.ring;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bars);
   unsigned char *xs = smem + L.xs;
-  float4 *css = reinterpret_cast<float4 *>(smem + L.cs);  // [j][token pair]: (C0, Sx0, C1, Sx1)
+  float2 *css = reinterpret_cast<float2 *>(smem + L.cs);  // [j][token]: (C or E, Sx)
   float *part = reinterpret_cast<float *>(smem + L.part);
   float *red = reinterpret_cast<float *>(smem + L.red);
+  int *meta = reinterpret_cast<int *>(smem + L.meta);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, t = lane & 3;
@@ -176,77 +242,67 @@ __global__ void __launch_bounds__(kThreads, 1) narrow_kernel(NarrowArgs a) {
   uint32_t kbase;
   asm volatile("mov.b32 %0, 0x3F803F80;" : "=r"(kbase));
 
+  unsigned char *my_ring = ring + warp * RING * kTileBytes;
+  uint64_t *my_bars = bars + warp * RING;
+  if (lane < RING) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(my_bars + lane)) : "memory");
+  }
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  __syncwarp();
+
   int round_v = v_lo;
   int T = min(geo.tr, v_hi - round_v);
-  int U = T * KSL;
+  int U = T * Q;
   int ua = range_start(U, warp), ub = range_start(U, warp + 1);
-  // loader cursor: next unit to load (as row tile + slice-local group) and units left
-  int ld_vt = round_v + ua / KSL, ld_j = ua % KSL, ld_left = ub - ua;
+  uint32_t issued = 0;  // tiles this warp consumed in earlier rounds (ring phase)
 
-  // Issue the loads of the next stage: consecutive groups of one row tile.
-  // Rows beyond N read row N-1 (in bounds; their results are never stored).
-  auto load_stage = [&](Stage &S) {
-    const int n = min(kChunk, min(KSL - ld_j, ld_left));
-    S.vt = ld_vt;
-    S.j0 = ld_j;
-    S.n = n;
-    const int mat = NMAT == 2 ? (ld_vt & 1) : 0;
-    const int rt = NMAT == 2 ? (ld_vt >> 1) : ld_vt;
-    const int rA = min(rt * 16 + gid, last_row), rB = min(rt * 16 + gid + 8, last_row);
-    const uint32_t *W = mat == 0 ? a.w[0] : a.w[1];
-    const uint16_t *Sp = mat == 0 ? a.s[0] : a.s[1];
-    const uint16_t *Bp = mat == 0 ? a.b[0] : a.b[1];
-    const int g = g0 + ld_j;
-    const uint32_t *pa = W + (size_t)rA * wpr + g * 4 + t;
-    const uint32_t *pb = W + (size_t)rB * wpr + g * 4 + t;
-    const uint16_t *sa = Sp + (size_t)rA * G + g;
-    const uint16_t *sb = Sp + (size_t)rB * G + g;
-#pragma unroll
-    for (int i = 0; i < kChunk; ++i) {
-      if (i < n) {
-        S.wa[i] = __ldg(pa + 4 * i);
-        S.wb[i] = __ldg(pb + 4 * i);
-        S.s[i] = (uint32_t)__ldg(sa + i) | ((uint32_t)__ldg(sb + i) << 16);
-        if (AFFINE) {
-          if (Bp) {
-            S.b[i] = (uint32_t)__ldg(Bp + (size_t)rA * G + g + i) |
-                     ((uint32_t)__ldg(Bp + (size_t)rB * G + g + i) << 16);
-          } else {
-            S.b[i] = 0xFFFFFFFFu;  // no stored bias: derive -s/2
-          }
-        }
+  // lane 0: TMA of the round's tile (row tile lv, quad q) into the slot of
+  // sequence number `seq`
+  auto issue = [&](int lv, int q, uint32_t seq) {
+    const int vt = round_v + lv;
+    const int mat = NMAT == 2 ? (vt & 1) : 0;
+    const int rt = NMAT == 2 ? (vt >> 1) : vt;
+    const int slot = (int)(seq % (uint32_t)RING);
+    const uint32_t bar = smem_u32(my_bars + slot);
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(kTileBytes)
+                 : "memory");
+    const CUtensorMap *tm = mat == 0 ? &tm0 : &tm1;
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(smem_u32(my_ring + slot * kTileBytes)), "l"(tm), "r"((g0 + q * kQuad) * 4), "r"(rt * 16),
+        "r"(bar)
+        : "memory");
+  };
+  auto prime = [&]() {  // first RING tiles of this warp's range
+    if (lane == 0) {
+      int lv = ua / Q, q = ua - (ua / Q) * Q;
+      for (int i = 0; i < RING && ua + i < ub; ++i) {
+        issue(lv, q, issued + (uint32_t)i);
+        if (++q == Q) { q = 0; ++lv; }
       }
     }
-    ld_left -= n;
-    ld_j += n;
-    if (ld_j == KSL) {
-      ld_j = 0;
-      ++ld_vt;
-    }
   };
-
-  Stage SA, SB;
-  // the first weights go out before anything else
-  if (ld_left > 0) load_stage(SA);
+  prime();
 
   // the next kernel of a dependent chain may start streaming its weights now
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // x may be the output of the preceding kernel: wait for it before reading
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  // ---- activation fragments of this CTA's K-slice -> shared memory, for 8
-  //      tokens (rows m >= M are zero, so every lane loads unconditionally)
+  // ---- activation fragments of this CTA's K-slice -> shared memory, padded
+  //      with zeros to whole tiles, plus the zero block for lanes gid >= M
   {
-    const int nitems = KSL * 8 * 4;  // (j, m, t) blocks of 32 k
+    const int jn = Q * kQuad;
+    const int nitems = jn * M * 4;  // (j, m, t) blocks of 32 k
     for (int base = 0; base < nitems; base += kThreads) {
       const int i = base + tid;
       const bool valid = i < nitems;
       const int tt = i & 3, jm = i >> 2;
-      const int j = jm >> 3, m = jm & 7;
+      const int j = jm / M, m = jm - j * M;
       float c = 0.f, sx = 0.f;
       if (valid) {
         uint32_t pr[16];
-        if (m < M) {
+        if (j < KSL) {
           const uint4 *src =
               reinterpret_cast<const uint4 *>(a.x + (size_t)m * K + (size_t)(g0 + j) * 128 + 32 * tt);
           uint32_t xv[16];
@@ -283,120 +339,186 @@ __global__ void __launch_bounds__(kThreads, 1) narrow_kernel(NarrowArgs a) {
       sx += __shfl_xor_sync(0xffffffffu, sx, 2);
       if (valid && tt == 0) {
         // symmetric metadata folds the derived bias in: E = C + Sx / 2
-        float *cf = reinterpret_cast<float *>(css) + (size_t)j * 16 + (m >> 1) * 4 + (m & 1) * 2;
-        cf[0] = AFFINE ? c : fmaf(0.5f, sx, c);
-        cf[1] = sx;
+        css[j * 8 + m] = make_float2(AFFINE ? c : fmaf(0.5f, sx, c), sx);
       }
     }
+    // zero block, and the (C, Sx) entries of tokens m >= M
+    unsigned char *zb = xs + (size_t)jn * M * 4 * kXsThreadStride;
+    for (int i = tid; i < 4 * kXsThreadStride / 16; i += kThreads)
+      reinterpret_cast<uint4 *>(zb)[i] = make_uint4(0, 0, 0, 0);
+    for (int i = tid; i < jn * 8; i += kThreads)
+      if ((i & 7) >= M) css[i] = make_float2(0.f, 0.f);
   }
   __syncthreads();
 
+  // per-lane constants of the compute loop (32-bit shared-memory addresses)
+  const uint32_t xlane = smem_u32(gid < M ? xs + ((size_t)gid * 4 + t) * kXsThreadStride
+                                          : xs + ((size_t)Q * kQuad * M * 4 + t) * kXsThreadStride);
+  const uint32_t xj_stride = gid < M ? (uint32_t)(M * 4 * kXsThreadStride) : 0u;  // per group
+  const uint32_t clane = smem_u32(css + 2 * t);
+  const uint32_t ring_lane = smem_u32(my_ring) + gid * 64 + 4 * t;
+  const uint32_t part_lane = smem_u32(part) + (uint32_t)((gid * 8 + 2 * t) * 4);
+  // word offsets of the four groups of a tile under the 64-byte swizzle (rows
+  // gid and gid + 8 share it: ((r >> 1) & 3) is the same for both)
+  const int swz = (gid >> 1) & 3;
+  uint32_t woff[kQuad];
+#pragma unroll
+  for (int u = 0; u < kQuad; ++u) woff[u] = (uint32_t)((u ^ swz) << 4);
+
   while (true) {
-    // ---- stream this warp's units [ua, ub) of the round, one stage at a time
-    const int vt_first = round_v + ua / KSL;
+    // ---- stream this warp's tiles [ua, ub) of the round
+    const int vt_first = round_v + ua / Q;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    auto flush = [&](int vt) {
-      float *pp = part + ((size_t)(warp * geo.rpw + (vt - vt_first)) * 16) * 8;
-      pp[gid * 8 + 2 * t] = acc[0];
-      pp[gid * 8 + 2 * t + 1] = acc[1];
-      pp[(gid + 8) * 8 + 2 * t] = acc[2];
-      pp[(gid + 8) * 8 + 2 * t + 1] = acc[3];
-      acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+    // scales (and biases) of one tile's 4 groups, rows gid and gid + 8; groups
+    // past this K-slice (tile padding) read as scale 0
+    auto load_meta = [&](int lv, int q, uint32_t (&sw)[kQuad], uint32_t (&bw)[kQuad]) {
+      const int vt = round_v + lv;
+      const int rt = NMAT == 2 ? (vt >> 1) : vt;
+      const int mat = NMAT == 2 ? (vt & 1) : 0;
+      const int rA = min(rt * 16 + gid, last_row), rB = min(rt * 16 + gid + 8, last_row);
+      const int jb = q * kQuad;
+      const size_t oA = (size_t)rA * G + g0 + jb, oB = (size_t)rB * G + g0 + jb;
+      const uint16_t *pA = (mat == 0 ? a.s[0] : a.s[1]) + oA;
+      const uint16_t *pB = (mat == 0 ? a.s[0] : a.s[1]) + oB;
+      const uint16_t *Bp = mat == 0 ? a.b[0] : a.b[1];
+      if (jb + kQuad <= KSL) {  // whole tile inside the K-slice (all but a slice's last tile)
+#pragma unroll
+        for (int u = 0; u < kQuad; ++u) {
+          sw[u] = (uint32_t)__ldg(pA + u) | ((uint32_t)__ldg(pB + u) << 16);
+          if (AFFINE) bw[u] = Bp ? ((uint32_t)__ldg(Bp + oA + u) | ((uint32_t)__ldg(Bp + oB + u) << 16))
+                                 : 0xFFFFFFFFu;  // no stored bias: derive -s/2
+        }
+      } else {  // groups past the slice (tile padding) read as scale 0
+#pragma unroll
+        for (int u = 0; u < kQuad; ++u) {
+          const bool in = jb + u < KSL;
+          sw[u] = in ? ((uint32_t)__ldg(pA + u) | ((uint32_t)__ldg(pB + u) << 16)) : 0u;
+          if (AFFINE)
+            bw[u] = Bp ? (in ? ((uint32_t)__ldg(Bp + oA + u) | ((uint32_t)__ldg(Bp + oB + u) << 16)) : 0u)
+                       : 0xFFFFFFFFu;
+        }
+      }
     };
-    auto compute_stage = [&](const Stage &S) {
-      const unsigned char *xb = xs + ((size_t)(S.j0 * 8 + gid) * 4 + t) * kXsThreadStride;
-      const float4 *cb = css + (size_t)S.j0 * 4 + t;
+    auto prefetch_meta_l2 = [&](int lv, int q) {
+      const int vt = round_v + lv;
+      const int rt = NMAT == 2 ? (vt >> 1) : vt;
+      const uint16_t *Sp = (NMAT == 2 && (vt & 1)) ? a.s[1] : a.s[0];
+      const int r = min(rt * 16 + (lane & 15), last_row);
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(Sp + (size_t)r * G + g0 + q * kQuad));
+    };
+    uint32_t sw[kQuad], bw[kQuad], swn[kQuad], bwn[kQuad];
+    // cursors (row tile, quad) of the current tile, the next one, and the one
+    // RING ahead (the refill target), advanced without divisions
+    int lv = ua / Q, q = ua - (ua / Q) * Q;
+    int lv1 = lv, q1 = q;
+    if (++q1 == Q) { q1 = 0; ++lv1; }
+    int lvR = (ua + RING) / Q, qR = (ua + RING) - ((ua + RING) / Q) * Q;
+    int slot = (int)(issued % (uint32_t)RING);
+    uint32_t phase = (issued / (uint32_t)RING) & 1u;
+    if (ua < ub) load_meta(lv, q, sw, bw);
+    for (int tile = ua; tile < ub; ++tile) {
+      const uint32_t seq = issued + (uint32_t)(tile - ua);
+      const int vt = round_v + lv;
+      const int jb = q * kQuad;
+      if (tile + 1 < ub) load_meta(lv1, q1, swn, bwn);
+      if (tile + RING < ub && lane < 16) prefetch_meta_l2(lvR, qR);
+      const uint32_t tb = ring_lane + (uint32_t)(slot * kTileBytes);
+      const uint32_t xb = xlane + (uint32_t)jb * xj_stride;
+      // a wait that ran out has set the device error word; the results of this
+      // call are then undefined, but the CTA still reaches its barriers
+      mbar_wait(smem_u32(my_bars + slot), phase);
 #pragma unroll
-      for (int i = 0; i < kChunk; ++i) {
-        if (i < S.n) {
-          uint32_t bfr[16];
-          const uint4 *src = reinterpret_cast<const uint4 *>(xb + (size_t)i * 8 * 4 * kXsThreadStride);
+      for (int u = 0; u < kQuad; ++u) {
+        const int j = jb + u;
+        const uint32_t w0 = lds32(tb + woff[u]);
+        const uint32_t w1 = lds32(tb + woff[u] + 8 * 64);
+        uint32_t bfr[16];
+        const uint32_t xu = xb + (uint32_t)u * xj_stride;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 v = src[q];
-            bfr[4 * q] = v.x; bfr[4 * q + 1] = v.y; bfr[4 * q + 2] = v.z; bfr[4 * q + 3] = v.w;
-          }
-          const uint32_t w0 = S.wa[i], w1 = S.wb[i], w08 = w0 >> 8, w18 = w1 >> 8;
-          float d[4] = {0.f, 0.f, 0.f, 0.f};
-          uint32_t af[4];
+        for (int qq = 0; qq < 4; ++qq) {
+          uint4 v = lds128(xu + 16 * qq);
+          bfr[4 * qq] = v.x; bfr[4 * qq + 1] = v.y; bfr[4 * qq + 2] = v.z; bfr[4 * qq + 3] = v.w;
+        }
+        const uint32_t w08 = w0 >> 8, w18 = w1 >> 8;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t af[4];
 #define Q1_MMA_STEP(JJ)                              \
   af[0] = pair_reg<2 * (JJ)>(w0, w08, kbase);        \
   af[1] = pair_reg<2 * (JJ)>(w1, w18, kbase);        \
   af[2] = pair_reg<2 * (JJ) + 1>(w0, w08, kbase);    \
   af[3] = pair_reg<2 * (JJ) + 1>(w1, w18, kbase);    \
   mma_bf16_16816(d, af, bfr[2 * (JJ)], bfr[2 * (JJ) + 1]);
-          Q1_MMA_STEP(0) Q1_MMA_STEP(1) Q1_MMA_STEP(2) Q1_MMA_STEP(3)
-          Q1_MMA_STEP(4) Q1_MMA_STEP(5) Q1_MMA_STEP(6) Q1_MMA_STEP(7)
+        Q1_MMA_STEP(0) Q1_MMA_STEP(1) Q1_MMA_STEP(2) Q1_MMA_STEP(3)
+        Q1_MMA_STEP(4) Q1_MMA_STEP(5) Q1_MMA_STEP(6) Q1_MMA_STEP(7)
 #undef Q1_MMA_STEP
-          const float4 cc = cb[(size_t)i * 4];  // (C or E, Sx) of tokens 2t, 2t+1
-          const float sa = __half2float(__ushort_as_half((uint16_t)(S.s[i] & 0xFFFFu)));
-          const float sb = __half2float(__ushort_as_half((uint16_t)(S.s[i] >> 16)));
-          if (AFFINE) {
-            float ba, bb;
-            if (S.b[i] == 0xFFFFFFFFu) {  // matrix without stored biases: symmetric
-              ba = __fmul_rn(-0.5f, sa);
-              bb = __fmul_rn(-0.5f, sb);
-            } else {
-              ba = __half2float(__ushort_as_half((uint16_t)(S.b[i] & 0xFFFFu)));
-              bb = __half2float(__ushort_as_half((uint16_t)(S.b[i] >> 16)));
-            }
-            acc[0] = fmaf(sa, d[0] - cc.x, fmaf(ba, cc.y, acc[0]));
-            acc[1] = fmaf(sa, d[1] - cc.z, fmaf(ba, cc.w, acc[1]));
-            acc[2] = fmaf(sb, d[2] - cc.x, fmaf(bb, cc.y, acc[2]));
-            acc[3] = fmaf(sb, d[3] - cc.z, fmaf(bb, cc.w, acc[3]));
+        const float4 cc = lds128f(clane + (uint32_t)j * 64);  // (C or E, Sx) of tokens 2t, 2t+1
+        const float sa = __half2float(__ushort_as_half((uint16_t)(sw[u] & 0xFFFFu)));
+        const float sb = __half2float(__ushort_as_half((uint16_t)(sw[u] >> 16)));
+        if (AFFINE) {
+          float ba, bb;
+          if (bw[u] == 0xFFFFFFFFu) {  // matrix without stored biases: symmetric
+            ba = __fmul_rn(-0.5f, sa);
+            bb = __fmul_rn(-0.5f, sb);
           } else {
-            acc[0] = fmaf(sa, d[0] - cc.x, acc[0]);
-            acc[1] = fmaf(sa, d[1] - cc.z, acc[1]);
-            acc[2] = fmaf(sb, d[2] - cc.x, acc[2]);
-            acc[3] = fmaf(sb, d[3] - cc.z, acc[3]);
+            ba = __half2float(__ushort_as_half((uint16_t)(bw[u] & 0xFFFFu)));
+            bb = __half2float(__ushort_as_half((uint16_t)(bw[u] >> 16)));
           }
+          acc[0] = fmaf(sa, d[0] - cc.x, fmaf(ba, cc.y, acc[0]));
+          acc[1] = fmaf(sa, d[1] - cc.z, fmaf(ba, cc.w, acc[1]));
+          acc[2] = fmaf(sb, d[2] - cc.x, fmaf(bb, cc.y, acc[2]));
+          acc[3] = fmaf(sb, d[3] - cc.z, fmaf(bb, cc.w, acc[3]));
+        } else {
+          acc[0] = fmaf(sa, d[0] - cc.x, acc[0]);
+          acc[1] = fmaf(sa, d[1] - cc.z, acc[1]);
+          acc[2] = fmaf(sb, d[2] - cc.x, acc[2]);
+          acc[3] = fmaf(sb, d[3] - cc.z, acc[3]);
         }
       }
-    };
-    // two stages in flight: load the next while computing the current
-    bool have_a = ua < ub, have_b = false;
-    while (have_a || have_b) {
-      if (have_a) {
-        have_b = ld_left > 0;
-        if (have_b) load_stage(SB);
-        compute_stage(SA);
-        if (!have_b || SB.vt != SA.vt) flush(SA.vt);
-        have_a = false;
+#pragma unroll
+      for (int u = 0; u < kQuad; ++u) {
+        sw[u] = swn[u];
+        if (AFFINE) bw[u] = bwn[u];
       }
-      if (have_b) {
-        have_a = ld_left > 0;
-        if (have_a) load_stage(SA);
-        compute_stage(SB);
-        if (!have_a || SA.vt != SB.vt) flush(SB.vt);
-        have_b = false;
+      // the slot is free once every lane has read it: refill it RING tiles ahead
+      __syncwarp();
+      if (lane == 0 && tile + RING < ub) issue(lvR, qR, seq + (uint32_t)RING);
+      // row tile finished (next tile belongs to another one, or range ends)
+      if (tile + 1 == ub || lv1 != lv) {
+        const uint32_t pp = part_lane + (uint32_t)((warp * geo.rpw + (vt - vt_first)) * 16 * 8 * 4);
+        asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(pp), "f"(acc[0]), "f"(acc[1]) : "memory");
+        asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(pp + 8 * 8 * 4), "f"(acc[2]), "f"(acc[3])
+                     : "memory");
+        acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
       }
+      // advance the cursors and the ring position
+      lv = lv1;
+      q = q1;
+      if (++q1 == Q) { q1 = 0; ++lv1; }
+      if (++qR == Q) { qR = 0; ++lvR; }
+      if (++slot == RING) { slot = 0; phase ^= 1u; }
     }
+    issued += (uint32_t)(ub - ua);
 
-    // ---- the next round's geometry, and its first stage of weights in flight
+    // ---- the next round's geometry
     const int next_v = round_v + T;
     int nT = 0, nU = 0, nua = 0, nub = 0;
     if (next_v < v_hi) {
       nT = min(geo.tr, v_hi - next_v);
-      nU = nT * KSL;
+      nU = nT * Q;
       nua = range_start(nU, warp);
       nub = range_start(nU, warp + 1);
-      ld_vt = next_v + nua / KSL;
-      ld_j = nua % KSL;
-      ld_left = nub - nua;
-      if (ld_left > 0) load_stage(SA);
     }
     __syncthreads();
 
     // ---- combine the warps' partials per row tile, in warp order.  The
     //      contributing warps of row tile lv and each warp's first row tile
     //      are computed once (meta[]), then every element sums its slots.
-    int *meta = reinterpret_cast<int *>(smem + L.meta);  // [0,16): first lv per warp (-1 empty); [16..): wf | wl << 8
     if (tid < kWarps) {
       const int a0 = range_start(U, tid), a1 = range_start(U, tid + 1);
-      meta[tid] = a0 < a1 ? a0 / KSL : -1;
+      meta[tid] = a0 < a1 ? a0 / Q : -1;
     }
     for (int lv = tid; lv < T; lv += kThreads)
-      meta[kWarps + lv] = warp_of_unit(lv * KSL, U) | (warp_of_unit(lv * KSL + KSL - 1, U) << 8);
+      meta[kWarps + lv] = warp_of_tile(lv * Q, U) | (warp_of_tile(lv * Q + Q - 1, U) << 8);
     __syncthreads();
     for (int i = tid; i < T * 128; i += kThreads) {
       const int lv = i >> 7, e = i & 127;
@@ -448,6 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1) narrow_kernel(NarrowArgs a) {
     U = nU;
     ua = nua;
     ub = nub;
+    prime();
   }
 }
 
@@ -472,7 +595,7 @@ int max_clusters(int ks) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(ks * 64), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = 96 * 1024;  // a typical footprint; residency is bound by 1 CTA/SM anyway
+  cfg.dynamicSmemBytes = 96 * 1024;  // residency is bound by one CTA per SM anyway
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeClusterDimension;
   attr.val.clusterDim.x = (unsigned)ks;
@@ -490,8 +613,36 @@ int max_clusters(int ks) {
   return n;
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void *p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// Packed words [N][K/32] as a 2-D uint32 tensor; boxes of 16 words x 16 rows
+// with the 64-byte swizzle; rows >= N and words >= K/32 read as zero.
+bool make_word_map(CUtensorMap *map, const uint32_t *w, int64_t N, int64_t K) {
+  auto encode = encode_fn();
+  if (!encode) return false;
+  cuuint64_t gdim[2] = {(cuuint64_t)(K / 32), (cuuint64_t)N};
+  cuuint64_t gstride[1] = {(cuuint64_t)(K / 32) * 4};
+  cuuint32_t box[2] = {16, 16};
+  cuuint32_t estride[2] = {1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t *>(w), gdim, gstride, box,
+                estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int NMAT, bool AFFINE>
-cudaError_t launch_impl(NarrowArgs args, cudaStream_t st, bool pdl) {
+cudaError_t launch_impl(NarrowArgs args, const uint32_t *w0, const uint32_t *w1, cudaStream_t st,
+                        bool pdl) {
   auto kern = narrow_kernel<NMAT, AFFINE>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -499,11 +650,15 @@ cudaError_t launch_impl(NarrowArgs args, cudaStream_t st, bool pdl) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
+  CUtensorMap tm0, tm1;
+  if (!make_word_map(&tm0, w0, args.N, args.K)) return cudaErrorInvalidValue;
+  if (!make_word_map(&tm1, w1, args.N, args.K)) return cudaErrorInvalidValue;
   const int G = args.K / 128;
+  const int M = args.M;
   const int NT = (int)((args.N + 15) / 16);
-  // Pick the cluster size (K slices) that minimises the units of the busiest
-  // CTA: ceil(row tiles per cluster) x ceil(groups per slice), among those
-  // whose shared memory fits.
+  // Pick the cluster size (K slices) that minimises the tiles of the busiest
+  // CTA, ceil(row tiles per cluster) x ceil(tiles per slice), among those
+  // whose shared memory fits; for it, the deepest TMA ring that fits.
   Geo best{};
   long best_cost = -1;
   for (int ks = 1; ks <= 8; ks *= 2) {
@@ -511,31 +666,35 @@ cudaError_t launch_impl(NarrowArgs args, cudaStream_t st, bool pdl) {
     int nclus = max_clusters<NMAT, AFFINE>(ks);
     if (nclus > NT) nclus = NT;
     const int kslmax = (G + ks - 1) / ks, kslmin = G / ks;
+    const int qmax = (kslmax + kQuad - 1) / kQuad, qmin = (kslmin + kQuad - 1) / kQuad;
     const int vmax = ((NT + nclus - 1) / nclus) * NMAT;
-    const int xs_bytes = align_up(kslmax * 8 * 4 * kXsThreadStride, 128) + align_up(kslmax * 8 * 8, 128);
-    int tr = vmax, rpw = 0;
-    bool ok = false;
-    for (;;) {
-      const int upw = (tr * kslmax + kWarps - 1) / kWarps;  // units per warp, at most
-      rpw = (upw + kslmin - 1) / kslmin + 1;
-      const int total = xs_bytes + kWarps * rpw * 512 + tr * 512 + align_up((kWarps + tr) * 4, 128);
-      if (total <= kSmemMax) { ok = true; break; }
-      if (tr <= NMAT) break;
-      tr = tr / 2;
-      if (NMAT == 2) tr &= ~1;
-      if (tr < NMAT) tr = NMAT;
-    }
-    if (!ok) continue;
-    const int rounds = (vmax + tr - 1) / tr;
-    const long cost = (long)vmax * kslmax + (long)rounds * 64;  // a round costs ~2 cluster barriers
-    if (best_cost < 0 || cost < best_cost) {
-      best_cost = cost;
-      best = Geo{ks, nclus, tr, rpw};
+    for (int ring = 8; ring >= 3; --ring) {
+      int tr = vmax, rpw = 0;
+      bool ok = false;
+      for (;;) {
+        const int upw = (tr * qmax + kWarps - 1) / kWarps;  // tiles per warp, at most
+        rpw = (upw + qmin - 1) / qmin + 1;
+        if (smem_layout(qmax, M, tr, rpw, ring).total <= kSmemMax) { ok = true; break; }
+        if (tr <= NMAT) break;
+        tr = tr / 2;
+        if (NMAT == 2) tr &= ~1;
+        if (tr < NMAT) tr = NMAT;
+      }
+      if (!ok) continue;
+      const int rounds = (vmax + tr - 1) / tr;
+      // tiles of the busiest CTA, a round's two cluster barriers, and a shallow ring
+      const long cost = (long)vmax * qmax * 4 + (long)rounds * 256 + (8 - ring) * 8;
+      if (best_cost < 0 || cost < best_cost) {
+        best_cost = cost;
+        best = Geo{ks, nclus, tr, rpw, ring};
+      }
+      break;  // deepest ring that fits for this ks
     }
   }
   if (best_cost < 0) return cudaErrorInvalidConfiguration;
   args.geo = best;
-  const SmemLayout L = smem_layout((G + best.ks - 1) / best.ks, best.tr, best.rpw);
+  const int qmax = ((G + best.ks - 1) / best.ks + kQuad - 1) / kQuad;
+  const SmemLayout L = smem_layout(qmax, M, best.tr, best.rpw, best.ring);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(best.nclus * best.ks), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -550,7 +709,7 @@ cudaError_t launch_impl(NarrowArgs args, cudaStream_t st, bool pdl) {
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, kern, args);
+  return cudaLaunchKernelEx(&cfg, kern, tm0, tm1, args);
 }
 
 NarrowArgs make_args(const void *x, int64_t M, int64_t N, int64_t K, void *out) {
@@ -568,25 +727,33 @@ NarrowArgs make_args(const void *x, int64_t M, int64_t N, int64_t K, void *out) 
 cudaError_t launch_narrow(const WeightView &W, const void *x, int64_t M, void *y,
                           cudaStream_t st, bool pdl) {
   NarrowArgs a = make_args(x, M, W.N, W.K, y);
-  a.w[0] = a.w[1] = W.w;
   a.s[0] = a.s[1] = W.s;
   a.b[0] = a.b[1] = W.b;
-  return W.b ? launch_impl<1, true>(a, st, pdl) : launch_impl<1, false>(a, st, pdl);
+  return W.b ? launch_impl<1, true>(a, W.w, W.w, st, pdl) : launch_impl<1, false>(a, W.w, W.w, st, pdl);
 }
 
 cudaError_t launch_narrow_gate_up(const WeightView &G, const WeightView &U, const void *x,
                                   int64_t M, void *h, cudaStream_t st, bool pdl) {
   NarrowArgs a = make_args(x, M, G.N, G.K, h);
-  a.w[0] = G.w;
-  a.w[1] = U.w;
   a.s[0] = G.s;
   a.s[1] = U.s;
   a.b[0] = G.b;
   a.b[1] = U.b;
   // With mixed metadata the affine variant runs for both matrices; it derives
   // -scale/2 for the one whose biases pointer is null.
-  if (G.b || U.b) return launch_impl<2, true>(a, st, pdl);
-  return launch_impl<2, false>(a, st, pdl);
+  if (G.b || U.b) return launch_impl<2, true>(a, G.w, U.w, st, pdl);
+  return launch_impl<2, false>(a, G.w, U.w, st, pdl);
+}
+
+unsigned int read_and_clear_narrow_errors(cudaStream_t st, cudaError_t *err) {
+  unsigned int v = 0, zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_narrow_err, sizeof(v), 0, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess && v)
+    e = cudaMemcpyToSymbolAsync(g_narrow_err, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (err) *err = e;
+  return v;
 }
 
 }  // namespace q1

@@ -73,6 +73,10 @@ def test_threshold_env_read_at_load(libpath):
 
 
 def test_binding_raises_without_library(tmp_path):
-    from bit_affine_quantized_g128_gb300 import q1
-    with pytest.raises(RuntimeError):
-        q1.load_library(str(tmp_path / "missing.so")) if q1._lib is None else (_ for _ in ()).throw(RuntimeError())
+    # a fresh process: the binding refuses to run without the CUDA library
+    code = ("from bit_affine_quantized_g128_gb300 import q1\n"
+            "try:\n    q1.load_library(%r)\nexcept RuntimeError as e:\n    print('raised', e)\n"
+            % str(tmp_path / "missing.so"))
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, cwd=ROOT,
+                         check=True).stdout
+    assert out.startswith("raised")
