@@ -3,6 +3,12 @@
 // rates, and back-to-back 12.5 MB streaming launches in a CUDA graph with and
 // without programmatic dependent launch.
 //
+// The MMA loops keep their operands loop-invariant, so they time the MMA
+// instructions alone.  For e4m3 that hides the cost that matters: in a real
+// kernel whose fp8 operands change every step, ncu's per-opcode counts show
+// each m16n8k32 e4m3 mma.sync executing as two HMMAs plus F2FP operand
+// conversions on the CUDA cores.
+//
 //   nvcc -gencode arch=compute_103a,code=sm_103a -O3 -o /tmp/gb300_pipes \
 //        bit_affine_quantized_g128_gb300/probe/gb300_pipes.cu && /tmp/gb300_pipes
 //

@@ -124,6 +124,25 @@ def test_qmv_and_leading_dims(q1):
     check_matmul(y3.reshape(8, N), yo, x, wd, "[2,4,K]")
 
 
+@pytest.mark.parametrize("affine", [False, True])
+def test_narrow_mixed_magnitudes(q1, affine):
+    # rows far above and below 1, and groups with a single large outlier:
+    # exercises the per-(group, token) power-of-two scale of the activations
+    M, N, K = 8, 512, 2048
+    t, x = _case(N, K, M, affine, seed=17)
+    x = x.float()
+    x[1] *= 1e6
+    x[2] *= 1e-6
+    x[3, 5] *= 1e4
+    x[4, 130:140] = 0.0
+    x[5, 256:384] = 0.0  # an all-zero group
+    x = x.to(torch.bfloat16)
+    W = q1.Q1Weight.from_host(t)
+    y = q1.qmm_narrow(W, x.to(DEV))
+    check_matmul(y, O.qmm(x, t.words, t.scales, t.biases, K), x,
+                 O.dequantize_f32(t.words, t.scales, t.biases, K), "narrow mixed magnitudes")
+
+
 def test_narrow_deterministic(q1):
     t, x = _case(2048, 5120, 4, False, seed=7)
     W = q1.Q1Weight.from_host(t)
