@@ -24,11 +24,11 @@
 //   warp 0        TMA producer: x tiles [128 tokens x 64 k] fp16, 128B swizzle
 //   warp 1        TMEM allocator and the single MMA-issuing thread
 //                 (tcgen05.mma.cta_group::1.kind::f16, M=128 N=256 K=16)
-//   warps 2..9    dequantizers: each thread owns one weight row, reads the
-//                 packed words of one group (uint4) and the group's
-//                 scale/bias, and writes 64 fp16 per k-step into the
-//                 128B-swizzled K-major layout the MMA reads; then the
-//                 epilogue: TMEM -> registers -> scale -> bf16 -> global.
+//   warps 2..17   dequantizers: two threads per weight row read the packed
+//                 words of one group (uint4) and the group's scale/bias; each
+//                 writes 32 fp16 (one word) per k-step into the 128B-swizzled
+//                 K-major layout the MMA reads; then the epilogue:
+//                 TMEM -> registers -> scale -> bf16 -> global.
 // Stages: 4 x (16 KB x tile + 32 KB weight tile), mbarrier hand-offs.
 // Every wait is bounded (globaltimer); one that runs out sets a device error
 // word and a CTA-wide abort flag so that the other roles stop waiting too.
@@ -49,9 +49,9 @@ constexpr int BM = 128;  // tokens per tile (TMEM lanes)
 constexpr int BN = 256;  // weight rows per tile (MMA N)
 constexpr int BK = 64;   // k per stage (one 128-byte swizzle atom of bf16)
 constexpr int STAGES = 4;
-constexpr int kThreadsWide = 320;  // 10 warps
+constexpr int kThreadsWide = 576;  // 18 warps
 constexpr int kDeqWarp0 = 2;
-constexpr int kDeqThreads = 256;
+constexpr int kDeqThreads = 512;   // two threads per weight row: one word each per k-step
 constexpr uint32_t A_BYTES = BM * BK * 2;  // 16 KB
 constexpr uint32_t B_BYTES = BN * BK * 2;  // 32 KB
 constexpr uint32_t kTmemCols = 256;
@@ -263,8 +263,9 @@ wide_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint32_t *__restri
       umma_commit(&sh->accum_full);  // arrives once every issued MMA has completed
     }
   } else {
-    // ---------------- dequantizers: thread d owns weight row n0 + d
-    const int d = tid - kDeqWarp0 * 32;
+    // ---------------- dequantizers: threads 2r and 2r+1 own weight row n0 + r;
+    //                  thread 2r+wh expands word wh of each 64-k stage
+    const int d = (tid - kDeqWarp0 * 32) >> 1, wh = tid & 1;
     const int n = n0 + d;
     const bool ok_row = n < N;
     const int wpr = K / 32, G = K / 128;
@@ -289,35 +290,38 @@ wide_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint32_t *__restri
       const uint32_t lo16 = __half_as_ushort(__float2half_rn(bi));
       const uint32_t hi16 = __half_as_ushort(__float2half_rn(__fadd_rn(sc, bi)));
       const uint32_t lo2 = lo16 | (lo16 << 16), hi2 = hi16 | (hi16 << 16);
+      // both k-steps of the group: wait for both stages, write both, then one
+      // proxy fence and the two arrivals (halves the fence/arrive hand-offs)
+      const int ks0 = 2 * g;
+      const int s0 = ks0 % STAGES, s1 = (ks0 + 1) % STAGES;
+      const uint32_t ph0 = (uint32_t)(ks0 / STAGES) & 1u, ph1 = (uint32_t)((ks0 + 1) / STAGES) & 1u;
+      // one lane waits, the warp follows its verdict (keeps the warp converged)
+      int okw = 0;
+      if (lane == 0)
+        okw = alive && mbar_wait(&sh->empty[s0], ph0 ^ 1u, sh) && mbar_wait(&sh->empty[s1], ph1 ^ 1u, sh);
+      okw = __shfl_sync(0xffffffffu, okw, 0);
+      if (!okw) {
+        alive = false;
+        return;
+      }
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const int ks = 2 * g + h;
-        const int s = ks % STAGES;
-        const uint32_t ph = (uint32_t)(ks / STAGES) & 1u;
-        // one lane waits, the warp follows its verdict (keeps the warp converged)
-        int okw = 0;
-        if (lane == 0) okw = alive && mbar_wait(&sh->empty[s], ph ^ 1u, sh);
-        okw = __shfl_sync(0xffffffffu, okw, 0);
-        if (!okw) {
-          alive = false;
-          return;
-        }
-        unsigned char *rowp = sb + s * B_BYTES + d * 128;
+        unsigned char *rowp = sb + (h == 0 ? s0 : s1) * B_BYTES + d * 128;
+        const uint32_t word = h == 0 ? (wh == 0 ? gd.w.x : gd.w.y) : (wh == 0 ? gd.w.z : gd.w.w);
+        uint32_t out[16];
+        expand_word(word, lo2, hi2, out);
 #pragma unroll
-        for (int wi = 0; wi < 2; ++wi) {
-          const uint32_t word = h == 0 ? (wi == 0 ? gd.w.x : gd.w.y) : (wi == 0 ? gd.w.z : gd.w.w);
-          uint32_t out[16];
-          expand_word(word, lo2, hi2, out);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int c = wi * 4 + q;  // 16-byte chunk: k = 8c .. 8c+7 of this stage
-            *reinterpret_cast<uint4 *>(rowp + ((c ^ (d & 7)) << 4)) =
-                make_uint4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
-          }
+        for (int q = 0; q < 4; ++q) {
+          const int c = wh * 4 + q;  // 16-byte chunk: k = 8c .. 8c+7 of this stage
+          *reinterpret_cast<uint4 *>(rowp + ((c ^ (d & 7)) << 4)) =
+              make_uint4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh->full_b[s]);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&sh->full_b[s0]);
+        mbar_arrive(&sh->full_b[s1]);
       }
     };
     GroupData r0, r1, r2;
@@ -341,12 +345,12 @@ wide_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint32_t *__restri
     if (acc_ok) {
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       asm volatile("griddepcontrol.wait;" ::: "memory");  // inv_scale comes from the prep kernel
-      const int quarter = warp & 3, half = (warp - kDeqWarp0) >> 2;
+      const int quarter = warp & 3, part = (warp - kDeqWarp0) >> 2;  // 4 column quarters
       const int m = m0 + 32 * quarter + lane;
       const float rs = m < M ? inv_scale[m] : 0.f;
 #pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        const int col = half * 128 + cc * 32;
+      for (int cc = 0; cc < 2; ++cc) {
+        const int col = part * 64 + cc * 32;
         uint32_t v[32];
         const uint32_t taddr = tmem_d + ((uint32_t)(32 * quarter) << 16) + (uint32_t)col;
         asm volatile(
