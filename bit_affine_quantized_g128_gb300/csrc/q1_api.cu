@@ -125,6 +125,7 @@ q1_status q1_dequantize(const q1_weight *W, q1_dtype out_t, void *out, q1_stream
 q1_status q1_qmv(const q1_weight *W, const void *x, q1_dtype dtype, void *y, q1_stream stream) {
   q1_status s = matmul_common(W, x, 1, dtype, y);
   if (s != Q1_OK) return s;
+  if (W->K > q1::kNarrowMaxK) return Q1_ERR_SHAPE;
   return cuda_status(q1::launch_narrow(q1::view(W), x, 1, y, (cudaStream_t)stream, true));
 }
 
@@ -132,7 +133,7 @@ q1_status q1_qmm_narrow(const q1_weight *W, const void *x, int64_t M, q1_dtype d
                         q1_stream stream) {
   q1_status s = matmul_common(W, x, M, dtype, y);
   if (s != Q1_OK) return s;
-  if (M > q1::kNarrowMaxM) return Q1_ERR_SHAPE;
+  if (M > q1::kNarrowMaxM || W->K > q1::kNarrowMaxK) return Q1_ERR_SHAPE;
   return cuda_status(q1::launch_narrow(q1::view(W), x, M, y, (cudaStream_t)stream, true));
 }
 
@@ -146,7 +147,7 @@ q1_status q1_qmm(const q1_weight *W, const void *x, int64_t M, q1_dtype dtype, v
                  void *workspace, size_t workspace_bytes, q1_stream stream) {
   q1_status s = matmul_common(W, x, M, dtype, y);
   if (s != Q1_OK) return s;
-  if (M <= g_max_rows.load())
+  if (M <= g_max_rows.load() && W->K <= q1::kNarrowMaxK)
     return cuda_status(q1::launch_narrow(q1::view(W), x, M, y, (cudaStream_t)stream, true));
   s = check_ws(workspace, workspace_bytes, q1::wide_workspace_bytes(M, W->K));
   if (s != Q1_OK) return s;
@@ -187,6 +188,7 @@ q1_status q1_ffn_fused(const q1_weight *gate, const q1_weight *up, const q1_weig
   if (M < 1 || M > q1::kNarrowMaxM) return Q1_ERR_SHAPE;
   const int64_t D = gate->K, F = gate->N;
   if (up->K != D || up->N != F || down->K != F || down->N != D) return Q1_ERR_SHAPE;
+  if (D > q1::kNarrowMaxK || F > q1::kNarrowMaxK) return Q1_ERR_SHAPE;
   if (!aligned(x, 16) || !aligned(y, 16)) return Q1_ERR_ALIGN;
   s = check_ws(workspace, workspace_bytes, q1_ffn_workspace_size(M, D, F));
   if (s != Q1_OK) return s;

@@ -12,6 +12,8 @@ namespace q1 {
 constexpr int kGroup = 128;      // weights per scale/bias group
 constexpr int kWordBits = 32;    // weights per packed word
 constexpr int kNarrowMaxM = 8;   // token rows of one mma.sync n8 tile
+// K of the narrow kernel: a cluster of at most 8 CTAs x 10 span warps x 512 k
+constexpr int64_t kNarrowMaxK = 8 * 10 * 512;
 
 // Metadata pointers resolved for a launch.
 struct WeightView {

@@ -22,30 +22,39 @@
 //   p = 7     : bits 7, 23 (exponent lsb) -> 0.5 + 0.5 q
 //   p = 8..14 : bits p-8, p+8 of word>>8  -> 1 + 2^(p-15) q
 //   p = 15    : bits 15, 31 (sign)        -> 1 - 2 q
-// The activations are pre-scaled by 1/d_p (a power of two, exact in bf16) and
-// permuted into the same (p, p+16) pairs in shared memory by each CTA for its
-// own K-slice, so one group of 128 k gives D = C_g + S1 with
+// The activations are scaled by 1/d_p (a power of two: exact) and paired as
+// (x_p, x_{p+16}), so one group of 128 k gives D = C_g + S1 with
 // S1 = sum_{k in g} q_k x_k and C_g = sum a_p x'_k.  Per group and row:
-//   symmetric: y += s * (D - C_g - Sx_g / 2)
+//   symmetric: y += s * (D - E_g),  E_g = C_g + Sx_g / 2
 //   affine   : y += s * (D - C_g) + b * Sx_g         (Sx_g = sum_{k in g} x_k)
-// which is w = s*q + b summed over the group.
+// which is w = s*q + b summed over the group.  C_g and Sx_g / 2 come from the
+// tensor cores too: one MMA chain per group whose A rows 0..7 hold the a_p
+// pattern and rows 8..15 hold d_p / 2 (all exact in bf16); -E_g (or -C_g) is
+// then the accumulator that the group's MMA chain starts from.
 //
-// Work decomposition (persistent: one 16-warp CTA per SM, all resident):
-//   * a thread-block cluster of KS CTAs splits K into KS slices (CTA rank r
-//     owns groups [G r / KS, G (r+1) / KS) and keeps their activation
-//     fragments in shared memory for the whole kernel);
-//   * the clusters split the 16-row tiles of W into contiguous ranges;
-//   * a tile is 16 rows x 4 groups (1 KB of packed words).  Inside a CTA the
-//     tiles of the current round are cut into 16 equal contiguous ranges, one
-//     per warp; each warp streams its tiles through its own ring of shared
-//     memory slots filled by TMA (64-byte swizzle: conflict-free reads), so
-//     several kilobytes per warp are always in flight;
-//   * partial sums go to shared memory, are combined over warps in warp
-//     order, then over the cluster's CTAs in rank order through distributed
-//     shared memory (deterministic: fixed summation order, no atomics).
-// One pair of cluster barriers per round; most shapes need a single round.
+// Work decomposition (one CTA per SM: up to 10 consumer warps and one
+// producer warp):
+//   * K is cut into spans of 4 groups (512 k).  A thread-block cluster of KS
+//     CTAs splits the spans into KS contiguous slices; inside a CTA every
+//     consumer warp owns one span for the whole launch and keeps its
+//     activation fragments (64 registers) and the span's C/E terms in
+//     registers;
+//   * the clusters split the 16-row tiles of W into contiguous ranges; the
+//     R warps that own the same span take every R-th row tile of the range;
+//   * the producer warp streams the CTA's row tiles, in order, through a
+//     ring of row-tile slots: per slot one 1 KB TMA box per span (16 rows x
+//     16 words, 64-byte swizzle: conflict-free reads) and one box with the
+//     16 rows' scales (and biases) of the whole K-slice, all completing on
+//     the slot's mbarrier; the consumers hand the slot back through a second
+//     mbarrier;
+//   * the four groups' MMA chains of a tile are interleaved, so that a warp
+//     always has four independent MMAs in flight;
+//   * per-tile partial sums go to shared memory and are combined over the
+//     spans in a fixed order, then over the cluster's CTAs in rank order
+//     through distributed shared memory (deterministic, no atomics).
 // Every mbarrier wait is bounded: one that runs out sets a device error word.
 #include <cooperative_groups.h>
+#include <cstring>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -61,31 +70,45 @@ __device__ unsigned int g_narrow_err = 0;
 
 namespace {
 
-constexpr int kWarps = 16;
-constexpr int kThreads = kWarps * 32;
-constexpr int kQuad = 4;              // groups per tile
-constexpr int kTileBytes = 16 * 64;   // 16 rows x 16 words
-constexpr int kXsThreadStride = 80;   // bytes per (group, token, quad-thread) block of x'
+constexpr int kMaxWarps = 10;                     // consumer warps
+constexpr int kMaxThreads = (kMaxWarps + 1) * 32;  // + the producer warp
+constexpr int kQuad = 4;                          // groups per span
+constexpr int kTileBytes = 16 * 64;               // 16 rows x 16 words
 constexpr int kSmemMax = 227 * 1024;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
 __host__ __device__ constexpr int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
-// 1 / d_p and a_p of the bit-position encoding above.
-__device__ __forceinline__ float inv_d(int p) {
-  return p < 7 ? (float)(1 << (7 - p)) : (p == 7 ? 2.0f : (p < 15 ? (float)(1 << (15 - p)) : -0.5f));
+// bf16 bit patterns (both halves) of the encoding constants
+constexpr uint32_t bf16_pow2(int e) { return (uint32_t)(e + 127) << 7; }
+constexpr uint32_t dup2(uint32_t h) { return h | (h << 16); }
+constexpr uint32_t inv_d_bits(int p) {  // 1 / d_p
+  return dup2(p < 7 ? bf16_pow2(7 - p)
+                    : p == 7 ? bf16_pow2(1) : p < 15 ? bf16_pow2(15 - p) : (0x8000u | bf16_pow2(-1)));
 }
-__device__ __forceinline__ float a_of(int p) { return p == 7 ? 0.5f : 1.0f; }
+constexpr uint32_t a_bits(int p) { return dup2(p == 7 ? bf16_pow2(-1) : bf16_pow2(0)); }  // a_p
+constexpr uint32_t halfd_bits(int p) {                                                   // d_p / 2
+  return dup2(p < 7 ? bf16_pow2(p - 8)
+                    : p == 7 ? bf16_pow2(-2) : p < 15 ? bf16_pow2(p - 16) : (0x8000u | bf16_pow2(0)));
+}
 
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4],
-                                               uint32_t b0, uint32_t b1) {
+__device__ __forceinline__ void mma_acc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
   // not volatile: no side effects, so the compiler may interleave the
   // independent MMA chains of a tile's four groups
-  asm(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
       "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// first MMA of a chain: accumulator input c, output d
+__device__ __forceinline__ void mma_from(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1, const float (&c)[4]) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%11,%12,%13};\n"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]),
+        "f"(c[3]));
 }
 
 // Two weights (bits p and p+16 of `src`) -> bf16x2 with base 1.0: one LOP3
@@ -104,6 +127,18 @@ __device__ __forceinline__ uint32_t pair_reg(uint32_t w, uint32_t w8, uint32_t b
   else return sel<0x80008000u>(w, base);
 }
 
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t s) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(s));
+  return d;
+}
+// bf16x2 a * b, exact for a power-of-two b (the -0 addend keeps signs of zeros)
+__device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(0x80008000u));
+  return d;
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
@@ -112,14 +147,9 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
   return v;
 }
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ float4 lds128f(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
   return v;
 }
 __device__ __forceinline__ unsigned long long globaltimer() {
@@ -157,27 +187,32 @@ __device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity) {
 struct Geo {
   int ks;     // CTAs per cluster (K slices)
   int nclus;  // clusters
+  int qm;     // span slots per CTA (spans of the widest slice)
+  int R;      // consumer warps per span (row-tile interleave)
   int tr;     // virtual row tiles per round
-  int rpw;    // partial slots per warp (row tiles one warp can touch in a round)
-  int ring;   // TMA slots per warp
+  int ring;   // ring slots (row tiles in flight) per CTA
+  int mst;    // tokens stored per partial row (1, 2, 4 or 8)
 };
+
+// metadata row of a slot: the groups of spans (q_lo & ~1) .. q_lo + qm, in
+// whole boxes of 8 groups
+__host__ __device__ inline int meta_groups(int qm) { return (4 * (qm + 1) + 7) / 8 * 8; }
 
 struct SmemLayout {
-  int ring, bars, xs, cs, part, red, meta, total;
+  int ring, meta, bars, part, red, total;
+  int slot_words, slot_meta;  // bytes per ring slot
 };
 
-// qmax: tiles (of 4 groups) per row tile in the widest K-slice; mst: tokens stored
-__host__ __device__ inline SmemLayout smem_layout(int qmax, int mst, int tr, int rpw, int ring) {
+__host__ __device__ inline SmemLayout smem_layout(const Geo &g, bool affine) {
   SmemLayout L;
+  L.slot_words = g.qm * kTileBytes;
+  L.slot_meta = align_up(16 * meta_groups(g.qm) * 2 * (affine ? 2 : 1), 128);
   int off = 0;
-  L.ring = off; off += kWarps * ring * kTileBytes;
-  L.bars = off; off += align_up(kWarps * ring * 8, 128);
-  // x' for qmax*4 groups x mst tokens, then one zero block (lanes with no token)
-  L.xs = off; off += align_up((qmax * kQuad * mst + 1) * 4 * kXsThreadStride, 128);
-  L.cs = off; off += align_up(qmax * kQuad * 8 * 8, 128);
-  L.part = off; off += kWarps * rpw * 16 * 8 * 4;
-  L.red = off; off += tr * 16 * 8 * 4;
-  L.meta = off; off += align_up((kWarps + tr) * 4, 128);
+  L.ring = off; off += g.ring * L.slot_words;
+  L.meta = off; off += g.ring * L.slot_meta;
+  L.bars = off; off += align_up(2 * g.ring * 8, 128);
+  L.part = off; off += g.tr * g.qm * 16 * g.mst * 4;
+  L.red = off; off += g.ks > 1 ? g.tr * 16 * g.mst * 4 : 0;
   L.total = off + 1024;  // slack for aligning the dynamic shared memory base
   return L;
 }
@@ -193,384 +228,357 @@ struct NarrowArgs {
   Geo geo;
 };
 
-// Start of warp w's contiguous tile range when U tiles are cut into 16.
-__host__ __device__ __forceinline__ int range_start(int U, int w) { return (U * w) / kWarps; }
-// The warp whose range holds tile X (the last warp whose range starts at or before X).
-__device__ __forceinline__ int warp_of_tile(int X, int U) {
-  int w = (kWarps * (X + 1) + U - 1) / U - 1;
-  return w < 0 ? 0 : (w > kWarps - 1 ? kWarps - 1 : w);
+// Tensor maps of the (up to two) matrices: packed words, scales, biases.
+struct Maps {
+  CUtensorMap w[2], s[2], b[2];
+};
+
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void consumer_sync(int nthreads) {
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }
 
-template <int NMAT, bool AFFINE>
-__global__ void __launch_bounds__(kThreads, 1)
-narrow_kernel(const __grid_constant__ CUtensorMap tm0, const __grid_constant__ CUtensorMap tm1,
-              NarrowArgs a) {
+// One CTA: NC = qm * R consumer warps and one producer warp (the last).
+// The producer streams the CTA's row tiles in order through a ring of
+// row-tile slots: per slot one 1 KB TMA box per span of the CTA (16 rows x
+// 16 words, 64-byte swizzle) and the rows' metadata.  Consumer warp
+// (qi, ri) owns span q_lo + qi and takes the row tiles ri, ri + R, ... of
+// each round.
+// FASTMETA: G % 8 == 0 and 16-byte aligned metadata, so the scales (and
+// biases) come as one TMA box of meta_groups(qm) groups x 16 rows; otherwise
+// the producer's lanes load them (zero past K) and store them before their
+// arrivals.  Either way a slot's metadata is [16 rows][meta_groups] fp16
+// starting at group 4 (q_lo & ~1).
+template <int NMAT, bool AFFINE, bool FASTMETA>
+__global__ void __launch_bounds__(kMaxThreads, 1)
+narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  // TMA with the 64-byte swizzle wants 512-byte aligned slots: align the base
+  // TMA with the 64-byte swizzle wants 512-byte aligned boxes: align the base
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   cg::cluster_group cluster = cg::this_cluster();
 
   const int M = a.M, K = a.K, G = K / 128;
+  const int64_t N = a.N;
   const Geo geo = a.geo;
-  const int KS = geo.ks, RING = geo.ring;
-  const int rank = (int)cluster.block_rank();
-  const int clus = blockIdx.x / KS;
-  const int g0 = (int)(((int64_t)rank * G) / KS), g1 = (int)(((int64_t)(rank + 1) * G) / KS);
-  const int KSL = g1 - g0;
-  const int Q = (KSL + kQuad - 1) / kQuad;  // tiles per row tile in this slice
-  const int qmax = ((G + KS - 1) / KS + kQuad - 1) / kQuad;
-  const SmemLayout L = smem_layout(qmax, M, geo.tr, geo.rpw, RING);
-  unsigned char *ring = smem + L.ring;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bars);
-  unsigned char *xs = smem + L.xs;
-  float2 *css = reinterpret_cast<float2 *>(smem + L.cs);  // [j][token]: (C or E, Sx)
-  float *part = reinterpret_cast<float *>(smem + L.part);
-  float *red = reinterpret_cast<float *>(smem + L.red);
-  int *meta = reinterpret_cast<int *>(smem + L.meta);
+  const int KS = geo.ks, RING = geo.ring, QM = geo.qm, R = geo.R, TR = geo.tr, MST = geo.mst;
+  const SmemLayout L = smem_layout(geo, AFFINE);
+  const int NC = QM * R;                    // consumer warps
+  const int MROW = meta_groups(QM) * 2;     // bytes per metadata row
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, t = lane & 3;
-  const int NT = (int)((a.N + 15) / 16);
-  const int last_row = (int)(a.N - 1);
-  // this cluster's virtual row tiles (matrix = v % NMAT, row tile = v / NMAT)
+  const int rank = (int)cluster.block_rank();
+  const int clus = blockIdx.x / KS;
+  const int QK = (G + kQuad - 1) / kQuad;  // spans in K
+  const int q_lo = (int)(((int64_t)QK * rank) / KS), q_hi = (int)(((int64_t)QK * (rank + 1)) / KS);
+  const int QS = q_hi - q_lo;               // spans of this CTA
+  const int q_base = q_lo & ~1;             // first span of the metadata rows
+  const int NT = (int)((N + 15) / 16);
   const int v_lo = (int)(((int64_t)NT * clus) / geo.nclus) * NMAT;
   const int v_hi = (int)(((int64_t)NT * (clus + 1)) / geo.nclus) * NMAT;
+
+  const uint32_t ring_s = smem_u32(smem + L.ring);
+  const uint32_t meta_s = smem_u32(smem + L.meta);
+  const uint32_t full_s = smem_u32(smem + L.bars);  // full[RING], then empty[RING]
+  const uint32_t empty_s = full_s + 8 * RING;
+  float *part = reinterpret_cast<float *>(smem + L.part);
+  float *red = reinterpret_cast<float *>(smem + L.red);
+
+  if (warp == NC && lane < RING) {
+    // full: the producer's expect_tx (plus, without metadata TMA, the 32
+    // producer lanes' arrivals); empty: one arrival per consumer warp
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(full_s + 8 * lane), "r"(FASTMETA ? 1 : 33)
+                 : "memory");
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(empty_s + 8 * lane), "r"(QS) : "memory");
+  }
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  __syncthreads();
+
+  // the next kernel of a dependent chain may start streaming its weights now
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  if (warp == NC) {
+    // ================= producer =================
+    const int nv = v_hi - v_lo;
+    int j = 0;
+    uint32_t slot = 0, ph = 0;
+    auto issue_next = [&]() {
+      const int v = v_lo + j;
+      const int mat = NMAT == 2 ? (v & 1) : 0;
+      const int rt = NMAT == 2 ? (v >> 1) : v;
+      const bool has_b = AFFINE && (mat ? a.b[1] : a.b[0]) != nullptr;
+      const uint32_t fb = full_s + 8 * slot;
+      // the slot's previous tile has been read by its consumer warps
+      mbar_wait(empty_s + 8 * slot, ph ^ 1u);
+      const uint32_t mdst = meta_s + slot * L.slot_meta;
+      if (lane == 0) {
+        const uint32_t bytes =
+            QS * kTileBytes + (FASTMETA ? (uint32_t)(16 * MROW) * (has_b ? 2u : 1u) : 0u);
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb), "r"(bytes) : "memory");
+        const CUtensorMap *wm = mat ? &maps.w[1] : &maps.w[0];
+        const uint32_t wdst = ring_s + slot * L.slot_words;
+        for (int qs = 0; qs < QS; ++qs) tma_2d(wdst + qs * kTileBytes, wm, (q_lo + qs) * 16, rt * 16, fb);
+        if (FASTMETA) {
+          tma_2d(mdst, mat ? &maps.s[1] : &maps.s[0], q_base * kQuad, rt * 16, fb);
+          if (has_b) tma_2d(mdst + 16 * MROW, mat ? &maps.b[1] : &maps.b[0], q_base * kQuad, rt * 16, fb);
+        }
+      }
+      if (!FASTMETA) {
+        const uint16_t *sp = mat ? a.s[1] : a.s[0];
+        const uint16_t *bp = mat ? a.b[1] : a.b[0];
+        for (int e = lane; e < 16 * QS * (has_b ? 2 : 1); e += 32) {
+          const int r = e & 15, qs = (e >> 4) % QS, isb = (e >> 4) / QS;
+          const int64_t row = (int64_t)rt * 16 + r;
+          const int s = q_lo + qs;
+          const uint16_t *src = (isb ? bp : sp) + row * G + s * kQuad;
+          uint32_t h[kQuad];
+#pragma unroll
+          for (int u = 0; u < kQuad; ++u) h[u] = (row < N && s * kQuad + u < G) ? (uint32_t)__ldg(src + u) : 0u;
+          asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(mdst + isb * 16 * MROW + r * MROW +
+                                                              (s - q_base) * 8),
+                       "r"(h[0] | (h[1] << 16)), "r"(h[2] | (h[3] << 16))
+                       : "memory");
+        }
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(fb) : "memory");
+      }
+      __syncwarp();
+      ++j;
+      if (++slot == (uint32_t)RING) {
+        slot = 0;
+        ph ^= 1u;
+      }
+    };
+    for (int r = 0, rb = v_lo; rb < v_hi; ++r, rb += TR) {
+      // this round's tiles and the next round's first RING: their slots were
+      // last used by tiles of this round or earlier, which the consumers
+      // finish before the round's barriers
+      const int target = min(nv, (r + 1) * TR + RING);
+      while (j < target) issue_next();
+      if (KS > 1) {
+        cluster.sync();
+        cluster.sync();
+      }
+    }
+    return;
+  }
+
+  // ================= consumers =================
+  const int qi = warp % QM, ri = warp / QM;
+  const bool active = qi < QS;
+  const int span = q_lo + qi;  // groups 4 span .. 4 span + 3
+  const int nthreads = NC * 32;
+
+  // x may be the output of the preceding kernel: wait for it before reading
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  // ---- activation fragments of this warp's span (token gid, word t of each
+  //      group) and the per-group accumulator seeds
+  uint32_t bfr[kQuad][16];
+  float seed[kQuad][4];
+  float sx[kQuad][2];
+  if (active) {
+#pragma unroll
+    for (int u = 0; u < kQuad; ++u) {
+      const int g = span * kQuad + u;
+      uint32_t xv[16];
+      if (gid < M && g < G) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(a.x + (size_t)gid * K + (size_t)g * 128 + 32 * t);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 v = __ldg(src + q);
+          xv[4 * q] = v.x; xv[4 * q + 1] = v.y; xv[4 * q + 2] = v.z; xv[4 * q + 3] = v.w;
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 16; ++q) xv[q] = 0u;
+      }
+#define Q1_PAIR(P) \
+  bfr[u][P] = bmul2(prmt(xv[(P) >> 1], xv[8 + ((P) >> 1)], ((P) & 1) ? 0x7632u : 0x5410u), inv_d_bits(P));
+      Q1_PAIR(0) Q1_PAIR(1) Q1_PAIR(2) Q1_PAIR(3) Q1_PAIR(4) Q1_PAIR(5) Q1_PAIR(6) Q1_PAIR(7)
+      Q1_PAIR(8) Q1_PAIR(9) Q1_PAIR(10) Q1_PAIR(11) Q1_PAIR(12) Q1_PAIR(13) Q1_PAIR(14) Q1_PAIR(15)
+#undef Q1_PAIR
+      // rows 0..7: C_g = sum a_p x'; rows 8..15: Sx_g / 2 = sum (d_p / 2) x'
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+#define Q1_CE(JJ)                                                                                   \
+  mma_acc(d, a_bits(2 * (JJ)), halfd_bits(2 * (JJ)), a_bits(2 * (JJ) + 1), halfd_bits(2 * (JJ) + 1), \
+          bfr[u][2 * (JJ)], bfr[u][2 * (JJ) + 1]);
+      Q1_CE(0) Q1_CE(1) Q1_CE(2) Q1_CE(3) Q1_CE(4) Q1_CE(5) Q1_CE(6) Q1_CE(7)
+#undef Q1_CE
+      // tokens 2t, 2t+1
+      const float e0 = AFFINE ? d[0] : d[0] + d[2], e1 = AFFINE ? d[1] : d[1] + d[3];
+      seed[u][0] = -e0; seed[u][1] = -e1; seed[u][2] = -e0; seed[u][3] = -e1;
+      sx[u][0] = 2.f * d[2];
+      sx[u][1] = 2.f * d[3];
+    }
+  }
 
   // bf16x2 (1.0, 1.0), kept in one register for every unpack LOP3 (opaque to
   // the compiler, so that it is not re-materialised per instruction)
   uint32_t kbase;
   asm volatile("mov.b32 %0, 0x3F803F80;" : "=r"(kbase));
-
-  unsigned char *my_ring = ring + warp * RING * kTileBytes;
-  uint64_t *my_bars = bars + warp * RING;
-  if (lane < RING) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(my_bars + lane)) : "memory");
-  }
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  __syncwarp();
-
-  int round_v = v_lo;
-  int T = min(geo.tr, v_hi - round_v);
-  int U = T * Q;
-  int ua = range_start(U, warp), ub = range_start(U, warp + 1);
-  uint32_t issued = 0;  // tiles this warp consumed in earlier rounds (ring phase)
-
-  // lane 0: TMA of the round's tile (row tile lv, quad q) into the slot of
-  // sequence number `seq`
-  auto issue = [&](int lv, int q, uint32_t seq) {
-    const int vt = round_v + lv;
-    const int mat = NMAT == 2 ? (vt & 1) : 0;
-    const int rt = NMAT == 2 ? (vt >> 1) : vt;
-    const int slot = (int)(seq % (uint32_t)RING);
-    const uint32_t bar = smem_u32(my_bars + slot);
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(kTileBytes)
-                 : "memory");
-    const CUtensorMap *tm = mat == 0 ? &tm0 : &tm1;
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-        ::"r"(smem_u32(my_ring + slot * kTileBytes)), "l"(tm), "r"((g0 + q * kQuad) * 4), "r"(rt * 16),
-        "r"(bar)
-        : "memory");
-  };
-  auto prime = [&]() {  // first RING tiles of this warp's range
-    if (lane == 0) {
-      int lv = ua / Q, q = ua - (ua / Q) * Q;
-      for (int i = 0; i < RING && ua + i < ub; ++i) {
-        issue(lv, q, issued + (uint32_t)i);
-        if (++q == Q) { q = 0; ++lv; }
-      }
-    }
-  };
-  prime();
-
-  // the next kernel of a dependent chain may start streaming its weights now
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  // x may be the output of the preceding kernel: wait for it before reading
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-
-  // ---- activation fragments of this CTA's K-slice -> shared memory, padded
-  //      with zeros to whole tiles, plus the zero block for lanes gid >= M
-  {
-    const int jn = Q * kQuad;
-    const int nitems = jn * M * 4;  // (j, m, t) blocks of 32 k
-    for (int base = 0; base < nitems; base += kThreads) {
-      const int i = base + tid;
-      const bool valid = i < nitems;
-      const int tt = i & 3, jm = i >> 2;
-      const int j = jm / M, m = jm - j * M;
-      float c = 0.f, sx = 0.f;
-      if (valid) {
-        uint32_t pr[16];
-        if (j < KSL) {
-          const uint4 *src =
-              reinterpret_cast<const uint4 *>(a.x + (size_t)m * K + (size_t)(g0 + j) * 128 + 32 * tt);
-          uint32_t xv[16];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 v = __ldg(src + q);
-            xv[4 * q] = v.x; xv[4 * q + 1] = v.y; xv[4 * q + 2] = v.z; xv[4 * q + 3] = v.w;
-          }
-#pragma unroll
-          for (int p = 0; p < 16; ++p) {
-            // x[p] is half (p & 1) of xv[p >> 1]; x[p+16] likewise in xv[8 + (p >> 1)]
-            const uint32_t lo_bits = (p & 1) ? (xv[p >> 1] >> 16) : (xv[p >> 1] & 0xFFFFu);
-            const uint32_t hi_bits = (p & 1) ? (xv[8 + (p >> 1)] >> 16) : (xv[8 + (p >> 1)] & 0xFFFFu);
-            const float xl = __uint_as_float(lo_bits << 16), xh = __uint_as_float(hi_bits << 16);
-            const float sc = inv_d(p);
-            const float pl = xl * sc, ph = xh * sc;  // exact: power-of-two scaling
-            const __nv_bfloat162 pb = __floats2bfloat162_rn(pl, ph);
-            pr[p] = *reinterpret_cast<const uint32_t *>(&pb);
-            c = fmaf(a_of(p), pl + ph, c);
-            sx += xl + xh;
-          }
-        } else {
-#pragma unroll
-          for (int p = 0; p < 16; ++p) pr[p] = 0u;
-        }
-        uint4 *dst = reinterpret_cast<uint4 *>(xs + ((size_t)jm * 4 + tt) * kXsThreadStride);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pr[4 * q], pr[4 * q + 1], pr[4 * q + 2], pr[4 * q + 3]);
-      }
-      // the four quad blocks of one (j, m) sit in adjacent lanes
-      c += __shfl_xor_sync(0xffffffffu, c, 1);
-      sx += __shfl_xor_sync(0xffffffffu, sx, 1);
-      c += __shfl_xor_sync(0xffffffffu, c, 2);
-      sx += __shfl_xor_sync(0xffffffffu, sx, 2);
-      if (valid && tt == 0) {
-        // symmetric metadata folds the derived bias in: E = C + Sx / 2
-        css[j * 8 + m] = make_float2(AFFINE ? c : fmaf(0.5f, sx, c), sx);
-      }
-    }
-    // zero block, and the (C, Sx) entries of tokens m >= M
-    unsigned char *zb = xs + (size_t)jn * M * 4 * kXsThreadStride;
-    for (int i = tid; i < 4 * kXsThreadStride / 16; i += kThreads)
-      reinterpret_cast<uint4 *>(zb)[i] = make_uint4(0, 0, 0, 0);
-    for (int i = tid; i < jn * 8; i += kThreads)
-      if ((i & 7) >= M) css[i] = make_float2(0.f, 0.f);
-  }
-  __syncthreads();
-
-  // per-lane constants of the compute loop (32-bit shared-memory addresses)
-  const uint32_t xlane = smem_u32(gid < M ? xs + ((size_t)gid * 4 + t) * kXsThreadStride
-                                          : xs + ((size_t)Q * kQuad * M * 4 + t) * kXsThreadStride);
-  const uint32_t xj_stride = gid < M ? (uint32_t)(M * 4 * kXsThreadStride) : 0u;  // per group
-  const uint32_t clane = smem_u32(css + 2 * t);
-  const uint32_t ring_lane = smem_u32(my_ring) + gid * 64 + 4 * t;
-  const uint32_t part_lane = smem_u32(part) + (uint32_t)((gid * 8 + 2 * t) * 4);
   // word offsets of the four groups of a tile under the 64-byte swizzle (rows
   // gid and gid + 8 share it: ((r >> 1) & 3) is the same for both)
   const int swz = (gid >> 1) & 3;
-  uint32_t woff[kQuad];
-#pragma unroll
-  for (int u = 0; u < kQuad; ++u) woff[u] = (uint32_t)((u ^ swz) << 4);
+  const uint32_t wlane = ring_s + qi * kTileBytes + gid * 64 + 4 * t;
+  const uint32_t mlane = meta_s + gid * MROW + (span - q_base) * 8;
 
-  while (true) {
-    // ---- stream this warp's tiles [ua, ub) of the round
-    const int vt_first = round_v + ua / Q;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    // scales (and biases) of one tile's 4 groups, rows gid and gid + 8; groups
-    // past this K-slice (tile padding) read as scale 0
-    auto load_meta = [&](int lv, int q, uint32_t (&sw)[kQuad], uint32_t (&bw)[kQuad]) {
-      const int vt = round_v + lv;
-      const int rt = NMAT == 2 ? (vt >> 1) : vt;
-      const int mat = NMAT == 2 ? (vt & 1) : 0;
-      const int rA = min(rt * 16 + gid, last_row), rB = min(rt * 16 + gid + 8, last_row);
-      const int jb = q * kQuad;
-      const size_t oA = (size_t)rA * G + g0 + jb, oB = (size_t)rB * G + g0 + jb;
-      const uint16_t *pA = (mat == 0 ? a.s[0] : a.s[1]) + oA;
-      const uint16_t *pB = (mat == 0 ? a.s[0] : a.s[1]) + oB;
-      const uint16_t *Bp = mat == 0 ? a.b[0] : a.b[1];
-      if (jb + kQuad <= KSL) {  // whole tile inside the K-slice (all but a slice's last tile)
+  for (int rb = v_lo; rb < v_hi; rb += TR) {
+    const int trc = min(TR, v_hi - rb);
+    if (active && ri < trc) {
+      // ring position of this warp's first tile of the round
+      const int j0 = rb - v_lo + ri;
+      uint32_t slot = (uint32_t)(j0 % RING), ph = (uint32_t)((j0 / RING) & 1);
+      for (int lt = ri; lt < trc; lt += R) {
+        const uint32_t tb = wlane + slot * L.slot_words;
+        const uint32_t mb = mlane + slot * L.slot_meta;
+        // a wait that ran out has set the device error word; the results of
+        // this call are then undefined, but the CTA still reaches its barriers
+        mbar_wait(full_s + 8 * slot, ph);
+        uint32_t wa[kQuad], wb[kQuad];
 #pragma unroll
         for (int u = 0; u < kQuad; ++u) {
-          sw[u] = (uint32_t)__ldg(pA + u) | ((uint32_t)__ldg(pB + u) << 16);
-          if (AFFINE) bw[u] = Bp ? ((uint32_t)__ldg(Bp + oA + u) | ((uint32_t)__ldg(Bp + oB + u) << 16))
-                                 : 0xFFFFFFFFu;  // no stored bias: derive -s/2
+          wa[u] = lds32(tb + ((u ^ swz) << 4));
+          wb[u] = lds32(tb + ((u ^ swz) << 4) + 8 * 64);
         }
-      } else {  // groups past the slice (tile padding) read as scale 0
+        const uint2 sa = lds64(mb), sb = lds64(mb + 8 * MROW);
+        uint2 ba = make_uint2(0, 0), bb = make_uint2(0, 0);
+        const bool has_b = AFFINE && ((NMAT == 2 && ((rb + lt) & 1)) ? a.b[1] : a.b[0]) != nullptr;
+        if (AFFINE && has_b) {
+          ba = lds64(mb + 16 * MROW);
+          bb = lds64(mb + 24 * MROW);
+        }
+        // the slot's data is in registers once the loads complete; release it
+        // after the first use of every loaded value (the unpack below)
+        uint32_t wa8[kQuad], wb8[kQuad];
 #pragma unroll
         for (int u = 0; u < kQuad; ++u) {
-          const bool in = jb + u < KSL;
-          sw[u] = in ? ((uint32_t)__ldg(pA + u) | ((uint32_t)__ldg(pB + u) << 16)) : 0u;
-          if (AFFINE)
-            bw[u] = Bp ? (in ? ((uint32_t)__ldg(Bp + oA + u) | ((uint32_t)__ldg(Bp + oB + u) << 16)) : 0u)
-                       : 0xFFFFFFFFu;
+          wa8[u] = wa[u] >> 8;
+          wb8[u] = wb[u] >> 8;
         }
-      }
-    };
-    auto prefetch_meta_l2 = [&](int lv, int q) {
-      const int vt = round_v + lv;
-      const int rt = NMAT == 2 ? (vt >> 1) : vt;
-      const uint16_t *Sp = (NMAT == 2 && (vt & 1)) ? a.s[1] : a.s[0];
-      const int r = min(rt * 16 + (lane & 15), last_row);
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(Sp + (size_t)r * G + g0 + q * kQuad));
-    };
-    uint32_t sw[kQuad], bw[kQuad], swn[kQuad], bwn[kQuad];
-    // cursors (row tile, quad) of the current tile, the next one, and the one
-    // RING ahead (the refill target), advanced without divisions
-    int lv = ua / Q, q = ua - (ua / Q) * Q;
-    int lv1 = lv, q1 = q;
-    if (++q1 == Q) { q1 = 0; ++lv1; }
-    int lvR = (ua + RING) / Q, qR = (ua + RING) - ((ua + RING) / Q) * Q;
-    int slot = (int)(issued % (uint32_t)RING);
-    uint32_t phase = (issued / (uint32_t)RING) & 1u;
-    if (ua < ub) load_meta(lv, q, sw, bw);
-    for (int tile = ua; tile < ub; ++tile) {
-      const uint32_t seq = issued + (uint32_t)(tile - ua);
-      const int vt = round_v + lv;
-      const int jb = q * kQuad;
-      if (tile + 1 < ub) load_meta(lv1, q1, swn, bwn);
-      if (tile + RING < ub && lane < 16) prefetch_meta_l2(lvR, qR);
-      const uint32_t tb = ring_lane + (uint32_t)(slot * kTileBytes);
-      const uint32_t xb = xlane + (uint32_t)jb * xj_stride;
-      // a wait that ran out has set the device error word; the results of this
-      // call are then undefined, but the CTA still reaches its barriers
-      mbar_wait(smem_u32(my_bars + slot), phase);
+        // four independent chains (one per group), interleaved step by step
+        float d[kQuad][4];
 #pragma unroll
-      for (int u = 0; u < kQuad; ++u) {
-        const int j = jb + u;
-        const uint32_t w0 = lds32(tb + woff[u]);
-        const uint32_t w1 = lds32(tb + woff[u] + 8 * 64);
-        uint32_t bfr[16];
-        const uint32_t xu = xb + (uint32_t)u * xj_stride;
+        for (int u = 0; u < kQuad; ++u)
+          mma_from(d[u], pair_reg<0>(wa[u], wa8[u], kbase), pair_reg<0>(wb[u], wb8[u], kbase),
+                   pair_reg<1>(wa[u], wa8[u], kbase), pair_reg<1>(wb[u], wb8[u], kbase), bfr[u][0], bfr[u][1],
+                   seed[u]);
+#define Q1_MMA(JJ)                                                                                          \
+  _Pragma("unroll") for (int u = 0; u < kQuad; ++u)                                                         \
+      mma_acc(d[u], pair_reg<2 * (JJ)>(wa[u], wa8[u], kbase), pair_reg<2 * (JJ)>(wb[u], wb8[u], kbase),       \
+              pair_reg<2 * (JJ) + 1>(wa[u], wa8[u], kbase), pair_reg<2 * (JJ) + 1>(wb[u], wb8[u], kbase),     \
+              bfr[u][2 * (JJ)], bfr[u][2 * (JJ) + 1]);
+        Q1_MMA(1) Q1_MMA(2) Q1_MMA(3) Q1_MMA(4) Q1_MMA(5) Q1_MMA(6) Q1_MMA(7)
+#undef Q1_MMA
+        float acc[4];
 #pragma unroll
-        for (int qq = 0; qq < 4; ++qq) {
-          uint4 v = lds128(xu + 16 * qq);
-          bfr[4 * qq] = v.x; bfr[4 * qq + 1] = v.y; bfr[4 * qq + 2] = v.z; bfr[4 * qq + 3] = v.w;
-        }
-        const uint32_t w08 = w0 >> 8, w18 = w1 >> 8;
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t af[4];
-#define Q1_MMA_STEP(JJ)                              \
-  af[0] = pair_reg<2 * (JJ)>(w0, w08, kbase);        \
-  af[1] = pair_reg<2 * (JJ)>(w1, w18, kbase);        \
-  af[2] = pair_reg<2 * (JJ) + 1>(w0, w08, kbase);    \
-  af[3] = pair_reg<2 * (JJ) + 1>(w1, w18, kbase);    \
-  mma_bf16_16816(d, af, bfr[2 * (JJ)], bfr[2 * (JJ) + 1]);
-        Q1_MMA_STEP(0) Q1_MMA_STEP(1) Q1_MMA_STEP(2) Q1_MMA_STEP(3)
-        Q1_MMA_STEP(4) Q1_MMA_STEP(5) Q1_MMA_STEP(6) Q1_MMA_STEP(7)
-#undef Q1_MMA_STEP
-        const float4 cc = lds128f(clane + (uint32_t)j * 64);  // (C or E, Sx) of tokens 2t, 2t+1
-        const float sa = __half2float(__ushort_as_half((uint16_t)(sw[u] & 0xFFFFu)));
-        const float sb = __half2float(__ushort_as_half((uint16_t)(sw[u] >> 16)));
-        if (AFFINE) {
-          float ba, bb;
-          if (bw[u] == 0xFFFFFFFFu) {  // matrix without stored biases: symmetric
-            ba = __fmul_rn(-0.5f, sa);
-            bb = __fmul_rn(-0.5f, sb);
+        for (int u = 0; u < kQuad; ++u) {
+          const uint32_t hs_a = (u < 2 ? sa.x : sa.y) >> (16 * (u & 1));
+          const uint32_t hs_b = (u < 2 ? sb.x : sb.y) >> (16 * (u & 1));
+          const float s_a = __half2float(__ushort_as_half((uint16_t)hs_a));
+          const float s_b = __half2float(__ushort_as_half((uint16_t)hs_b));
+          if (u == 0) {
+            acc[0] = s_a * d[u][0]; acc[1] = s_a * d[u][1]; acc[2] = s_b * d[u][2]; acc[3] = s_b * d[u][3];
           } else {
-            ba = __half2float(__ushort_as_half((uint16_t)(bw[u] & 0xFFFFu)));
-            bb = __half2float(__ushort_as_half((uint16_t)(bw[u] >> 16)));
+            acc[0] = fmaf(s_a, d[u][0], acc[0]); acc[1] = fmaf(s_a, d[u][1], acc[1]);
+            acc[2] = fmaf(s_b, d[u][2], acc[2]); acc[3] = fmaf(s_b, d[u][3], acc[3]);
           }
-          acc[0] = fmaf(sa, d[0] - cc.x, fmaf(ba, cc.y, acc[0]));
-          acc[1] = fmaf(sa, d[1] - cc.z, fmaf(ba, cc.w, acc[1]));
-          acc[2] = fmaf(sb, d[2] - cc.x, fmaf(bb, cc.y, acc[2]));
-          acc[3] = fmaf(sb, d[3] - cc.z, fmaf(bb, cc.w, acc[3]));
-        } else {
-          acc[0] = fmaf(sa, d[0] - cc.x, acc[0]);
-          acc[1] = fmaf(sa, d[1] - cc.z, acc[1]);
-          acc[2] = fmaf(sb, d[2] - cc.x, acc[2]);
-          acc[3] = fmaf(sb, d[3] - cc.z, acc[3]);
+          if (AFFINE) {
+            float b_a, b_b;
+            if (has_b) {
+              b_a = __half2float(__ushort_as_half((uint16_t)((u < 2 ? ba.x : ba.y) >> (16 * (u & 1)))));
+              b_b = __half2float(__ushort_as_half((uint16_t)((u < 2 ? bb.x : bb.y) >> (16 * (u & 1)))));
+            } else {  // matrix without stored biases: symmetric
+              b_a = __fmul_rn(-0.5f, s_a);
+              b_b = __fmul_rn(-0.5f, s_b);
+            }
+            acc[0] = fmaf(b_a, sx[u][0], acc[0]); acc[1] = fmaf(b_a, sx[u][1], acc[1]);
+            acc[2] = fmaf(b_b, sx[u][0], acc[2]); acc[3] = fmaf(b_b, sx[u][1], acc[3]);
+          }
+        }
+        // every lane's values are consumed: release the slot to the producer
+        __syncwarp();
+        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(empty_s + 8 * slot) : "memory");
+        // partial sums of this (row tile, span): rows gid, gid + 8; tokens 2t, 2t+1
+        {
+          float *pp = part + ((size_t)(lt * QM + qi) * 16) * MST;
+          if (MST >= 2) {
+            if (2 * t < MST) {
+              const uint32_t p0 = smem_u32(pp + gid * MST + 2 * t);
+              asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(p0), "f"(acc[0]), "f"(acc[1]) : "memory");
+              asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(p0 + 8 * MST * 4), "f"(acc[2]),
+                           "f"(acc[3])
+                           : "memory");
+            }
+          } else if (t == 0) {
+            pp[gid] = acc[0];
+            pp[gid + 8] = acc[2];
+          }
+        }
+        slot += (uint32_t)R;
+        while (slot >= (uint32_t)RING) {
+          slot -= (uint32_t)RING;
+          ph ^= 1u;
         }
       }
-#pragma unroll
-      for (int u = 0; u < kQuad; ++u) {
-        sw[u] = swn[u];
-        if (AFFINE) bw[u] = bwn[u];
-      }
-      // the slot is free once every lane has read it: refill it RING tiles ahead
-      __syncwarp();
-      if (lane == 0 && tile + RING < ub) issue(lvR, qR, seq + (uint32_t)RING);
-      // row tile finished (next tile belongs to another one, or range ends)
-      if (tile + 1 == ub || lv1 != lv) {
-        const uint32_t pp = part_lane + (uint32_t)((warp * geo.rpw + (vt - vt_first)) * 16 * 8 * 4);
-        asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(pp), "f"(acc[0]), "f"(acc[1]) : "memory");
-        asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(pp + 8 * 8 * 4), "f"(acc[2]), "f"(acc[3])
-                     : "memory");
-        acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-      }
-      // advance the cursors and the ring position
-      lv = lv1;
-      q = q1;
-      if (++q1 == Q) { q1 = 0; ++lv1; }
-      if (++qR == Q) { qR = 0; ++lvR; }
-      if (++slot == RING) { slot = 0; phase ^= 1u; }
     }
-    issued += (uint32_t)(ub - ua);
+    consumer_sync(nthreads);
 
-    // ---- the next round's geometry
-    const int next_v = round_v + T;
-    int nT = 0, nU = 0, nua = 0, nub = 0;
-    if (next_v < v_hi) {
-      nT = min(geo.tr, v_hi - next_v);
-      nU = nT * Q;
-      nua = range_start(nU, warp);
-      nub = range_start(nU, warp + 1);
-    }
-    __syncthreads();
-
-    // ---- combine the warps' partials per row tile, in warp order.  The
-    //      contributing warps of row tile lv and each warp's first row tile
-    //      are computed once (meta[]), then every element sums its slots.
-    if (tid < kWarps) {
-      const int a0 = range_start(U, tid), a1 = range_start(U, tid + 1);
-      meta[tid] = a0 < a1 ? a0 / Q : -1;
-    }
-    for (int lv = tid; lv < T; lv += kThreads)
-      meta[kWarps + lv] = warp_of_tile(lv * Q, U) | (warp_of_tile(lv * Q + Q - 1, U) << 8);
-    __syncthreads();
-    for (int i = tid; i < T * 128; i += kThreads) {
-      const int lv = i >> 7, e = i & 127;
-      const int fl = meta[kWarps + lv];
-      float sum = 0.f;
-      for (int w = fl & 0xFF; w <= (fl >> 8); ++w) {
-        const int f = meta[w];
-        if (f < 0) continue;  // empty range: this warp wrote nothing
-        sum += part[((size_t)(w * geo.rpw + (lv - f)) * 16) * 8 + e];
+    // ---- combine the spans' partials of each output, in span order
+    const int npairs = trc / NMAT;
+    if (KS == 1) {
+      const int cnt = npairs * 16 * M;
+      for (int i = tid; i < cnt; i += nthreads) {
+        const int r = i & 15, lp = (i >> 4) % npairs, m = (i >> 4) / npairs;
+        const int lt = lp * NMAT;
+        const int64_t n = (int64_t)((rb + lt) / NMAT) * 16 + r;
+        float v0 = 0.f, v1 = 0.f;
+        for (int q = 0; q < QS; ++q) {
+          v0 += part[((size_t)(lt * QM + q) * 16 + r) * MST + m];
+          if (NMAT == 2) v1 += part[((size_t)((lt + 1) * QM + q) * 16 + r) * MST + m];
+        }
+        if (n < N) {
+          const float o = NMAT == 2 ? v0 / (1.0f + expf(-v0)) * v1 : v0;  // SiLU(gate) * up
+          a.out[(size_t)m * N + n] = __float2bfloat16_rn(o);
+        }
       }
-      red[(size_t)lv * 128 + e] = sum;
-    }
-    cluster.sync();
-
-    // ---- cluster reduction in rank order; rank r finishes 1/KS of the row tiles
-    {
-      int lo, hi;
-      if (NMAT == 2) {  // (gate, up) pairs of one row tile are adjacent: whole pairs per rank
-        const int pp = (T / 2 + KS - 1) / KS;
-        lo = min(T, rank * pp * 2);
-        hi = min(T, lo + pp * 2);
-      } else {
-        const int per = (T + KS - 1) / KS;
-        lo = min(T, rank * per);
-        hi = min(T, lo + per);
+      consumer_sync(nthreads);  // the next round rewrites the partials
+    } else {
+      const int cnt = trc * 16 * M;
+      for (int i = tid; i < cnt; i += nthreads) {
+        const int m = i % M, r = (i / M) & 15, lt = i / (16 * M);
+        float v = 0.f;
+        for (int q = 0; q < QS; ++q) v += part[((size_t)(lt * QM + q) * 16 + r) * MST + m];
+        red[((size_t)lt * 16 + r) * MST + m] = v;
       }
-      const int cnt = ((hi - lo) / NMAT) * 16 * M;
-      for (int i = tid; i < cnt; i += kThreads) {
-        const int lv = lo + (i / (16 * M)) * NMAT, r = (i / M) % 16, m = i % M;
-        const int64_t rt = (round_v + lv) / NMAT;
-        const int64_t n = rt * 16 + r;
-        if (n >= a.N) continue;
+      cluster.sync();
+      // rank k finishes 1/KS of the round's (pairs of) row tiles, summing the
+      // ranks' partials in rank order
+      const int per = (npairs + KS - 1) / KS;
+      const int lo = min(npairs, rank * per), hi = min(npairs, lo + per);
+      const int cnt2 = (hi - lo) * 16 * M;
+      for (int i = tid; i < cnt2; i += nthreads) {
+        const int r = i & 15, lp = lo + (i >> 4) % (hi - lo), m = (i >> 4) / (hi - lo);
+        const int lt = lp * NMAT;
+        const int64_t n = (int64_t)((rb + lt) / NMAT) * 16 + r;
         float v0 = 0.f, v1 = 0.f;
         for (int q = 0; q < KS; ++q) {
           const float *rq = cluster.map_shared_rank(red, q);
-          v0 += rq[(size_t)lv * 128 + r * 8 + m];
-          if (NMAT == 2) v1 += rq[(size_t)(lv + 1) * 128 + r * 8 + m];
+          v0 += rq[((size_t)lt * 16 + r) * MST + m];
+          if (NMAT == 2) v1 += rq[((size_t)(lt + 1) * 16 + r) * MST + m];
         }
-        float o = v0;
-        if (NMAT == 2) o = v0 / (1.0f + expf(-v0)) * v1;  // SiLU(gate) * up
-        a.out[(size_t)m * a.N + n] = __float2bfloat16_rn(o);
+        if (n < N) {
+          const float o = NMAT == 2 ? v0 / (1.0f + expf(-v0)) * v1 : v0;
+          a.out[(size_t)m * N + n] = __float2bfloat16_rn(o);
+        }
       }
+      cluster.sync();  // every rank is done reading this round's partials
     }
-    cluster.sync();  // every rank is done reading this round's partials
-
-    if (next_v >= v_hi) break;
-    round_v = next_v;
-    T = nT;
-    U = nU;
-    ua = nua;
-    ub = nub;
-    prime();
   }
 }
 
@@ -588,14 +596,14 @@ int sm_count_cached() {
   return n;
 }
 
-template <int NMAT, bool AFFINE>
+template <int NMAT, bool AFFINE, bool FASTMETA>
 int max_clusters(int ks) {
   static int cache[9] = {0};
   if (cache[ks]) return cache[ks];
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(ks * 64), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = 96 * 1024;  // residency is bound by one CTA per SM anyway
+  cfg.blockDim = dim3(kMaxThreads, 1, 1);
+  cfg.dynamicSmemBytes = 160 * 1024;  // one CTA per SM
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeClusterDimension;
   attr.val.clusterDim.x = (unsigned)ks;
@@ -604,7 +612,7 @@ int max_clusters(int ks) {
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, narrow_kernel<NMAT, AFFINE>, &cfg) != cudaSuccess || n < 1) {
+  if (cudaOccupancyMaxActiveClusters(&n, narrow_kernel<NMAT, AFFINE, FASTMETA>, &cfg) != cudaSuccess || n < 1) {
     cudaGetLastError();
     n = sm_count_cached() / ks;
   }
@@ -627,7 +635,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // Packed words [N][K/32] as a 2-D uint32 tensor; boxes of 16 words x 16 rows
-// with the 64-byte swizzle; rows >= N and words >= K/32 read as zero.
+// (one span block) with the 64-byte swizzle; rows >= N and words >= K/32
+// read as zero.
 bool make_word_map(CUtensorMap *map, const uint32_t *w, int64_t N, int64_t K) {
   auto encode = encode_fn();
   if (!encode) return false;
@@ -635,81 +644,138 @@ bool make_word_map(CUtensorMap *map, const uint32_t *w, int64_t N, int64_t K) {
   cuuint64_t gstride[1] = {(cuuint64_t)(K / 32) * 4};
   cuuint32_t box[2] = {16, 16};
   cuuint32_t estride[2] = {1, 1};
-  return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t *>(w), gdim, gstride, box,
-                estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t *>(w), gdim, gstride, box, estride,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NMAT, bool AFFINE>
-cudaError_t launch_impl(NarrowArgs args, const uint32_t *w0, const uint32_t *w1, cudaStream_t st,
-                        bool pdl) {
-  auto kern = narrow_kernel<NMAT, AFFINE>;
+// Scales or biases [N][G] fp16 as a 2-D uint16 tensor; boxes of box_groups
+// (a multiple of 8) groups x 16 rows, no swizzle; rows >= N and groups >= G
+// read as zero.  Needs G % 8 == 0 (16-byte rows) and a 16-byte aligned base.
+bool make_meta_map(CUtensorMap *map, const uint16_t *m, int64_t N, int64_t G, int box_groups) {
+  auto encode = encode_fn();
+  if (!encode) return false;
+  cuuint64_t gdim[2] = {(cuuint64_t)G, (cuuint64_t)N};
+  cuuint64_t gstride[1] = {(cuuint64_t)G * 2};
+  cuuint32_t box[2] = {(cuuint32_t)box_groups, 16};
+  cuuint32_t estride[2] = {1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<uint16_t *>(m), gdim, gstride, box, estride,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Pick the geometry: among cluster sizes KS (K slices) whose consumer warps
+// fit, the one with the least estimated work on the busiest SM, in tile
+// units: its tiles (spans x virtual row tiles of the widest cluster range),
+// about 0.7 tile per warp for the activation fragments, the cluster
+// exchange, and the extra rounds when the partial sums do not fit at once.
+template <int NMAT, bool AFFINE, bool FASTMETA>
+bool choose_geo(int64_t N, int K, int M, Geo *out) {
+  const int G = K / 128;
+  const int QK = (G + kQuad - 1) / kQuad;
+  const int NT = (int)((N + 15) / 16);
+  const int mst = M <= 1 ? 1 : (M <= 2 ? 2 : (M <= 4 ? 4 : 8));
+  double best = -1.0;
+  for (int ks = 1; ks <= 8; ks *= 2) {
+    if (ks > QK) break;
+    const int qm = (QK + ks - 1) / ks;
+    if (qm > kMaxWarps) continue;
+    int nclus = max_clusters<NMAT, AFFINE, FASTMETA>(ks);
+    if (nclus > NT) nclus = NT;
+    const int tv = ((NT + nclus - 1) / nclus) * NMAT;  // virtual row tiles of the widest range
+    int R = kMaxWarps / qm;
+    if (R > tv) R = tv;
+    if (R < 1) R = 1;
+    const int W = qm * R;
+    // ring: row tiles in flight; at least R + 1 so that every consumer warp
+    // can have its next tile loading
+    int ring = tv < 8 ? tv : 8;
+    if (ring < R + 1) ring = R + 1 < tv ? R + 1 : tv;
+    if (ring < 2) ring = 2;
+    Geo g{ks, nclus, qm, R, tv, ring, mst};
+    // shrink the round, then the ring, until shared memory fits
+    while (smem_layout(g, AFFINE).total > kSmemMax) {
+      if (g.tr > 16 * NMAT) {
+        g.tr = (g.tr / 2 / NMAT) * NMAT;
+      } else if (g.ring > 3 && g.ring > R + 1) {
+        --g.ring;
+      } else if (g.tr > NMAT) {
+        g.tr = (g.tr / 2 / NMAT) * NMAT;
+        if (g.tr < NMAT) g.tr = NMAT;
+      } else if (g.ring > 2) {
+        --g.ring;
+      } else {
+        break;
+      }
+    }
+    if (smem_layout(g, AFFINE).total > kSmemMax) continue;
+    // the producer refills a slot only after its tile is read: with R warps
+    // per span, a ring shorter than R + 1 could starve a warp
+    if (g.ring < (R + 1 < tv ? R + 1 : tv)) continue;
+    const int rounds = (tv + g.tr - 1) / g.tr;
+    double tiles = (double)qm * tv;
+    if (W < 8) tiles *= 8.0 / W;  // too few warps to keep the pipes busy
+    const double cost = tiles + 0.7 * W + (ks > 1 ? 20.0 : 0.0) + 20.0 * (rounds - 1);
+    if (best < 0 || cost < best) {
+      best = cost;
+      *out = g;
+    }
+  }
+  return best >= 0;
+}
+
+template <int NMAT, bool AFFINE, bool FASTMETA>
+cudaError_t launch_impl(NarrowArgs args, const uint32_t *w0, const uint32_t *w1, cudaStream_t st, bool pdl) {
+  auto kern = narrow_kernel<NMAT, AFFINE, FASTMETA>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  CUtensorMap tm0, tm1;
-  if (!make_word_map(&tm0, w0, args.N, args.K)) return cudaErrorInvalidValue;
-  if (!make_word_map(&tm1, w1, args.N, args.K)) return cudaErrorInvalidValue;
-  const int G = args.K / 128;
-  const int M = args.M;
-  const int NT = (int)((args.N + 15) / 16);
-  // Pick the cluster size (K slices) that minimises the tiles of the busiest
-  // CTA, ceil(row tiles per cluster) x ceil(tiles per slice), among those
-  // whose shared memory fits; for it, the deepest TMA ring that fits.
-  Geo best{};
-  long best_cost = -1;
-  for (int ks = 1; ks <= 8; ks *= 2) {
-    if (ks > G) break;
-    int nclus = max_clusters<NMAT, AFFINE>(ks);
-    if (nclus > NT) nclus = NT;
-    const int kslmax = (G + ks - 1) / ks, kslmin = G / ks;
-    const int qmax = (kslmax + kQuad - 1) / kQuad, qmin = (kslmin + kQuad - 1) / kQuad;
-    const int vmax = ((NT + nclus - 1) / nclus) * NMAT;
-    for (int ring = 8; ring >= 3; --ring) {
-      int tr = vmax, rpw = 0;
-      bool ok = false;
-      for (;;) {
-        const int upw = (tr * qmax + kWarps - 1) / kWarps;  // tiles per warp, at most
-        rpw = (upw + qmin - 1) / qmin + 1;
-        if (smem_layout(qmax, M, tr, rpw, ring).total <= kSmemMax) { ok = true; break; }
-        if (tr <= NMAT) break;
-        tr = tr / 2;
-        if (NMAT == 2) tr &= ~1;
-        if (tr < NMAT) tr = NMAT;
-      }
-      if (!ok) continue;
-      const int rounds = (vmax + tr - 1) / tr;
-      // tiles of the busiest CTA, a round's two cluster barriers, and a shallow ring
-      const long cost = (long)vmax * qmax * 4 + (long)rounds * 256 + (8 - ring) * 8;
-      if (best_cost < 0 || cost < best_cost) {
-        best_cost = cost;
-        best = Geo{ks, nclus, tr, rpw, ring};
-      }
-      break;  // deepest ring that fits for this ks
+  Geo g;
+  if (!choose_geo<NMAT, AFFINE, FASTMETA>(args.N, args.K, args.M, &g)) return cudaErrorInvalidConfiguration;
+  args.geo = g;
+  Maps maps;
+  memset(&maps, 0, sizeof(maps));
+  if (!make_word_map(&maps.w[0], w0, args.N, args.K)) return cudaErrorInvalidValue;
+  if (!make_word_map(&maps.w[1], w1, args.N, args.K)) return cudaErrorInvalidValue;
+  if (FASTMETA) {
+    const int64_t G = args.K / 128;
+    for (int i = 0; i < 2; ++i) {
+      if (!make_meta_map(&maps.s[i], args.s[i], args.N, G, meta_groups(g.qm))) return cudaErrorInvalidValue;
+      if (args.b[i] && !make_meta_map(&maps.b[i], args.b[i], args.N, G, meta_groups(g.qm)))
+        return cudaErrorInvalidValue;
     }
   }
-  if (best_cost < 0) return cudaErrorInvalidConfiguration;
-  args.geo = best;
-  const int qmax = ((G + best.ks - 1) / best.ks + kQuad - 1) / kQuad;
-  const SmemLayout L = smem_layout(qmax, M, best.tr, best.rpw, best.ring);
+  const SmemLayout L = smem_layout(g, AFFINE);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(best.nclus * best.ks), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.gridDim = dim3((unsigned)(g.nclus * g.ks), 1, 1);
+  cfg.blockDim = dim3((unsigned)((g.qm * g.R + 1) * 32), 1, 1);
   cfg.dynamicSmemBytes = (size_t)L.total;
   cfg.stream = st;
   cudaLaunchAttribute attrs[2];
   attrs[0].id = cudaLaunchAttributeClusterDimension;
-  attrs[0].val.clusterDim.x = (unsigned)best.ks;
+  attrs[0].val.clusterDim.x = (unsigned)g.ks;
   attrs[0].val.clusterDim.y = 1;
   attrs[0].val.clusterDim.z = 1;
   attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, kern, tm0, tm1, args);
+  return cudaLaunchKernelEx(&cfg, kern, maps, args);
+}
+
+template <int NMAT, bool AFFINE>
+cudaError_t launch_meta(NarrowArgs args, const uint32_t *w0, const uint32_t *w1, cudaStream_t st, bool pdl) {
+  // metadata by TMA needs 16-byte rows (G % 8 == 0) and 16-byte aligned arrays
+  bool fast = (args.K / 128) % 8 == 0;
+  for (int i = 0; i < 2; ++i) {
+    fast = fast && (reinterpret_cast<uintptr_t>(args.s[i]) & 15) == 0;
+    fast = fast && (reinterpret_cast<uintptr_t>(args.b[i]) & 15) == 0;
+  }
+  if (fast) return launch_impl<NMAT, AFFINE, true>(args, w0, w1, st, pdl);
+  return launch_impl<NMAT, AFFINE, false>(args, w0, w1, st, pdl);
 }
 
 NarrowArgs make_args(const void *x, int64_t M, int64_t N, int64_t K, void *out) {
@@ -729,7 +795,7 @@ cudaError_t launch_narrow(const WeightView &W, const void *x, int64_t M, void *y
   NarrowArgs a = make_args(x, M, W.N, W.K, y);
   a.s[0] = a.s[1] = W.s;
   a.b[0] = a.b[1] = W.b;
-  return W.b ? launch_impl<1, true>(a, W.w, W.w, st, pdl) : launch_impl<1, false>(a, W.w, W.w, st, pdl);
+  return W.b ? launch_meta<1, true>(a, W.w, W.w, st, pdl) : launch_meta<1, false>(a, W.w, W.w, st, pdl);
 }
 
 cudaError_t launch_narrow_gate_up(const WeightView &G, const WeightView &U, const void *x,
@@ -741,8 +807,8 @@ cudaError_t launch_narrow_gate_up(const WeightView &G, const WeightView &U, cons
   a.b[1] = U.b;
   // With mixed metadata the affine variant runs for both matrices; it derives
   // -scale/2 for the one whose biases pointer is null.
-  if (G.b || U.b) return launch_impl<2, true>(a, G.w, U.w, st, pdl);
-  return launch_impl<2, false>(a, G.w, U.w, st, pdl);
+  if (G.b || U.b) return launch_meta<2, true>(a, G.w, U.w, st, pdl);
+  return launch_meta<2, false>(a, G.w, U.w, st, pdl);
 }
 
 unsigned int read_and_clear_narrow_errors(cudaStream_t st, cudaError_t *err) {

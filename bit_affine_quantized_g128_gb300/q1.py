@@ -42,6 +42,10 @@ class _CWeight(ctypes.Structure):
 _lib = None
 
 
+
+# K of the narrow kernel (q1_qmv / q1_qmm_narrow); q1_qmm runs larger K on the prefill path
+NARROW_MAX_K = 40960
+
 def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     """Load libq1.so (after torch, so that both share one CUDA runtime)."""
     global _lib
@@ -187,7 +191,7 @@ def qmm(W: Q1Weight, x: torch.Tensor, workspace: Optional[torch.Tensor] = None,
     M = x2.shape[0]
     y = out if out is not None else torch.empty((M, W.N), dtype=x.dtype, device=x.device)
     ws = workspace
-    if ws is None and M > get_qmm_max_rows():
+    if ws is None and (M > get_qmm_max_rows() or W.K > NARROW_MAX_K):
         ws = qmm_workspace(M, W.N, W.K, x.device)
     wp, wn = (ws.data_ptr(), ws.numel()) if ws is not None else (None, 0)
     _check("q1_qmm", lib().q1_qmm(W.cref(), x2.data_ptr(), M, _DT[x.dtype], y.data_ptr(), wp, wn,

@@ -105,7 +105,11 @@ q1_status q1_dequantize(const q1_weight *W, q1_dtype out_t, void *out, q1_stream
  *   temporary).  Its tiles are fp16: symmetric weights are exact and affine
  *   ones rounded once at 2^-11; the activations enter as fp16 rows scaled by
  *   a power of two per row (kept in the workspace), which is exact for every
- *   activation whose scaled value is a normal fp16 number. */
+ *   activation whose scaled value is a normal fp16 number.
+ * The narrow kernel covers K <= 40960 (a cluster of at most 8 CTAs, each with
+ * 10 warps that own 512 k each): q1_qmv and q1_qmm_narrow return
+ * Q1_ERR_SHAPE above it, and q1_qmm runs such K on the prefill path for any
+ * M (workspace required). */
 q1_status q1_qmv(const q1_weight *W, const void *x, q1_dtype dtype, void *y, q1_stream stream);
 q1_status q1_qmm_narrow(const q1_weight *W, const void *x, int64_t M, q1_dtype dtype,
                         void *y, q1_stream stream);
@@ -131,7 +135,7 @@ q1_status q1_embed_gather(const q1_weight *E, const int32_t *ids, int64_t T, q1_
 
 /* ---- fused dense FFN (higgs PR #212, "What": fused dense-FFN operations) ---
  * y[M][D] = Down . (SiLU(Gate . x) * (Up . x)) with SiLU(g) = g / (1 + e^-g).
- * gate, up: [F][D]; down: [D][F].  1 <= M <= 8.  x [M][D], y [M][D] bf16.
+ * gate, up: [F][D]; down: [D][F].  1 <= M <= 8; D, F <= 40960.  x [M][D], y [M][D] bf16.
  * The intermediate h [M][F] is kept in bf16 at the start of the workspace
  * (q1_ffn_workspace_size(M, D, F) bytes, 256-byte aligned); it is still
  * there when the call's work completes. */

@@ -125,9 +125,25 @@ def test_qmv_and_leading_dims(q1):
 
 
 @pytest.mark.parametrize("affine", [False, True])
+def test_k_beyond_narrow_kernel(q1, affine):
+    # K above the narrow kernel's 40960: the narrow calls refuse the shape,
+    # q1_qmm runs the prefill path even for M <= the row threshold
+    N, K = 48, 40960 + 512
+    t, x = _case(N, K, 3, affine, seed=23)
+    W = q1.Q1Weight.from_host(t)
+    with pytest.raises(q1.Q1Error):
+        q1.qmv(W, x[0].to(DEV))
+    with pytest.raises(q1.Q1Error):
+        q1.qmm_narrow(W, x.to(DEV))
+    y = q1.qmm(W, x.to(DEV))
+    check_matmul(y, O.qmm(x, t.words, t.scales, t.biases, K), x,
+                 O.dequantize_f32(t.words, t.scales, t.biases, K), "qmm K=41472")
+
+
+@pytest.mark.parametrize("affine", [False, True])
 def test_narrow_mixed_magnitudes(q1, affine):
-    # rows far above and below 1, and groups with a single large outlier:
-    # exercises the per-(group, token) power-of-two scale of the activations
+    # rows far above and below 1, and groups with a single large outlier: the
+    # activations enter the MMAs scaled by 1/d_p (up to 2^7), in bf16 range
     M, N, K = 8, 512, 2048
     t, x = _case(N, K, M, affine, seed=17)
     x = x.float()
