@@ -24,7 +24,7 @@ EXPORTED = [
     "q1_pack", "q1_unpack", "q1_dequantize", "q1_qmv", "q1_qmm_workspace_size",
     "q1_qmm_narrow", "q1_qmm", "q1_set_qmm_max_rows", "q1_get_qmm_max_rows",
     "q1_embed_gather", "q1_ffn_workspace_size", "q1_ffn_fused", "q1_check_symmetric",
-    "q1_device_errors", "q1_status_string",
+    "q1_device_errors", "q1_status_string", "q1_ffn_fused_noalloc",
 ]
 
 
@@ -41,10 +41,11 @@ class _CWeight(ctypes.Structure):
 
 _lib = None
 
-
-
 # K of the narrow kernel (q1_qmv / q1_qmm_narrow); q1_qmm runs larger K on the prefill path
 NARROW_MAX_K = 40960
+# bytes of the library's fixed array that holds h for q1_ffn_fused_noalloc
+FFN_NOALLOC_BYTES = 512 * 1024
+
 
 def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     """Load libq1.so (after torch, so that both share one CUDA runtime)."""
@@ -70,6 +71,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "q1_embed_gather": ([W, P, I64, I32, P, P, P], I32),
         "q1_ffn_workspace_size": ([I64, I64, I64], SZ),
         "q1_ffn_fused": ([W, W, W, P, I64, I32, P, P, SZ, P], I32),
+        "q1_ffn_fused_noalloc": ([W, W, W, P, I64, I32, P, P], I32),
         "q1_check_symmetric": ([W, P, P], I32),
         "q1_device_errors": ([ctypes.POINTER(ctypes.c_uint), P], I32),
         "q1_status_string": ([I32], ctypes.c_char_p),
@@ -233,6 +235,20 @@ def ffn_fused(gate: Q1Weight, up: Q1Weight, down: Q1Weight, x: torch.Tensor,
     _check("q1_ffn_fused", lib().q1_ffn_fused(gate.cref(), up.cref(), down.cref(), x2.data_ptr(), M,
                                               _DT[x.dtype], y.data_ptr(), ws.data_ptr(),
                                               ws.numel(), _stream()))
+    return y.reshape(*lead, down.N)
+
+
+def ffn_fused_noalloc(gate: Q1Weight, up: Q1Weight, down: Q1Weight, x: torch.Tensor,
+                      out=None) -> torch.Tensor:
+    """q1_ffn_fused with h in the library's fixed device array (no workspace,
+    no allocation in the call; `out` may be preallocated too)."""
+    lead = x.shape[:-1]
+    x2 = _flat(x, gate.K)
+    M = x2.shape[0]
+    y = out if out is not None else torch.empty((M, down.N), dtype=x.dtype, device=x.device)
+    _check("q1_ffn_fused_noalloc", lib().q1_ffn_fused_noalloc(gate.cref(), up.cref(), down.cref(),
+                                                              x2.data_ptr(), M, _DT[x.dtype],
+                                                              y.data_ptr(), _stream()))
     return y.reshape(*lead, down.N)
 
 

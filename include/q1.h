@@ -144,6 +144,29 @@ q1_status q1_ffn_fused(const q1_weight *gate, const q1_weight *up, const q1_weig
                        const void *x, int64_t M, q1_dtype dtype, void *y, void *workspace,
                        size_t workspace_bytes, q1_stream stream);
 
+/* ---- fused FFN without any allocation ---------------------------------------
+ * The source method has no counterpart of this call: it exists for callers
+ * that must not allocate memory at all, not even a workspace.  It computes
+ * exactly what q1_ffn_fused computes (same kernels, same results) and keeps h
+ * in a fixed array inside this library instead of a caller workspace:
+ *   - the array holds Q1_FFN_NOALLOC_BYTES (512 KiB) per device, so the call
+ *     needs M * F * 2 <= Q1_FFN_NOALLOC_BYTES (e.g. M <= 8 with F <= 32768);
+ *     larger shapes return Q1_ERR_WORKSPACE and launch nothing;
+ *   - the call allocates nothing (no cudaMalloc / cudaFree, no allocating
+ *     library call);
+ *   - the first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) and caches it: make that first call before any
+ *     stream capture on that device;
+ *   - nothing in the array has to start at zero: the gate/up kernel writes
+ *     all of h before the down kernel reads it;
+ *   - the array is shared by every call on the device: calls that can
+ *     overlap in time (other streams, other host threads) race on it, so
+ *     order them (one stream, or events);
+ *   - h of the last call stays in the array until the next call. */
+#define Q1_FFN_NOALLOC_BYTES (512u * 1024u)
+q1_status q1_ffn_fused_noalloc(const q1_weight *gate, const q1_weight *up, const q1_weight *down,
+                               const void *x, int64_t M, q1_dtype dtype, void *y, q1_stream stream);
+
 /* ---- symmetric check (higgs PR #212, walkthrough: symmetric bias
  * compaction and validation) -------------------------------------------------
  * Writes 1 to *d_is_symmetric (device int32) iff every stored bias equals
