@@ -44,7 +44,7 @@ WORKLOAD = "q1 decode QMV M=1, 64 layers x {gate,up 17408x5120; down 5120x17408;
 # DRAM traffic per launch of the narrow kernel on the gate shape (17408 x 5120,
 # M = 1), from ncu (dram__bytes_read.sum + dram__bytes_write.sum), and the
 # sha256 of q1_narrow.cu it was taken on; reported as null once the source differs.
-NCU_TRAFFIC = {"bytes": None, "source_sha256": None}
+NCU_TRAFFIC = {"bytes": 12584448, "source_sha256": "a71c9058884ddad5461c24bee7b8404e65b6c097c53a237a1bd42466f4f1c442"}
 
 
 def weight_bytes(N, K, affine):
@@ -441,7 +441,8 @@ def gpu_arm(args):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 3), "traffic": traffic,
                      "peak_source": peak_src,
-                     "kernel": "narrow_kernel<1,false> (mma.sync bf16, cluster K-split)"},
+                     "kernel": "narrow_kernel<1,false,true> (mma.sync bf16, span-stationary warps, producer warp)",
+                     "achieved_from": "graph time / launches (launch gaps included)"},
         "clocks": clocks,
         "e2e": e2e,
         "gpu_launches": launches,
