@@ -211,8 +211,8 @@ __host__ __device__ inline SmemLayout smem_layout(const Geo &g, bool affine) {
   L.ring = off; off += g.ring * L.slot_words;
   L.meta = off; off += g.ring * L.slot_meta;
   L.bars = off; off += align_up(2 * g.ring * 8, 128);
-  L.part = off; off += g.tr * g.qm * 16 * g.mst * 4;
-  L.red = off; off += g.ks > 1 ? g.tr * 16 * g.mst * 4 : 0;
+  L.part = off; off += g.tr * g.qm * 16 * (g.mst < 2 ? 2 : g.mst) * 4;
+  L.red = off; off += g.ks > 1 ? g.tr * 16 * (g.mst < 2 ? 2 : g.mst) * 4 : 0;
   L.total = off + 1024;  // slack for aligning the dynamic shared memory base
   return L;
 }
@@ -226,6 +226,9 @@ struct NarrowArgs {
   const __nv_bfloat16 *x;  // [M][K]
   __nv_bfloat16 *out;      // y [M][N] or h [M][N]
   Geo geo;
+  // strides of the shared-memory layout, computed on the host so that the
+  // tile loop reads them as constants
+  int slot_words, slot_meta, part_tile;
 };
 
 // Tensor maps of the (up to two) matrices: packed words, scales, biases.
@@ -266,7 +269,8 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
   const int M = a.M, K = a.K, G = K / 128;
   const int64_t N = a.N;
   const Geo geo = a.geo;
-  const int KS = geo.ks, RING = geo.ring, QM = geo.qm, R = geo.R, TR = geo.tr, MST = geo.mst;
+  const int KS = geo.ks, RING = geo.ring, QM = geo.qm, R = geo.R, TR = geo.tr;
+  const int MST = geo.mst < 2 ? 2 : geo.mst;  // tokens stored per partial row (a lane stores a pair)
   const SmemLayout L = smem_layout(geo, AFFINE);
   const int NC = QM * R;                    // consumer warps
   const int MROW = meta_groups(QM) * 2;     // bytes per metadata row
@@ -378,43 +382,53 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // ---- activation fragments of this warp's span (token gid, word t of each
-  //      group) and the per-group accumulator seeds
+  //      group) and the per-group accumulator seeds: all loads first, then
+  //      the fragments, then the four groups' C/E chains interleaved
   uint32_t bfr[kQuad][16];
   float seed[kQuad][4];
   float sx[kQuad][2];
   if (active) {
+    uint32_t xv[kQuad][16];
 #pragma unroll
     for (int u = 0; u < kQuad; ++u) {
       const int g = span * kQuad + u;
-      uint32_t xv[16];
       if (gid < M && g < G) {
         const uint4 *src = reinterpret_cast<const uint4 *>(a.x + (size_t)gid * K + (size_t)g * 128 + 32 * t);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const uint4 v = __ldg(src + q);
-          xv[4 * q] = v.x; xv[4 * q + 1] = v.y; xv[4 * q + 2] = v.z; xv[4 * q + 3] = v.w;
+          xv[u][4 * q] = v.x; xv[u][4 * q + 1] = v.y; xv[u][4 * q + 2] = v.z; xv[u][4 * q + 3] = v.w;
         }
       } else {
 #pragma unroll
-        for (int q = 0; q < 16; ++q) xv[q] = 0u;
+        for (int q = 0; q < 16; ++q) xv[u][q] = 0u;
       }
+    }
+#pragma unroll
+    for (int u = 0; u < kQuad; ++u) {
 #define Q1_PAIR(P) \
-  bfr[u][P] = bmul2(prmt(xv[(P) >> 1], xv[8 + ((P) >> 1)], ((P) & 1) ? 0x7632u : 0x5410u), inv_d_bits(P));
+  bfr[u][P] = bmul2(prmt(xv[u][(P) >> 1], xv[u][8 + ((P) >> 1)], ((P) & 1) ? 0x7632u : 0x5410u), inv_d_bits(P));
       Q1_PAIR(0) Q1_PAIR(1) Q1_PAIR(2) Q1_PAIR(3) Q1_PAIR(4) Q1_PAIR(5) Q1_PAIR(6) Q1_PAIR(7)
       Q1_PAIR(8) Q1_PAIR(9) Q1_PAIR(10) Q1_PAIR(11) Q1_PAIR(12) Q1_PAIR(13) Q1_PAIR(14) Q1_PAIR(15)
 #undef Q1_PAIR
-      // rows 0..7: C_g = sum a_p x'; rows 8..15: Sx_g / 2 = sum (d_p / 2) x'
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
-#define Q1_CE(JJ)                                                                                   \
-  mma_acc(d, a_bits(2 * (JJ)), halfd_bits(2 * (JJ)), a_bits(2 * (JJ) + 1), halfd_bits(2 * (JJ) + 1), \
-          bfr[u][2 * (JJ)], bfr[u][2 * (JJ) + 1]);
-      Q1_CE(0) Q1_CE(1) Q1_CE(2) Q1_CE(3) Q1_CE(4) Q1_CE(5) Q1_CE(6) Q1_CE(7)
+    }
+    // rows 0..7: C_g = sum a_p x'; rows 8..15: Sx_g / 2 = sum (d_p / 2) x'
+    float d[kQuad][4];
+#pragma unroll
+    for (int u = 0; u < kQuad; ++u) d[u][0] = d[u][1] = d[u][2] = d[u][3] = 0.f;
+#define Q1_CE(JJ)                                                                                           \
+  _Pragma("unroll") for (int u = 0; u < kQuad; ++u)                                                         \
+      mma_acc(d[u], a_bits(2 * (JJ)), halfd_bits(2 * (JJ)), a_bits(2 * (JJ) + 1), halfd_bits(2 * (JJ) + 1), \
+              bfr[u][2 * (JJ)], bfr[u][2 * (JJ) + 1]);
+    Q1_CE(0) Q1_CE(1) Q1_CE(2) Q1_CE(3) Q1_CE(4) Q1_CE(5) Q1_CE(6) Q1_CE(7)
 #undef Q1_CE
+#pragma unroll
+    for (int u = 0; u < kQuad; ++u) {
       // tokens 2t, 2t+1
-      const float e0 = AFFINE ? d[0] : d[0] + d[2], e1 = AFFINE ? d[1] : d[1] + d[3];
+      const float e0 = AFFINE ? d[u][0] : d[u][0] + d[u][2], e1 = AFFINE ? d[u][1] : d[u][1] + d[u][3];
       seed[u][0] = -e0; seed[u][1] = -e1; seed[u][2] = -e0; seed[u][3] = -e1;
-      sx[u][0] = 2.f * d[2];
-      sx[u][1] = 2.f * d[3];
+      sx[u][0] = 2.f * d[u][2];
+      sx[u][1] = 2.f * d[u][3];
     }
   }
 
@@ -428,18 +442,24 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
   const uint32_t wlane = ring_s + qi * kTileBytes + gid * 64 + 4 * t;
   const uint32_t mlane = meta_s + gid * MROW + (span - q_base) * 8;
 
+  // this lane's partial sums (rows gid, gid + 8 of span qi; tokens 2t, 2t+1)
+  const uint32_t plane = smem_u32(part) + (uint32_t)(((qi * 16 + gid) * MST + 2 * t) * 4);
+  const bool pstore = 2 * t < MST;
+  const uint32_t SW = (uint32_t)a.slot_words, SM = (uint32_t)a.slot_meta, PT = (uint32_t)a.part_tile;
+
   for (int rb = v_lo; rb < v_hi; rb += TR) {
     const int trc = min(TR, v_hi - rb);
     if (active && ri < trc) {
-      // ring position of this warp's first tile of the round
+      // ring position of this warp's first tile of the round; from there the
+      // slot pointers advance by R slots per tile
       const int j0 = rb - v_lo + ri;
       uint32_t slot = (uint32_t)(j0 % RING), ph = (uint32_t)((j0 / RING) & 1);
+      uint32_t tb = wlane + slot * SW, mb = mlane + slot * SM, fb = full_s + 8 * slot;
+      uint32_t pp = plane + (uint32_t)ri * PT;
       for (int lt = ri; lt < trc; lt += R) {
-        const uint32_t tb = wlane + slot * L.slot_words;
-        const uint32_t mb = mlane + slot * L.slot_meta;
         // a wait that ran out has set the device error word; the results of
         // this call are then undefined, but the CTA still reaches its barriers
-        mbar_wait(full_s + 8 * slot, ph);
+        mbar_wait(fb, ph);
         uint32_t wa[kQuad], wb[kQuad];
 #pragma unroll
         for (int u = 0; u < kQuad; ++u) {
@@ -453,8 +473,6 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
           ba = lds64(mb + 16 * MROW);
           bb = lds64(mb + 24 * MROW);
         }
-        // the slot's data is in registers once the loads complete; release it
-        // after the first use of every loaded value (the unpack below)
         uint32_t wa8[kQuad], wb8[kQuad];
 #pragma unroll
         for (int u = 0; u < kQuad; ++u) {
@@ -503,26 +521,24 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
         }
         // every lane's values are consumed: release the slot to the producer
         __syncwarp();
-        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(empty_s + 8 * slot) : "memory");
-        // partial sums of this (row tile, span): rows gid, gid + 8; tokens 2t, 2t+1
-        {
-          float *pp = part + ((size_t)(lt * QM + qi) * 16) * MST;
-          if (MST >= 2) {
-            if (2 * t < MST) {
-              const uint32_t p0 = smem_u32(pp + gid * MST + 2 * t);
-              asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(p0), "f"(acc[0]), "f"(acc[1]) : "memory");
-              asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(p0 + 8 * MST * 4), "f"(acc[2]),
-                           "f"(acc[3])
-                           : "memory");
-            }
-          } else if (t == 0) {
-            pp[gid] = acc[0];
-            pp[gid + 8] = acc[2];
-          }
+        if (lane == 0)
+          asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(fb + 8 * RING) : "memory");
+        if (pstore) {
+          asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(pp), "f"(acc[0]), "f"(acc[1]) : "memory");
+          asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(pp + 8 * MST * 4), "f"(acc[2]), "f"(acc[3])
+                       : "memory");
         }
+        // advance R slots (the chooser keeps R < RING)
+        pp += (uint32_t)R * PT;
         slot += (uint32_t)R;
-        while (slot >= (uint32_t)RING) {
+        tb += (uint32_t)R * SW;
+        mb += (uint32_t)R * SM;
+        fb += 8u * (uint32_t)R;
+        if (slot >= (uint32_t)RING) {
           slot -= (uint32_t)RING;
+          tb -= (uint32_t)RING * SW;
+          mb -= (uint32_t)RING * SM;
+          fb -= 8u * (uint32_t)RING;
           ph ^= 1u;
         }
       }
@@ -736,6 +752,12 @@ cudaError_t launch_impl(NarrowArgs args, const uint32_t *w0, const uint32_t *w1,
   Geo g;
   if (!choose_geo<NMAT, AFFINE, FASTMETA>(args.N, args.K, args.M, &g)) return cudaErrorInvalidConfiguration;
   args.geo = g;
+  {
+    const SmemLayout L0 = smem_layout(g, AFFINE);
+    args.slot_words = L0.slot_words;
+    args.slot_meta = L0.slot_meta;
+    args.part_tile = g.qm * 16 * (g.mst < 2 ? 2 : g.mst) * 4;
+  }
   Maps maps;
   memset(&maps, 0, sizeof(maps));
   if (!make_word_map(&maps.w[0], w0, args.N, args.K)) return cudaErrorInvalidValue;
