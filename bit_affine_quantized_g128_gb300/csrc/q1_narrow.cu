@@ -167,20 +167,19 @@ __device__ __forceinline__ bool mbar_try(uint32_t addr, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait; false when it ran out (the device error word is set).
-__device__ __noinline__ bool mbar_wait_bounded(uint32_t addr, uint32_t parity) {
+// Bounded wait, all inline (no call in the tile loop): false when it ran out
+// (the device error word is set).
+__device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity) {
+  if (mbar_try(addr, parity)) return true;
   const unsigned long long t0 = globaltimer();
-  for (uint32_t i = 0;; ++i) {
+#pragma unroll 1
+  for (uint32_t i = 1;; ++i) {
     if (mbar_try(addr, parity)) return true;
-    if ((i & 15u) == 15u && globaltimer() - t0 > kWaitLimitNs) {
+    if ((i & 15u) == 0u && globaltimer() - t0 > kWaitLimitNs) {
       atomicOr(&g_narrow_err, 1u);
       return false;
     }
   }
-}
-__device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity) {
-  if (mbar_try(addr, parity)) return true;
-  return mbar_wait_bounded(addr, parity);
 }
 
 // Launch geometry, decided on the host.
