@@ -18,10 +18,13 @@
 // epilogue multiplies by 2^-e_m.  A small prep kernel writes the scaled fp16
 // rows and the scales into the caller's workspace.
 //
-// One CTA computes a 128-token x 256-row output tile (one SM; 192 KB of shared
-// memory keeps it alone on the SM, so its 256-column TMEM allocation cannot
-// contend):
-//   warp 0        TMA producer: x tiles [128 tokens x 64 k] fp16, 128B swizzle
+// One CTA computes MT x 128 tokens x 256 rows (MT = 2 when that needs fewer
+// CTA-times than MT = 1, see launch_wide):
+// every dequantized weight tile feeds MT MMAs, one per 128-token tile, into
+// MT 256-column TMEM accumulators.  About 192 KB of shared memory keeps the
+// CTA alone on its SM, so its TMEM allocation (256 or 512 columns) cannot
+// contend:
+//   warp 0        TMA producer: x tiles [MT x 128 tokens x 64 k] fp16, 128B swizzle
 //   warp 1        TMEM allocator and the single MMA-issuing thread
 //                 (tcgen05.mma.cta_group::1.kind::f16, M=128 N=256 K=16)
 //   warps 2..17   dequantizers: two threads per weight row read the packed
@@ -29,7 +32,8 @@
 //                 writes 32 fp16 (one word) per k-step into the 128B-swizzled
 //                 K-major layout the MMA reads; then the epilogue:
 //                 TMEM -> registers -> scale -> bf16 -> global.
-// Stages: 4 x (16 KB x tile + 32 KB weight tile), mbarrier hand-offs.
+// Stages: 4 (MT = 1) or 3 (MT = 2) x (x tiles + 32 KB weight tile), mbarrier
+// hand-offs.
 // Every wait is bounded (globaltimer); one that runs out sets a device error
 // word and a CTA-wide abort flag so that the other roles stop waiting too.
 #include <cuda.h>
@@ -45,28 +49,31 @@ __device__ unsigned int g_wide_err = 0;
 
 namespace {
 
-constexpr int BM = 128;  // tokens per tile (TMEM lanes)
+constexpr int BM = 128;  // tokens per MMA tile (TMEM lanes)
 constexpr int BN = 256;  // weight rows per tile (MMA N)
-constexpr int BK = 64;   // k per stage (one 128-byte swizzle atom of bf16)
-constexpr int STAGES = 4;
+constexpr int BK = 64;   // k per stage (one 128-byte swizzle atom of fp16)
+// MT token tiles of BM per CTA share every dequantized weight tile (MT = 2
+// halves the dequantization per MMA); the stages then shrink from 4 to 3
+template <int MT> constexpr int kStages = MT == 1 ? 4 : 3;
 constexpr int kThreadsWide = 576;  // 18 warps
 constexpr int kDeqWarp0 = 2;
 constexpr int kDeqThreads = 512;   // two threads per weight row: one word each per k-step
-constexpr uint32_t A_BYTES = BM * BK * 2;  // 16 KB
+constexpr uint32_t A_TILE = BM * BK * 2;   // 16 KB per token tile
 constexpr uint32_t B_BYTES = BN * BK * 2;  // 32 KB
-constexpr uint32_t kTmemCols = 256;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
+constexpr int kMaxStages = 4;
 struct __align__(8) WideShared {
-  uint64_t full_a[STAGES];
-  uint64_t full_b[STAGES];
-  uint64_t empty[STAGES];
+  uint64_t full_a[kMaxStages];
+  uint64_t full_b[kMaxStages];
+  uint64_t empty[kMaxStages];
   uint64_t accum_full;
   uint32_t tmem_base;
   volatile int abort_flag;
 };
 
-constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + STAGES * (A_BYTES + B_BYTES) + sizeof(WideShared);
+template <int MT>
+constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + kStages<MT> * (MT * A_TILE + B_BYTES) + sizeof(WideShared);
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -191,6 +198,7 @@ struct GroupData {
   uint16_t s, b;
 };
 
+template <int MT>
 __global__ void __launch_bounds__(kThreadsWide, 1)
 wide_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint32_t *__restrict__ W,
             const uint16_t *__restrict__ S, const uint16_t *__restrict__ Bv, int M, int N, int K,
@@ -198,12 +206,15 @@ wide_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint32_t *__restri
   extern __shared__ unsigned char smem_raw[];
   unsigned char *base = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  constexpr int STAGES = kStages<MT>;
+  constexpr uint32_t A_BYTES = MT * A_TILE;        // the stage's x tiles (MT x 128 tokens)
+  constexpr uint32_t kTmemCols = 256 * MT;         // one 256-column accumulator per token tile
   unsigned char *sa = base;                        // STAGES x A_BYTES
   unsigned char *sb = base + STAGES * A_BYTES;     // STAGES x B_BYTES
   WideShared *sh = reinterpret_cast<WideShared *>(sb + STAGES * B_BYTES);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * BM;
+  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * (BM * MT);
   const int KSTEPS = K / BK;
 
   if (tid == 0) {
@@ -255,8 +266,10 @@ wide_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint32_t *__restri
         const uint32_t a_addr = smem_u32(sa + s * A_BYTES), b_addr = smem_u32(sb + s * B_BYTES);
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk) {
-          umma_bf16(tmem_d, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32),
-                    (ks > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt)
+            umma_bf16(tmem_d + 256u * mt, sw128_desc(a_addr + mt * A_TILE + kk * 32), sw128_desc(b_addr + kk * 32),
+                      (ks > 0 || kk > 0) ? 1u : 0u);
         }
         umma_commit(&sh->empty[s]);
       }
@@ -346,13 +359,14 @@ wide_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint32_t *__restri
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       asm volatile("griddepcontrol.wait;" ::: "memory");  // inv_scale comes from the prep kernel
       const int quarter = warp & 3, part = (warp - kDeqWarp0) >> 2;  // 4 column quarters
-      const int m = m0 + 32 * quarter + lane;
-      const float rs = m < M ? inv_scale[m] : 0.f;
 #pragma unroll 1
-      for (int cc = 0; cc < 2; ++cc) {
+      for (int mc = 0; mc < 2 * MT; ++mc) {
+        const int mt = mc >> 1, cc = mc & 1;
+        const int m = m0 + BM * mt + 32 * quarter + lane;
+        const float rs = m < M ? inv_scale[m] : 0.f;
         const int col = part * 64 + cc * 32;
         uint32_t v[32];
-        const uint32_t taddr = tmem_d + ((uint32_t)(32 * quarter) << 16) + (uint32_t)col;
+        const uint32_t taddr = tmem_d + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(256 * mt + col);
         asm volatile(
             "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
             "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
@@ -463,6 +477,41 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
+template <int MT>
+cudaError_t launch_wide_mma(const WeightView &W, const __half *x16, int64_t M, const float *inv_scale, void *y,
+                            cudaStream_t st) {
+  auto encode = get_encode();
+  if (!encode) return cudaErrorNotSupported;
+  CUtensorMap map;
+  cuuint64_t gdim[2] = {(cuuint64_t)W.K, (cuuint64_t)M};
+  cuuint64_t gstride[1] = {(cuuint64_t)W.K * 2};
+  cuuint32_t box[2] = {BK, (cuuint32_t)(BM * MT)};
+  cuuint32_t estride[2] = {1, 1};
+  CUresult r = encode(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half *>(x16), gdim, gstride, box,
+                      estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(wide_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes<MT>);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((W.N + BN - 1) / BN), (unsigned)((M + BM * MT - 1) / (BM * MT)), 1);
+  cfg.blockDim = dim3(kThreadsWide, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes<MT>;
+  cfg.stream = st;
+  cudaLaunchAttribute attr_pdl;
+  attr_pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr_pdl.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr_pdl;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, wide_kernel<MT>, map, W.w, W.s, W.b, (int)M, (int)W.N, (int)W.K, inv_scale,
+                            static_cast<__nv_bfloat16 *>(y));
+}
+
 }  // namespace
 
 size_t wide_workspace_bytes(int64_t M, int64_t K) {
@@ -486,35 +535,19 @@ cudaError_t launch_wide(const WeightView &W, const void *x, int64_t M, void *y, 
     if (e != cudaSuccess) return e;
   }
   // 2. the tcgen05 kernel, launched as a programmatic dependent of the prep:
-  //    barrier set-up, TMEM allocation and the first weight tiles overlap it
-  CUtensorMap map;
-  cuuint64_t gdim[2] = {(cuuint64_t)W.K, (cuuint64_t)M};
-  cuuint64_t gstride[1] = {(cuuint64_t)W.K * 2};
-  cuuint32_t box[2] = {BK, BM};
-  cuuint32_t estride[2] = {1, 1};
-  CUresult r = encode(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, x16, gdim, gstride, box, estride,
-                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((W.N + BN - 1) / BN), (unsigned)((M + BM - 1) / BM), 1);
-  cfg.blockDim = dim3(kThreadsWide, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = st;
-  cudaLaunchAttribute attr_pdl;
-  attr_pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr_pdl.val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = &attr_pdl;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, wide_kernel, map, W.w, W.s, W.b, (int)M, (int)W.N, (int)W.K,
-                            (const float *)inv_scale, static_cast<__nv_bfloat16 *>(y));
+  //    barrier set-up, TMEM allocation and the first weight tiles overlap it.
+  //    Two token tiles per CTA when that takes fewer CTA-times: one CTA runs
+  //    per SM, a CTA with two tiles takes ~1.5x the time of one with a single
+  //    tile (measured), and the waves are whole.
+  int sms = 0, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (sms <= 0) sms = 1;
+  const int64_t ntiles = (W.N + BN - 1) / BN;
+  const int64_t waves1 = (ntiles * ((M + BM - 1) / BM) + sms - 1) / sms;
+  const int64_t waves2 = (ntiles * ((M + 2 * BM - 1) / (2 * BM)) + sms - 1) / sms;
+  const bool two = M > BM && (double)waves2 * 1.5 < (double)waves1;
+  return two ? launch_wide_mma<2>(W, x16, M, inv_scale, y, st) : launch_wide_mma<1>(W, x16, M, inv_scale, y, st);
 }
 
 unsigned int read_and_clear_wide_errors(cudaStream_t st, cudaError_t *err) {

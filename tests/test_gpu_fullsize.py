@@ -55,7 +55,7 @@ def test_narrow_full_shapes(q1, M, N, K, affine):
     _check_rows(y, t, x, _rows(N, 128, M), f"narrow M={M} {N}x{K}")
 
 
-@pytest.mark.parametrize("M", [9, 128, 2048])
+@pytest.mark.parametrize("M", [9, 128, 1000, 2048])
 @pytest.mark.parametrize("N,K,affine", [(D_FF, D_MODEL, False), (D_MODEL, D_FF, True)])
 def test_prefill_full_shapes(q1, M, N, K, affine):
     t = synth.q1_tensor(N, K, seed=1004 + affine, affine=affine)
