@@ -124,6 +124,19 @@ def test_qmv_and_leading_dims(q1):
     check_matmul(y3.reshape(8, N), yo, x, wd, "[2,4,K]")
 
 
+@pytest.mark.parametrize("N,K", [(333, 4096), (1000, 5120)])
+@pytest.mark.parametrize("affine", [False, True])
+def test_qmm_narrow_many_spans(q1, N, K, affine):
+    # K with at least 16 spans of two groups: the 2-group-span kernel (up to
+    # 20 warps per CTA, the tile issue inside warp 0), ragged row tiles
+    for M in (1, 3, 8):
+        t, x = _case(N, K, M, affine, seed=N + K + 7 * M)
+        W = q1.Q1Weight.from_host(t)
+        y = q1.qmm_narrow(W, x.to(DEV))
+        check_matmul(y, O.qmm(x, t.words, t.scales, t.biases, K), x,
+                     O.dequantize_f32(t.words, t.scales, t.biases, K), f"narrow N={N} K={K} M={M}")
+
+
 @pytest.mark.parametrize("affine", [False, True])
 def test_k_beyond_narrow_kernel(q1, affine):
     # K above the narrow kernel's 40960: the narrow calls refuse the shape,
@@ -292,8 +305,8 @@ def test_embed_gather_empty(q1):
 
 # ------------------------------------------------------------------ fused FFN
 @pytest.mark.parametrize("M", [1, 4, 8])
-def test_ffn_fused(q1, M):
-    D, F = 512, 1408
+@pytest.mark.parametrize("D,F", [(512, 1408), (4096, 1024)])
+def test_ffn_fused(q1, M, D, F):
     gate = synth.q1_tensor(F, D, seed=301, affine=False)
     up = synth.q1_tensor(F, D, seed=302, affine=(M == 4))  # mixed metadata once
     down = synth.q1_tensor(D, F, seed=303, affine=False)
