@@ -34,8 +34,12 @@
 //                 TMEM -> registers -> scale -> bf16 -> global.
 // Stages: 4 (MT = 1) or 3 (MT = 2) x (x tiles + 32 KB weight tile), mbarrier
 // hand-offs.
+// When the tiles are too few to fill the SMs (small M, or the 5120-row down
+// projection), a cluster of up to 8 CTAs splits K for each tile and sums the
+// partial tiles through distributed shared memory (see SPLIT below).
 // Every wait is bounded (globaltimer); one that runs out sets a device error
 // word and a CTA-wide abort flag so that the other roles stop waiting too.
+#include <cooperative_groups.h>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -63,6 +67,9 @@ constexpr uint32_t B_BYTES = BN * BK * 2;  // 32 KB
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
 constexpr int kMaxStages = 4;
+// split-K partial tile in the (then idle) stage memory: 128 rows x 256 fp32,
+// rows padded by 16 bytes so that a warp's row-wise stores spread over the banks
+constexpr int kPartStride = BN + 4;
 struct __align__(8) WideShared {
   uint64_t full_a[kMaxStages];
   uint64_t full_b[kMaxStages];
@@ -198,11 +205,16 @@ struct GroupData {
   uint16_t s, b;
 };
 
-template <int MT>
+// SPLIT: a thread-block cluster of `ksplit` CTAs shares one output tile, each
+// taking a contiguous range of the 128-k groups; the fp32 partial tiles are
+// summed through distributed shared memory in rank order (deterministic, no
+// workspace).  Only with MT = 1.
+template <int MT, bool SPLIT>
 __global__ void __launch_bounds__(kThreadsWide, 1)
 wide_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint32_t *__restrict__ W,
             const uint16_t *__restrict__ S, const uint16_t *__restrict__ Bv, int M, int N, int K,
-            const float *__restrict__ inv_scale, __nv_bfloat16 *__restrict__ y) {
+            const float *__restrict__ inv_scale, __nv_bfloat16 *__restrict__ y, int ksplit) {
+  static_assert(!SPLIT || MT == 1, "split-K keeps one token tile per CTA");
   extern __shared__ unsigned char smem_raw[];
   unsigned char *base = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -214,8 +226,14 @@ wide_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint32_t *__restri
   WideShared *sh = reinterpret_cast<WideShared *>(sb + STAGES * B_BYTES);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * (BM * MT);
-  const int KSTEPS = K / BK;
+  const int rank = SPLIT ? (int)(blockIdx.x % (unsigned)ksplit) : 0;
+  const int n0 = (SPLIT ? (int)(blockIdx.x / (unsigned)ksplit) : (int)blockIdx.x) * BN;
+  const int m0 = blockIdx.y * (BM * MT);
+  // this CTA's groups [g_lo, g_hi) and k-steps (two per group)
+  const int GK = K / 128;
+  const int g_lo = SPLIT ? (int)(((int64_t)GK * rank) / ksplit) : 0;
+  const int g_hi = SPLIT ? (int)(((int64_t)GK * (rank + 1)) / ksplit) : GK;
+  const int KS0 = 2 * g_lo, KSTEPS = 2 * (g_hi - g_lo);
 
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -250,7 +268,7 @@ wide_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint32_t *__restri
         const uint32_t ph = (uint32_t)(ks / STAGES) & 1u;
         if (!mbar_wait(&sh->empty[s], ph ^ 1u, sh)) break;
         mbar_arrive_expect_tx(&sh->full_a[s], A_BYTES);
-        tma_load_2d(sa + s * A_BYTES, &tmap_x, &sh->full_a[s], ks * BK, m0);
+        tma_load_2d(sa + s * A_BYTES, &tmap_x, &sh->full_a[s], (KS0 + ks) * BK, m0);
       }
     }
   } else if (warp == 1) {
@@ -286,7 +304,7 @@ wide_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint32_t *__restri
     const uint16_t *srow = S + (size_t)(ok_row ? n : 0) * G;
     const uint16_t *brow = Bv ? Bv + (size_t)(ok_row ? n : 0) * G : nullptr;
     auto load = [&](int g, GroupData &gd) {
-      if (g < G && ok_row) {
+      if (g < g_hi && ok_row) {
         gd.w = __ldg(wrow + g);
         gd.s = srow[g];
         gd.b = brow ? brow[g] : (uint16_t)0;
@@ -305,7 +323,7 @@ wide_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint32_t *__restri
       const uint32_t lo2 = lo16 | (lo16 << 16), hi2 = hi16 | (hi16 << 16);
       // both k-steps of the group: wait for both stages, write both, then one
       // proxy fence and the two arrivals (halves the fence/arrive hand-offs)
-      const int ks0 = 2 * g;
+      const int ks0 = 2 * (g - g_lo);  // this CTA's k-step
       const int s0 = ks0 % STAGES, s1 = (ks0 + 1) % STAGES;
       const uint32_t ph0 = (uint32_t)(ks0 / STAGES) & 1u, ph1 = (uint32_t)((ks0 + 1) / STAGES) & 1u;
       // one lane waits, the warp follows its verdict (keeps the warp converged)
@@ -338,15 +356,15 @@ wide_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint32_t *__restri
       }
     };
     GroupData r0, r1, r2;
-    load(0, r0);
-    load(1, r1);
-    for (int g = 0; g < G && alive; g += 3) {
+    load(g_lo, r0);
+    load(g_lo + 1, r1);
+    for (int g = g_lo; g < g_hi && alive; g += 3) {
       load(g + 2, r2);
       process(g, r0);
-      if (g + 1 >= G || !alive) break;
+      if (g + 1 >= g_hi || !alive) break;
       load(g + 3, r0);
       process(g + 1, r1);
-      if (g + 2 >= G || !alive) break;
+      if (g + 2 >= g_hi || !alive) break;
       load(g + 4, r1);
       process(g + 2, r2);
     }
@@ -380,7 +398,15 @@ wide_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint32_t *__restri
             : "r"(taddr)
             : "memory");
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        if (m < M) {
+        if (SPLIT) {
+          // this rank's partial sums stay in shared memory for the cluster reduction
+          float *prow = reinterpret_cast<float *>(sa) + (size_t)(32 * quarter + lane) * kPartStride + col;
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4 *>(prow + 4 * q) =
+                make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                            __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+        } else if (m < M) {
           const int n = n0 + col;
           __nv_bfloat16 *dst = y + (size_t)m * N + n;
           // 16-byte stores need 16-byte aligned rows: N % 8 == 0
@@ -408,6 +434,39 @@ wide_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint32_t *__restri
 
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
+  if (SPLIT) {
+    // rank r finishes rows [128 r / S, 128 (r+1) / S) of the tile: the sum of
+    // the ranks' partial tiles in rank order, scaled back and rounded once
+    cooperative_groups::cluster_group cluster = cooperative_groups::this_cluster();
+    cluster.sync();
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // inv_scale comes from the prep kernel
+    const int r_lo = (BM * rank) / ksplit, r_hi = (BM * (rank + 1)) / ksplit;
+    const int nvec = (r_hi - r_lo) * (BN / 4);
+    for (int i = tid; i < nvec; i += kThreadsWide) {
+      const int r = r_lo + i / (BN / 4), c4 = i % (BN / 4);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int q = 0; q < ksplit; ++q) {
+        const float *pq = cluster.map_shared_rank(reinterpret_cast<float *>(sa), q);
+        const float4 v = *reinterpret_cast<const float4 *>(pq + (size_t)r * kPartStride + 4 * c4);
+        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+      }
+      const int m = m0 + r, n = n0 + 4 * c4;
+      if (m < M && n < N) {
+        const float rs = inv_scale[m];
+        __nv_bfloat16 *dst = y + (size_t)m * N + n;
+        if (n + 4 <= N && (N & 3) == 0) {
+          const __nv_bfloat162 p0 = __floats2bfloat162_rn(acc.x * rs, acc.y * rs);
+          const __nv_bfloat162 p1 = __floats2bfloat162_rn(acc.z * rs, acc.w * rs);
+          *reinterpret_cast<uint2 *>(dst) =
+              make_uint2(*reinterpret_cast<const uint32_t *>(&p0), *reinterpret_cast<const uint32_t *>(&p1));
+        } else {
+          const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+          for (int e = 0; e < 4 && n + e < N; ++e) dst[e] = __float2bfloat16_rn(a4[e] * rs);
+        }
+      }
+    }
+    cluster.sync();  // no rank leaves while another still reads its partial tile
+  }
   if (warp == 1) {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_d), "r"(kTmemCols)
@@ -477,9 +536,9 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
-template <int MT>
+template <int MT, bool SPLIT>
 cudaError_t launch_wide_mma(const WeightView &W, const __half *x16, int64_t M, const float *inv_scale, void *y,
-                            cudaStream_t st) {
+                            int ksplit, cudaStream_t st) {
   auto encode = get_encode();
   if (!encode) return cudaErrorNotSupported;
   CUtensorMap map;
@@ -493,23 +552,54 @@ cudaError_t launch_wide_mma(const WeightView &W, const __half *x16, int64_t M, c
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(wide_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(wide_kernel<MT, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes<MT>);
     if (e != cudaSuccess) return e;
     attr = true;
   }
+  const unsigned ntn = (unsigned)((W.N + BN - 1) / BN);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((W.N + BN - 1) / BN), (unsigned)((M + BM * MT - 1) / (BM * MT)), 1);
+  cfg.gridDim = dim3(ntn * (unsigned)(SPLIT ? ksplit : 1), (unsigned)((M + BM * MT - 1) / (BM * MT)), 1);
   cfg.blockDim = dim3(kThreadsWide, 1, 1);
   cfg.dynamicSmemBytes = kSmemBytes<MT>;
   cfg.stream = st;
-  cudaLaunchAttribute attr_pdl;
-  attr_pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr_pdl.val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = &attr_pdl;
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[0].val.programmaticStreamSerializationAllowed = 1;
+  attrs[1].id = cudaLaunchAttributeClusterDimension;
+  attrs[1].val.clusterDim.x = (unsigned)(SPLIT ? ksplit : 1);
+  attrs[1].val.clusterDim.y = 1;
+  attrs[1].val.clusterDim.z = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = SPLIT ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, wide_kernel<MT, SPLIT>, map, W.w, W.s, W.b, (int)M, (int)W.N, (int)W.K,
+                            inv_scale, static_cast<__nv_bfloat16 *>(y), SPLIT ? ksplit : 1);
+}
+
+// Clusters of `ks` split-K CTAs that can be resident at once (one per SM).
+int wide_split_clusters(int ks) {
+  static int cache[9] = {0};
+  if (ks < 2 || ks > 8) return 0;
+  if (cache[ks]) return cache[ks];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(ks * 32), 1, 1);
+  cfg.blockDim = dim3(kThreadsWide, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes<1>;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = (unsigned)ks;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, wide_kernel<MT>, map, W.w, W.s, W.b, (int)M, (int)W.N, (int)W.K, inv_scale,
-                            static_cast<__nv_bfloat16 *>(y));
+  cudaFuncSetAttribute(wide_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes<1>);
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, wide_kernel<1, true>, &cfg) != cudaSuccess || n < 1) {
+    cudaGetLastError();
+    n = 0;
+  }
+  cache[ks] = n;
+  return n;
 }
 
 }  // namespace
@@ -544,10 +634,35 @@ cudaError_t launch_wide(const WeightView &W, const void *x, int64_t M, void *y, 
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (sms <= 0) sms = 1;
   const int64_t ntiles = (W.N + BN - 1) / BN;
-  const int64_t waves1 = (ntiles * ((M + BM - 1) / BM) + sms - 1) / sms;
-  const int64_t waves2 = (ntiles * ((M + 2 * BM - 1) / (2 * BM)) + sms - 1) / sms;
-  const bool two = M > BM && (double)waves2 * 1.5 < (double)waves1;
-  return two ? launch_wide_mma<2>(W, x16, M, inv_scale, y, st) : launch_wide_mma<1>(W, x16, M, inv_scale, y, st);
+  const int64_t tiles1 = ntiles * ((M + BM - 1) / BM);
+  // Cost in CTA-times of a single-tile CTA over all of K: whole waves of
+  // resident CTAs (one per SM) x the time of one CTA.  A CTA with two token
+  // tiles takes ~1.5x (measured); a split-K CTA 1/S of it plus its share of
+  // the cluster reduction.
+  double best = (double)((tiles1 + sms - 1) / sms);
+  int mode = 1, best_split = 1;
+  if (M > BM) {
+    const int64_t tiles2 = ntiles * ((M + 2 * BM - 1) / (2 * BM));
+    const double c2 = 1.5 * (double)((tiles2 + sms - 1) / sms);
+    if (c2 < best) {
+      best = c2;
+      mode = 2;
+    }
+  }
+  const int GK = (int)(W.K / 128);
+  for (int ks = 2; ks <= 8 && ks <= GK / 2; ++ks) {
+    const int active = wide_split_clusters(ks);
+    if (active < 1) continue;
+    const double c = (double)((tiles1 + active - 1) / active) * (1.0 / ks + 0.05);
+    if (c < 0.9 * best) {
+      best = c;
+      mode = 3;
+      best_split = ks;
+    }
+  }
+  if (mode == 2) return launch_wide_mma<2, false>(W, x16, M, inv_scale, y, 1, st);
+  if (mode == 3) return launch_wide_mma<1, true>(W, x16, M, inv_scale, y, best_split, st);
+  return launch_wide_mma<1, false>(W, x16, M, inv_scale, y, 1, st);
 }
 
 unsigned int read_and_clear_wide_errors(cudaStream_t st, cudaError_t *err) {
