@@ -59,6 +59,16 @@ def step_bytes(M, affine=False):
     return tot * LAYERS
 
 
+def chain_bytes(M):
+    """Algorithmic bytes of one token of the decode chain: every weight once;
+    per layer h and a in/out of the attention product, a in and the FFN
+    intermediate out of the gate/up launch, the intermediate in and h out of
+    the down launch (bf16)."""
+    w = sum(weight_bytes(N, K, False) for _, N, K in SHAPES)
+    act = M * 2 * (4 * D_MODEL + 2 * D_FF)
+    return (w + act) * LAYERS
+
+
 # ---------------------------------------------------------------------------
 # clocks
 # ---------------------------------------------------------------------------
@@ -386,6 +396,20 @@ def gpu_arm(args):
             s_ = run_timed(torch, gm, n, stream)
             sub[f"narrow_M{M}_GBps"] = round(step_bytes(M) * n / s_ / 1e9, 1)
             del gm
+        # the synthetic decode chain over the same 64 layers (attention-like
+        # product, then the fused FFN; 192 dependent launches per token), M = 1
+        chain = [(ws["attn"], ws["gate"], ws["up"], ws["down"]) for ws in layers]
+        gc = torch.Generator(device=device)
+        gc.manual_seed(1010)
+        xc = torch.randn((1, D_MODEL), generator=gc, device=device).to(torch.bfloat16)
+        yc = torch.empty_like(xc)
+        wsc = q1.decode_chain_workspace(1, D_MODEL, D_FF, device)
+        gm = time_graph(torch, lambda: q1.decode_chain(chain, xc, workspace=wsc, out=yc), 3, 3, stream)
+        n = max(20, args.steps // 10)
+        s_ = run_timed(torch, gm, n, stream)
+        sub["decode_chain_ms_per_token"] = round(s_ / n * 1e3, 4)
+        sub["decode_chain_GBps"] = round(chain_bytes(1) * n / s_ / 1e9, 1)
+        del gm, chain
         del layers
         torch.cuda.empty_cache()
         # affine metadata (bias stored): M = 1

@@ -202,6 +202,59 @@ q1_status q1_ffn_fused(const q1_weight *gate, const q1_weight *up, const q1_weig
   return cuda_status(e);
 }
 
+size_t q1_decode_chain_workspace_size(int64_t M, int64_t D, int64_t F_max) {
+  if (M < 1 || M > 8 || D < 128 || F_max < 128 || D % 128 || F_max % 128) return 0;
+  // a [M][D], the current h [M][D], the FFN intermediate [M][F_max], all bf16
+  return 2 * align256((size_t)(M * D * 2)) + align256((size_t)(M * F_max * 2));
+}
+
+q1_status q1_decode_chain(const q1_decode_layer *layers, int32_t n_layers, const void *x,
+                          int64_t M, q1_dtype dtype, void *y, void *workspace,
+                          size_t workspace_bytes, q1_stream stream) {
+  q1_status s = check_device();
+  if (s != Q1_OK) return s;
+  if (!layers || !x || !y) return Q1_ERR_NULL;
+  if (n_layers < 1) return Q1_ERR_SHAPE;
+  if (dtype != Q1_BF16) return Q1_ERR_DTYPE;
+  if (M < 1 || M > q1::kNarrowMaxM) return Q1_ERR_SHAPE;
+  const int64_t D = layers[0].attn.N;
+  int64_t F_max = 0;
+  for (int32_t l = 0; l < n_layers; ++l) {
+    const q1_decode_layer &L = layers[l];
+    if ((s = check_weight(&L.attn)) != Q1_OK || (s = check_weight(&L.gate)) != Q1_OK ||
+        (s = check_weight(&L.up)) != Q1_OK || (s = check_weight(&L.down)) != Q1_OK)
+      return s;
+    const int64_t F = L.gate.N;
+    if (L.attn.N != D || L.attn.K != D || L.gate.K != D || L.up.K != D || L.up.N != F ||
+        L.down.K != F || L.down.N != D)
+      return Q1_ERR_SHAPE;
+    if (D > q1::kNarrowMaxK || F > q1::kNarrowMaxK) return Q1_ERR_SHAPE;
+    F_max = F > F_max ? F : F_max;
+  }
+  if (!aligned(x, 16) || !aligned(y, 16)) return Q1_ERR_ALIGN;
+  s = check_ws(workspace, workspace_bytes, q1_decode_chain_workspace_size(M, D, F_max));
+  if (s != Q1_OK) return s;
+  cudaStream_t st = (cudaStream_t)stream;
+  char *ws = static_cast<char *>(workspace);
+  void *a = ws;
+  void *hb = ws + align256((size_t)(M * D * 2));
+  void *fh = ws + 2 * align256((size_t)(M * D * 2));
+  cudaError_t e = cudaSuccess;
+  for (int32_t l = 0; l < n_layers && e == cudaSuccess; ++l) {
+    const q1_decode_layer &L = layers[l];
+    const void *in = l == 0 ? x : hb;
+    void *out = l == n_layers - 1 ? y : hb;
+    // every kernel reads its input only after its predecessor has completed
+    // (griddepcontrol.wait), and each predecessor completed only after its own
+    // predecessor: the down projection overwrites hb after the attention
+    // product that read it is done
+    e = q1::launch_narrow(q1::view(&L.attn), in, M, a, st, true);
+    if (e == cudaSuccess) e = q1::launch_narrow_gate_up(q1::view(&L.gate), q1::view(&L.up), a, M, fh, st, true);
+    if (e == cudaSuccess) e = q1::launch_narrow(q1::view(&L.down), fh, M, out, st, true);
+  }
+  return cuda_status(e);
+}
+
 q1_status q1_check_symmetric(const q1_weight *W, int32_t *d_is_symmetric, q1_stream stream) {
   q1_status s = check_device();
   if (s != Q1_OK) return s;

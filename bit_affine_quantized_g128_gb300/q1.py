@@ -25,6 +25,7 @@ EXPORTED = [
     "q1_qmm_narrow", "q1_qmm", "q1_set_qmm_max_rows", "q1_get_qmm_max_rows",
     "q1_embed_gather", "q1_ffn_workspace_size", "q1_ffn_fused", "q1_check_symmetric",
     "q1_device_errors", "q1_status_string", "q1_ffn_fused_noalloc",
+    "q1_decode_chain_workspace_size", "q1_decode_chain",
 ]
 
 
@@ -37,6 +38,10 @@ class Q1Error(RuntimeError):
 class _CWeight(ctypes.Structure):
     _fields_ = [("w", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("biases", ctypes.c_void_p),
                 ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("group_size", ctypes.c_int32)]
+
+
+class _CLayer(ctypes.Structure):
+    _fields_ = [("attn", _CWeight), ("gate", _CWeight), ("up", _CWeight), ("down", _CWeight)]
 
 
 _lib = None
@@ -73,6 +78,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "q1_ffn_fused": ([W, W, W, P, I64, I32, P, P, SZ, P], I32),
         "q1_ffn_fused_noalloc": ([W, W, W, P, I64, I32, P, P], I32),
         "q1_check_symmetric": ([W, P, P], I32),
+        "q1_decode_chain_workspace_size": ([I64, I64, I64], SZ),
+        "q1_decode_chain": ([ctypes.POINTER(_CLayer), I32, P, I64, I32, P, P, SZ, P], I32),
         "q1_device_errors": ([ctypes.POINTER(ctypes.c_uint), P], I32),
         "q1_status_string": ([I32], ctypes.c_char_p),
     }
@@ -255,6 +262,29 @@ def ffn_fused_noalloc(gate: Q1Weight, up: Q1Weight, down: Q1Weight, x: torch.Ten
 def ffn_h(ws: torch.Tensor, M: int, F: int) -> torch.Tensor:
     """The bf16 intermediate h [M, F] that the last q1_ffn_fused left in `ws`."""
     return ws[: M * F * 2].view(torch.bfloat16).reshape(M, F)
+
+
+def decode_chain_workspace(M: int, D: int, F_max: int, device) -> torch.Tensor:
+    n = lib().q1_decode_chain_workspace_size(M, D, F_max)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def decode_chain(layers, x: torch.Tensor, workspace=None, out=None) -> torch.Tensor:
+    """q1_decode_chain: layers is a sequence of (attn, gate, up, down) Q1Weights;
+    per layer a = attn . h, then h = down . (SiLU(gate . a) * (up . a))."""
+    layers = list(layers)
+    lead = x.shape[:-1]
+    D = layers[0][0].N
+    x2 = _flat(x, D)
+    M = x2.shape[0]
+    arr = (_CLayer * len(layers))(*[_CLayer(a._c, g._c, u._c, d._c) for (a, g, u, d) in layers])
+    y = out if out is not None else torch.empty((M, D), dtype=x.dtype, device=x.device)
+    if workspace is None:
+        workspace = decode_chain_workspace(M, D, max(g.N for (_, g, _, _) in layers), x.device)
+    _check("q1_decode_chain", lib().q1_decode_chain(arr, len(layers), x2.data_ptr(), M, _DT[x.dtype],
+                                                    y.data_ptr(), workspace.data_ptr(),
+                                                    workspace.numel(), _stream()))
+    return y.reshape(*lead, D)
 
 
 def check_symmetric(W: Q1Weight) -> torch.Tensor:

@@ -167,6 +167,34 @@ q1_status q1_ffn_fused(const q1_weight *gate, const q1_weight *up, const q1_weig
 q1_status q1_ffn_fused_noalloc(const q1_weight *gate, const q1_weight *up, const q1_weight *down,
                                const void *x, int64_t M, q1_dtype dtype, void *y, q1_stream stream);
 
+/* ---- synthetic decode chain -----------------------------------------------
+ * The Q1 linears of a decode step, layer after layer ("Support Bonsai-27B
+ * affine Q1", higgs PR #212, section "Measured impact": decode time of a
+ * model whose linears are all Q1; no attention, norms or residuals, so it is
+ * not a model).  For l = 0 .. n_layers-1, with h_0 = x:
+ *   a       = attn_l . h_l                               (the narrow product)
+ *   h_{l+1} = down_l . (SiLU(gate_l . a) * (up_l . a))   (the fused FFN)
+ * and y = h_{n_layers}.  Every intermediate is bf16, and the result is exactly
+ * that of the same q1_qmm_narrow and q1_ffn_fused calls made one by one (same
+ * kernels, same order).  All launches are chained with programmatic dependent
+ * launch, so each one streams its weights while its predecessor drains.
+ * layers: host array of n_layers >= 1 entries (the weights inside are device
+ * memory).  Every layer has the same D (attn [D][D]; gate, up [F_l][D];
+ * down [D][F_l]); F_l may differ.  1 <= M <= 8; D, F_l <= 40960.
+ * x, y [M][D] bf16, 16-byte aligned; y must not overlap x or the workspace.
+ * Workspace: q1_decode_chain_workspace_size(M, D, max F_l) bytes, 256-byte
+ * aligned (a, the current h and the FFN intermediate). */
+typedef struct {
+  q1_weight attn; /* [D][D] */
+  q1_weight gate; /* [F][D] */
+  q1_weight up;   /* [F][D] */
+  q1_weight down; /* [D][F] */
+} q1_decode_layer;
+size_t q1_decode_chain_workspace_size(int64_t M, int64_t D, int64_t F_max);
+q1_status q1_decode_chain(const q1_decode_layer *layers, int32_t n_layers, const void *x,
+                          int64_t M, q1_dtype dtype, void *y, void *workspace,
+                          size_t workspace_bytes, q1_stream stream);
+
 /* ---- symmetric check (higgs PR #212, walkthrough: symmetric bias
  * compaction and validation) -------------------------------------------------
  * Writes 1 to *d_is_symmetric (device int32) iff every stored bias equals

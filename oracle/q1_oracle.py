@@ -177,6 +177,29 @@ def ffn(x, gate, up, down, rows=None) -> np.ndarray:
     return y, h
 
 
+def decode_chain(x, layers) -> torch.Tensor:
+    """Synthetic decode chain: the Q1 linears of a decode step, layer after layer
+    ("Support Bonsai-27B affine Q1", section "Measured impact": the decode time
+    of a model whose linears are all Q1; no attention, norms or residuals).
+
+    Per layer, with h_0 = x: a = attn . h_l, then
+    h_{l+1} = Down . (SiLU(Gate . a) * (Up . a)).  The chain passes bf16
+    activations from one call to the next (every call takes and returns bf16
+    activations), so a and h_{l+1} are each rounded once to bf16; inside a
+    product and inside the FFN nothing is rounded (fp64, as in qmm and ffn).
+
+    layers: sequence of (attn, gate, up, down), each a (words, scales, biases,
+    K) tuple.  x: [M, D].  Returns h_L as a bf16 tensor [M, D].
+    """
+    h = x if isinstance(x, torch.Tensor) else torch.from_numpy(np.asarray(x))
+    h = h.to(torch.bfloat16)
+    for attn, gate, up, down in layers:
+        a = round_to(qmm(h, *attn), "bf16")
+        y, _ = ffn(a, gate, up, down)
+        h = round_to(y, "bf16")
+    return h
+
+
 # ---------------------------------------------------------------------------
 # Embedding gather ("Support Bonsai-27B affine Q1": Q1 embeddings, tied head)
 # ---------------------------------------------------------------------------

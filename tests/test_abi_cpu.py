@@ -52,6 +52,12 @@ def test_library_loads_and_host_only_calls_work(libpath):
     lib.q1_ffn_workspace_size.argtypes = [ctypes.c_int64] * 3
     assert lib.q1_ffn_workspace_size(8, 5120, 17408) == 8 * 17408 * 2
     assert lib.q1_ffn_workspace_size(9, 5120, 17408) == 0
+    lib.q1_decode_chain_workspace_size.restype = ctypes.c_size_t
+    lib.q1_decode_chain_workspace_size.argtypes = [ctypes.c_int64] * 3
+    # a and h [M][D] plus the FFN intermediate [M][F_max], bf16, each 256-byte aligned
+    assert lib.q1_decode_chain_workspace_size(1, 5120, 17408) == 2 * 10240 + 34816
+    assert lib.q1_decode_chain_workspace_size(3, 128, 384) == 2 * 768 + 2304
+    assert lib.q1_decode_chain_workspace_size(9, 5120, 17408) == 0
     lib.q1_set_qmm_max_rows(3)
     assert lib.q1_get_qmm_max_rows() == 3
     lib.q1_set_qmm_max_rows(100)

@@ -10,7 +10,7 @@ import torch
 
 from oracle import q1_oracle as O
 from bit_affine_quantized_g128_gb300 import synth
-from tests.tolerance import check_matmul
+from tests.tolerance import check_chain, check_matmul
 
 pytestmark = pytest.mark.gpu
 
@@ -320,6 +320,85 @@ def test_ffn_fused(q1, M, D, F):
     h = q1.ffn_h(ws, M, F).float().cpu().double().numpy()
     assert np.linalg.norm(h - ho) / np.linalg.norm(ho) < 5e-3
     check_matmul(y, yo, ho, O.dequantize_f32(down.words, down.scales, None, F), f"ffn M={M}")
+
+
+# ------------------------------------------------------------------ decode chain
+def _scaled(t, factor):
+    """The same bits with the metadata multiplied by `factor` (fp16): products
+    of these shapes then keep activations of order one through the chain."""
+    s = (t.scales.astype(np.float32) * factor).astype(np.float16)
+    b = None if t.biases is None else (t.biases.astype(np.float32) * factor).astype(np.float16)
+    return synth.Q1Tensor(t.words, s, b, t.K)
+
+
+def _chain_host(D, Fs, seed, affine=()):
+    layers = []
+    for l, F in enumerate(Fs):
+        base = seed + 10 * l
+        layers.append((
+            _scaled(synth.q1_tensor(D, D, seed=base, affine=("attn", l) in affine), 7.0),
+            _scaled(synth.q1_tensor(F, D, seed=base + 1, affine=("gate", l) in affine), 7.0),
+            _scaled(synth.q1_tensor(F, D, seed=base + 2, affine=("up", l) in affine), 7.0),
+            _scaled(synth.q1_tensor(D, F, seed=base + 3, affine=("down", l) in affine), 7.0)))
+    return layers
+
+
+@pytest.mark.parametrize("M", [1, 3, 8])
+def test_decode_chain_equals_the_calls_made_one_by_one(q1, M):
+    D, Fs = 256, [384, 256, 512]
+    host = _chain_host(D, Fs, seed=400, affine={("attn", 1), ("up", 2), ("down", 0)})
+    dev = [tuple(q1.Q1Weight.from_host(w) for w in L) for L in host]
+    x = synth.activations(M, D, seed=409).to(DEV)
+    y = q1.decode_chain(dev, x)
+    h = x
+    for A, G, U, Dn in dev:
+        a = q1.qmm_narrow(A, h)
+        h = q1.ffn_fused(G, U, Dn, a)
+    torch.cuda.synchronize()
+    assert torch.equal(y, h), "the chain differs from the same calls made one by one"
+    assert float(y.float().abs().max()) > 0
+
+
+@pytest.mark.parametrize("M", [1, 4])
+def test_decode_chain_oracle(q1, M):
+    D, Fs = 256, [512, 384]
+    host = _chain_host(D, Fs, seed=430)
+    dev = [tuple(q1.Q1Weight.from_host(w) for w in L) for L in host]
+    x = synth.activations(M, D, seed=439)
+    y = q1.decode_chain(dev, x.to(DEV))
+    tup = lambda t: (t.words, t.scales, t.biases, t.K)
+    layers = [tuple(tup(w) for w in L) for L in host]
+    yo = O.decode_chain(x, layers)
+    # the last product's input: the oracle's FFN intermediate of the last layer
+    h_prev = O.decode_chain(x, layers[:-1]) if len(layers) > 1 else x
+    attn, gate, up, down = layers[-1]
+    a = O.round_to(O.qmm(h_prev, *attn), "bf16")
+    _, h_last = O.ffn(a, gate, up, down)
+    wd = O.dequantize_f32(down[0], down[1], down[2], down[3])
+    check_chain(y, yo.double().numpy(), h_last, wd, stages=3 * len(layers), what=f"chain M={M}")
+
+
+def test_decode_chain_rejects_bad_arguments(q1):
+    D = 256
+    host = _chain_host(D, [256], seed=450)
+    dev = [tuple(q1.Q1Weight.from_host(w) for w in L) for L in host]
+    x = synth.activations(2, D, seed=459).to(DEV)
+    y = torch.empty_like(x)
+    lib = q1.lib()
+    arr = (q1._CLayer * 1)(q1._CLayer(*(w._c for w in dev[0])))
+    ws = q1.decode_chain_workspace(2, D, 256, DEV)
+    st = torch.cuda.current_stream().cuda_stream
+    call = lambda layers, n, M, nbytes: lib.q1_decode_chain(layers, n, x.data_ptr(), M, 0, y.data_ptr(),
+                                                            ws.data_ptr(), nbytes, st)
+    assert call(arr, 0, 2, ws.numel()) == 2          # no layers
+    assert call(arr, 1, 9, ws.numel()) == 2          # M > 8
+    assert call(arr, 1, 2, 256) == 6                 # workspace too small
+    bad = _chain_host(D, [256], seed=460)
+    bad[0] = (synth.q1_tensor(128, D, seed=461, affine=False),) + bad[0][1:]  # attn not [D][D]
+    bdev = [tuple(q1.Q1Weight.from_host(w) for w in L) for L in bad]
+    barr = (q1._CLayer * 1)(q1._CLayer(*(w._c for w in bdev[0])))
+    assert call(barr, 1, 2, ws.numel()) == 2
+    torch.cuda.synchronize()
 
 
 # ------------------------------------------------------------------ symmetric check

@@ -265,6 +265,44 @@ def test_ffn_brute_force_tiny():
     np.testing.assert_allclose(y, want, rtol=1e-10, atol=1e-12)
 
 
+# ---------------------------------------------------------------- decode chain
+def _selection(rows, K, sel):
+    """Affine Q1 tensor whose dequantized row n is the one-hot e_{sel[n]}:
+    scale 1, bias 0, bit sel[n] of row n set (packed here by hand)."""
+    words = np.zeros((rows, K // 32), dtype=np.uint32)
+    for n, k in enumerate(sel):
+        words[n, k // 32] |= np.uint32(1) << np.uint32(k % 32)
+    scales = np.full((rows, K // 128), np.float16(1.0))
+    biases = np.zeros((rows, K // 128), dtype=np.float16)
+    return (words, scales, biases, K)
+
+
+def test_decode_chain_on_selection_matrices():
+    """With one-hot weight rows every product is a gather: a = h[pi], g = a[rho],
+    u = a[sigma], h' = bf16(SiLU(g) * u)[tau].  Distinct random index maps per
+    layer catch a transposed operand, a swapped gate/up or a wrong layer order."""
+    D, F, M, L = 128, 256, 2, 2
+    rng = np.random.default_rng(77)
+    x = synth.activations(M, D, seed=78)
+    layers, maps = [], []
+    for _ in range(L):
+        pi = rng.permutation(D)
+        rho, sigma = rng.integers(0, D, F), rng.integers(0, D, F)
+        tau = rng.permutation(F)[:D]
+        layers.append((_selection(D, D, pi), _selection(F, D, rho), _selection(F, D, sigma),
+                       _selection(D, F, tau)))
+        maps.append((pi, rho, sigma, tau))
+    h = x.to(torch.float64)
+    for pi, rho, sigma, tau in maps:
+        a = h[:, pi]                       # exact: each output is one input value
+        hh = torch.nn.functional.silu(a[:, rho]) * a[:, sigma]
+        # one rounding to bf16 (through fp32, as the pinned bf16 rounding does)
+        h = hh[:, tau].to(torch.float32).to(torch.bfloat16).to(torch.float64)
+    got = O.decode_chain(x, layers)
+    assert got.dtype == torch.bfloat16
+    assert torch.equal(got.to(torch.float64), h)
+
+
 # ---------------------------------------------------------------- gather
 def test_embed_gather_rows_and_out_of_range():
     V, K = 10, 256
