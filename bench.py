@@ -421,6 +421,24 @@ def gpu_arm(args):
         sub["affine_M1_GBps"] = round(step_bytes(1, True) * n / s_ / 1e9, 1)
         del gm, la
         torch.cuda.empty_cache()
+        # exact repack of a dense bf16 projection (17408 x 5120) into Q1:
+        # GB/s of the dense read plus the words and scales written
+        W0 = q1.Q1Weight(synth.device_weight_words(D_FF, D_MODEL, 4242, device),
+                         synth.device_scales(D_FF, D_MODEL, 4243, device), None, D_MODEL)
+        dense = q1.dequantize(W0, torch.bfloat16)
+        bad = torch.zeros((1,), dtype=torch.int32, device=device)
+        Wr = q1.Q1Weight(torch.empty_like(W0.words), torch.empty_like(W0.scales), None, D_MODEL)
+        per = 10  # calls per graph replay
+        gm = time_graph(torch, lambda: [q1.pack_from_dense(dense, True, bad=bad, out=Wr) for _ in range(per)],
+                        3, 3, stream)
+        reps = 5
+        t_rp = run_timed(torch, gm, reps, stream) / (reps * per)
+        assert int(bad.item()) == 0 and torch.equal(Wr.words, W0.words)
+        del gm
+        rp_bytes = D_FF * D_MODEL * 2 + weight_bytes(D_FF, D_MODEL, False)
+        sub["repack_bf16_17408x5120_GBps"] = round(rp_bytes / t_rp / 1e9, 1)
+        del W0, dense
+        torch.cuda.empty_cache()
         # prefill on the tensor cores
         for M in (128, 2048):
             for shp in (SHAPES[0], SHAPES[2]):

@@ -255,6 +255,22 @@ q1_status q1_decode_chain(const q1_decode_layer *layers, int32_t n_layers, const
   return cuda_status(e);
 }
 
+q1_status q1_pack_from_dense(const void *dense, q1_dtype in_t, int64_t N, int64_t K, uint32_t *w,
+                             uint16_t *scales, uint16_t *biases, int32_t *d_bad_groups,
+                             q1_stream stream) {
+  q1_status s = check_device();
+  if (s != Q1_OK) return s;
+  if (!dense || !w || !scales || !d_bad_groups) return Q1_ERR_NULL;
+  if (in_t != Q1_BF16 && in_t != Q1_F16 && in_t != Q1_F32) return Q1_ERR_DTYPE;
+  if (N < 1 || K < 128 || K % 128 != 0 || K > (int64_t)1 << 24 || N > ((int64_t)1 << 31) - 1)
+    return Q1_ERR_SHAPE;
+  if (!aligned(dense, 16) || !aligned(w, 16) || !aligned(scales, 2) || (biases && !aligned(biases, 2)) ||
+      !aligned(d_bad_groups, 4))
+    return Q1_ERR_ALIGN;
+  return cuda_status(q1::launch_pack_from_dense(dense, in_t, N, K, w, scales, biases, d_bad_groups,
+                                                (cudaStream_t)stream));
+}
+
 q1_status q1_check_symmetric(const q1_weight *W, int32_t *d_is_symmetric, q1_stream stream) {
   q1_status s = check_device();
   if (s != Q1_OK) return s;

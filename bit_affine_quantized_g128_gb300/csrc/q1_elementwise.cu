@@ -1,5 +1,5 @@
-// Elementwise Q1 kernels: pack, unpack, dequantize, embedding gather and the
-// symmetric-metadata check.  All of them are HBM-bound streams: one thread per
+// Elementwise Q1 kernels: pack, unpack, dequantize, embedding gather, the
+// symmetric-metadata check and the exact repack of dense tensors.  All of them are HBM-bound streams: one thread per
 // packed 32-bit word, 16-byte loads/stores, grid-stride loops over a grid
 // sized in multiples of the SM count.
 //
@@ -196,6 +196,189 @@ __global__ void check_symmetric_kernel(const uint16_t *__restrict__ s,
   if (__syncthreads_or(mismatch) && threadIdx.x == 0) *result = 0;
 }
 
+// ---- exact repack from dense ("Bonsai masked gemv", cactus PR #775: tensors
+// whose 128-groups hold exactly two values repack with zero quantization error;
+// anything else is refused).  One warp per group; lane l holds the group's
+// values 4l .. 4l+3 as fp32 bit patterns (bf16 and fp16 widen exactly, so
+// patterns compare like the input's).
+
+// One fp16 step along the number line (nextafter toward +inf or -inf) of a
+// finite fp16 bit pattern.
+__device__ __forceinline__ uint32_t f16_next(uint32_t h, bool up) {
+  if ((h & 0x7FFFu) == 0u) return up ? 0x0001u : 0x8001u;  // from +-0 to +-(smallest subnormal)
+  const bool neg = (h & 0x8000u) != 0u;
+  return (up != neg) ? h + 1u : h - 1u;
+}
+
+// The fp32 bit patterns of lane l's values 4l .. 4l+3 of the group at element e0.
+template <int DT>
+__device__ __forceinline__ void load_group(const void *__restrict__ dense, int64_t e0, uint32_t (&p)[4]) {
+  if (DT == 2) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(static_cast<const float *>(dense) + e0));
+    p[0] = v.x; p[1] = v.y; p[2] = v.z; p[3] = v.w;
+  } else {
+    const uint2 v = __ldg(reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(dense) + e0));
+    p[0] = v.x & 0xFFFFu; p[1] = v.x >> 16; p[2] = v.y & 0xFFFFu; p[3] = v.y >> 16;
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ void widen(uint32_t (&p)[4]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if (DT == 0) p[j] <<= 16;
+    if (DT == 1) p[j] = __float_as_uint(__half2float(__ushort_as_half((uint16_t)p[j])));
+  }
+}
+
+// The metadata of one group from its values A and B (B == A: one value):
+// scale, bias, the pattern whose weights get bit 1 (two values) or whether
+// all bits are 1 (one value); false when the group is refused.
+__device__ __forceinline__ bool group_meta(uint32_t A, uint32_t B, bool two, bool ok, int symmetric,
+                                           uint32_t &hi_pat, bool &allone, uint32_t &sc, uint32_t &bi) {
+  hi_pat = 0u;
+  allone = false;
+  sc = 0u;
+  bi = 0u;
+  if (ok && !two) {
+    const float x = __uint_as_float(A);
+    if (symmetric) {
+      const bool neg = (A >> 31) != 0u;
+      sc = __half_as_ushort(__float2half_rn(__fmul_rn(neg ? -2.0f : 2.0f, x)));
+      const float sf = __half2float(__ushort_as_half((uint16_t)sc));
+      const float bb = __fmul_rn(-0.5f, sf);
+      ok = __float_as_uint(neg ? bb : __fadd_rn(sf, bb)) == A;
+      allone = !neg;
+    } else {
+      bi = __half_as_ushort(__float2half_rn(x));
+      ok = __float_as_uint(__half2float(__ushort_as_half((uint16_t)bi))) == A;
+    }
+  } else if (ok) {
+    const float fa = __uint_as_float(A), fb = __uint_as_float(B);
+    const bool a_lo = fa < fb || (fa == fb && (A >> 31) != 0u);  // -0 below +0
+    const uint32_t lo_pat = a_lo ? A : B;
+    hi_pat = a_lo ? B : A;
+    const float lo = __uint_as_float(lo_pat), hi = __uint_as_float(hi_pat);
+    if (symmetric) {
+      sc = __half_as_ushort(__float2half_rn(__fmul_rn(-2.0f, lo)));
+      const float sf = __half2float(__ushort_as_half((uint16_t)sc));
+      const float bb = __fmul_rn(-0.5f, sf);
+      ok = __float_as_uint(bb) == lo_pat && __float_as_uint(__fadd_rn(sf, bb)) == hi_pat;
+    } else {
+      bi = __half_as_ushort(__float2half_rn(lo));
+      const float bf = __half2float(__ushort_as_half((uint16_t)bi));
+      ok = __float_as_uint(bf) == lo_pat;
+      if (ok) {
+        // scales tried: RN16(hi - lo), then one step down, one up, two down, two up
+        const uint32_t c0 = __half_as_ushort(__float2half_rn(__fsub_rn(hi, lo)));
+        const uint32_t dn1 = f16_next(c0, false), up1 = f16_next(c0, true);
+        const uint32_t cands[5] = {c0, dn1, up1, f16_next(dn1, false), f16_next(up1, true)};
+        ok = false;
+#pragma unroll
+        for (int t = 0; t < 5; ++t) {
+          if (ok || (cands[t] & 0x7C00u) == 0x7C00u) continue;
+          const float sf = __half2float(__ushort_as_half((uint16_t)cands[t]));
+          if (__float_as_uint(__fadd_rn(sf, bf)) == hi_pat) {
+            ok = true;
+            sc = cands[t];
+          }
+        }
+      }
+    }
+  }
+  if (!ok) {
+    sc = 0u;
+    bi = 0u;
+  }
+  return ok;
+}
+
+// One warp per run of kRepackRun consecutive groups.  All the run's loads are
+// issued first (bytes in flight); then, per group, the warp finds its values
+// (lane 0's first value A; B = the first value that differs, by ballot; a
+// vote refuses a third); then lane u works out the metadata of group u of the
+// run, once; then each group's decisions are broadcast and its bits packed.
+constexpr int kRepackRun = 8;
+
+template <int DT>  // input: 0 bf16, 1 fp16, 2 fp32
+__global__ void pack_from_dense_kernel(const void *__restrict__ dense, int64_t N, int64_t K,
+                                       int symmetric, uint32_t *__restrict__ w,
+                                       uint16_t *__restrict__ s, uint16_t *__restrict__ b,
+                                       int32_t *__restrict__ bad) {
+  const unsigned FULL = 0xFFFFFFFFu;
+  const int lane = threadIdx.x & 31;
+  const int me = lane & (kRepackRun - 1);
+  const int64_t ngroups = N * (K / 128);
+  const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t grp0 = (((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * kRepackRun; grp0 < ngroups;
+       grp0 += nw * kRepackRun) {
+    // groups are numbered row-major (n * G + g), so a run is contiguous in
+    // memory: group grp starts at element grp * 128
+    uint32_t p[kRepackRun][4];
+#pragma unroll
+    for (int u = 0; u < kRepackRun; ++u) {
+      if (grp0 + u < ngroups) load_group<DT>(dense, (grp0 + u) * 128 + 4 * lane, p[u]);
+      else p[u][0] = p[u][1] = p[u][2] = p[u][3] = 0u;
+    }
+    // per group: the values A, B and the vote
+    uint32_t mA = 0u, mB = 0u;
+    bool mtwo = false, mok = false;
+#pragma unroll
+    for (int u = 0; u < kRepackRun; ++u) {
+      widen<DT>(p[u]);
+      const uint32_t A = __shfl_sync(FULL, p[u][0], 0);
+      uint32_t cand = A;
+      bool has = false;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (!has && p[u][j] != A) { cand = p[u][j]; has = true; }
+      const uint32_t hb = __ballot_sync(FULL, has);
+      const uint32_t B = hb ? __shfl_sync(FULL, cand, __ffs(hb) - 1) : A;
+      bool viol = false;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) viol |= p[u][j] != A && p[u][j] != B;
+      const bool finite = (A & 0x7F800000u) != 0x7F800000u && (B & 0x7F800000u) != 0x7F800000u;
+      const bool ok = !__any_sync(FULL, viol) && finite;
+      if (me == u) {
+        mA = A;
+        mB = B;
+        mtwo = hb != 0u;
+        mok = ok;
+      }
+    }
+    // lane u (and its copies u + 8, u + 16, u + 24): group u's metadata
+    uint32_t hi_pat, sc, bi;
+    bool allone;
+    const bool ok = group_meta(mA, mB, mtwo, mok, symmetric, hi_pat, allone, sc, bi);
+    const int64_t my = grp0 + me;
+    if (lane < kRepackRun && my < ngroups) {
+      s[my] = (uint16_t)sc;
+      if (b) b[my] = (uint16_t)bi;
+      if (!ok) atomicAdd(bad, 1);
+    }
+    // the bits: weights equal to hi (two values) or the single value's rule;
+    // word l / 8 of a group takes lane l's nibble at bits 4 (l % 8) .. +3
+#pragma unroll
+    for (int u = 0; u < kRepackRun; ++u) {
+      const int64_t grp = grp0 + u;
+      if (grp >= ngroups) break;  // uniform across the warp
+      const uint32_t hp = __shfl_sync(FULL, hi_pat, u);
+      const int mode = __shfl_sync(FULL, ok ? (mtwo ? 2 : (allone ? 1 : 0)) : 0, u);
+      uint32_t nib = 0u;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const bool bit = mode == 2 ? p[u][j] == hp : mode == 1;
+        nib |= (bit ? 1u : 0u) << j;
+      }
+      uint32_t word = nib << (4 * (lane & 7));
+      word |= __shfl_xor_sync(FULL, word, 1);
+      word |= __shfl_xor_sync(FULL, word, 2);
+      word |= __shfl_xor_sync(FULL, word, 4);
+      if ((lane & 7) == 0) w[grp * 4 + (lane >> 3)] = word;
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_pack(const uint8_t *bits, int64_t N, int64_t K, uint32_t *w, cudaStream_t st) {
@@ -246,6 +429,19 @@ cudaError_t launch_check_symmetric(const WeightView &W, int32_t *result, cudaStr
   if (e != cudaSuccess) return e;
   int64_t count = W.N * (W.K / 128);
   check_symmetric_kernel<<<grid_for(count, 256), 256, 0, st>>>(W.s, W.b, count, result);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_from_dense(const void *dense, q1_dtype t, int64_t N, int64_t K, uint32_t *w,
+                                   uint16_t *s, uint16_t *b, int32_t *bad, cudaStream_t st) {
+  const int64_t groups = N * (K / 128);
+  const unsigned g = grid_for((groups + kRepackRun - 1) / kRepackRun * 32, 256);
+  const int sym = b == nullptr ? 1 : 0;
+  switch (t) {
+    case Q1_BF16: pack_from_dense_kernel<0><<<g, 256, 0, st>>>(dense, N, K, sym, w, s, b, bad); break;
+    case Q1_F16: pack_from_dense_kernel<1><<<g, 256, 0, st>>>(dense, N, K, sym, w, s, b, bad); break;
+    default: pack_from_dense_kernel<2><<<g, 256, 0, st>>>(dense, N, K, sym, w, s, b, bad); break;
+  }
   return cudaGetLastError();
 }
 

@@ -35,6 +35,10 @@ cudaError_t launch_dequantize(const WeightView &W, q1_dtype t, void *out, cudaSt
 cudaError_t launch_gather(const WeightView &E, const int32_t *ids, int64_t T, q1_dtype t,
                           void *out, int32_t *bad, cudaStream_t st);
 cudaError_t launch_check_symmetric(const WeightView &W, int32_t *result, cudaStream_t st);
+// w/s/b [N][K/32], [N][K/128]: the exact Q1 form of dense [N][K] (b == nullptr:
+// symmetric); refused groups are zeroed and counted in *bad.
+cudaError_t launch_pack_from_dense(const void *dense, q1_dtype t, int64_t N, int64_t K, uint32_t *w,
+                                   uint16_t *s, uint16_t *b, int32_t *bad, cudaStream_t st);
 
 // ---- narrow path (q1_narrow.cu): one launch, no scratch
 // y [M][N] bf16 = x . W^T (x [M][K] bf16).

@@ -25,7 +25,7 @@ EXPORTED = [
     "q1_qmm_narrow", "q1_qmm", "q1_set_qmm_max_rows", "q1_get_qmm_max_rows",
     "q1_embed_gather", "q1_ffn_workspace_size", "q1_ffn_fused", "q1_check_symmetric",
     "q1_device_errors", "q1_status_string", "q1_ffn_fused_noalloc",
-    "q1_decode_chain_workspace_size", "q1_decode_chain",
+    "q1_decode_chain_workspace_size", "q1_decode_chain", "q1_pack_from_dense",
 ]
 
 
@@ -79,6 +79,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "q1_ffn_fused_noalloc": ([W, W, W, P, I64, I32, P, P], I32),
         "q1_check_symmetric": ([W, P, P], I32),
         "q1_decode_chain_workspace_size": ([I64, I64, I64], SZ),
+        "q1_pack_from_dense": ([P, I32, I64, I64, P, P, P, P, P], I32),
         "q1_decode_chain": ([ctypes.POINTER(_CLayer), I32, P, I64, I32, P, P, SZ, P], I32),
         "q1_device_errors": ([ctypes.POINTER(ctypes.c_uint), P], I32),
         "q1_status_string": ([I32], ctypes.c_char_p),
@@ -262,6 +263,30 @@ def ffn_fused_noalloc(gate: Q1Weight, up: Q1Weight, down: Q1Weight, x: torch.Ten
 def ffn_h(ws: torch.Tensor, M: int, F: int) -> torch.Tensor:
     """The bf16 intermediate h [M, F] that the last q1_ffn_fused left in `ws`."""
     return ws[: M * F * 2].view(torch.bfloat16).reshape(M, F)
+
+
+def pack_from_dense(dense: torch.Tensor, symmetric: bool, bad: Optional[torch.Tensor] = None,
+                    out: Optional[Q1Weight] = None):
+    """q1_pack_from_dense: the exact Q1 form of a dense [N, K] bf16/f16/f32
+    tensor.  Returns (Q1Weight, bad), bad a device int32 [1] that counts the
+    refused groups (added to `bad` when given).  `out` (a Q1Weight of the same
+    shape, with biases unless symmetric) receives the result in place."""
+    d = dense.contiguous()
+    N, K = int(d.shape[0]), int(d.shape[1])
+    dev = d.device
+    if out is None:
+        w = torch.empty((N, K // 32), dtype=torch.int32, device=dev)
+        s = torch.empty((N, K // 128), dtype=torch.float16, device=dev)
+        b = None if symmetric else torch.empty((N, K // 128), dtype=torch.float16, device=dev)
+        out = Q1Weight(w, s, b, K)
+    elif out.N != N or out.K != K or (out.biases is None) != symmetric:
+        raise ValueError("pack_from_dense: `out` does not match the dense shape or mode")
+    if bad is None:
+        bad = torch.zeros((1,), dtype=torch.int32, device=dev)
+    _check("q1_pack_from_dense", lib().q1_pack_from_dense(d.data_ptr(), _DT[d.dtype], N, K, out.words.data_ptr(),
+                                                          out.scales.data_ptr(), _ptr(out.biases),
+                                                          bad.data_ptr(), _stream()))
+    return out, bad
 
 
 def decode_chain_workspace(M: int, D: int, F_max: int, device) -> torch.Tensor:

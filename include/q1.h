@@ -92,6 +92,31 @@ q1_status q1_unpack(const uint32_t *w, int64_t N, int64_t K, uint8_t *bits, q1_s
  * once to nearest-even.  out 16-byte aligned.  Bit-exact. */
 q1_status q1_dequantize(const q1_weight *W, q1_dtype out_t, void *out, q1_stream stream);
 
+/* ---- exact repack from dense ("Bonsai masked gemv", cactus PR #775: tensors
+ * whose 128-groups hold exactly {-s,+s} are repacked with the checkpoint's own
+ * scales and zero quantization error; non-binary tensors are not) -----------
+ * dense [N][K] in in_t (Q1_BF16, Q1_F16 or Q1_F32), device, 16-byte aligned.
+ * Writes w [N][K/32] (16-byte aligned), scales [N][K/128] fp16 and, unless
+ * biases is NULL, biases [N][K/128] fp16.  biases == NULL asks for the
+ * symmetric form.  Per group of 128, values are compared by bit pattern (+0
+ * and -0 differ; a NaN or infinity refuses the group):
+ *   - more than two values: refused;
+ *   - two values lo < hi (-0 < +0): bit 1 where the value is hi;
+ *       symmetric: scale = RN16(-2 lo), kept if -0.5*scale == lo and
+ *         fl32(scale - 0.5*scale) == hi bit for bit;
+ *       affine: bias = RN16(lo), which must equal lo; scale = the first of
+ *         RN16(fl32(hi - lo)), one fp16 step down, one up, two down, two up
+ *         with fl32(scale + bias) == hi bit for bit;
+ *   - one value v: symmetric: scale = RN16(2v) with all bits 1 when v's sign
+ *     bit is clear, else RN16(-2v) with all bits 0 (kept if exact); affine:
+ *     bias = v (must be an fp16 value), scale = +0, all bits 0.
+ * A kept group dequantizes (q1_dequantize with out_t = in_t) to exactly the
+ * input bits.  A refused group gets zero words, scale and bias and adds 1 to
+ * *d_bad_groups (device int32, required; the caller zeroes it). */
+q1_status q1_pack_from_dense(const void *dense, q1_dtype in_t, int64_t N, int64_t K, uint32_t *w,
+                             uint16_t *scales, uint16_t *biases, int32_t *d_bad_groups,
+                             q1_stream stream);
+
 /* ---- matmul: y[M][N] = x[M][K] . Wd^T ------------------------------------
  * fp32 accumulation, bf16 in and out.  x and y 16-byte aligned.
  * q1_qmv: the M = 1 decode product (higgs PR #212, "What": the Q1 decode tile).

@@ -226,6 +226,123 @@ def embed_gather(ids, words, scales, biases, K: int, dtype: str = "bf16"):
 
 
 # ---------------------------------------------------------------------------
+# Exact repack from dense ("Bonsai masked gemv", cactus PR #775: tensors whose
+# 128-groups hold exactly two values repack with zero quantization error;
+# anything else is refused)
+# ---------------------------------------------------------------------------
+# Order in which fp16 scales around RN16(hi - lo) are tried, in fp16 steps.
+SCALE_STEPS = (0, -1, 1, -2, 2)
+
+
+def _bits32(v) -> int:
+    return int(np.array(v, dtype=np.float32).view(np.uint32))
+
+
+def _f16_step(h: np.float16, k: int) -> np.float16:
+    toward = np.float16(np.inf) if k > 0 else np.float16(-np.inf)
+    for _ in range(abs(k)):
+        h = np.nextafter(h, toward)
+    return h
+
+
+def pack_group(vals, symmetric: bool):
+    """Repack one group of 128 fp32 values exactly, or refuse (None).
+
+    Values are compared by bit pattern, so +0 and -0 are distinct values and
+    any NaN or infinity refuses the group.  With two values lo < hi (-0 < +0),
+    weight bits are 1 where the value is hi.  Returns (bits [128] uint8,
+    scale fp16, bias fp16 or None), the metadata chosen as follows:
+
+    * symmetric: scale = RN16(-2 lo) (one value v: scale = RN16(2v) with all
+      bits 1 if v's sign bit is clear, else RN16(-2v) with all bits 0), kept
+      only if the derived bias -0.5 * scale is lo and fl32(scale + bias) is hi,
+      bit for bit;
+    * affine: bias = RN16(lo), which must give lo back exactly; scale = the
+      first of RN16(fl32(hi - lo)) and its fp16 neighbours in SCALE_STEPS
+      order with fl32(scale + bias) == hi bit for bit (one value: bias = v,
+      scale = +0, all bits 0).
+    """
+    v = np.asarray(vals, dtype=np.float32).reshape(-1)
+    if not np.all(np.isfinite(v)):
+        return None
+    pats = v.view(np.uint32)
+    distinct = list(dict.fromkeys(int(p) for p in pats))
+    if len(distinct) > 2:
+        return None
+    f = [np.array(p, dtype=np.uint32).view(np.float32)[()] for p in distinct]
+    if len(distinct) == 1:
+        x = f[0]
+        if symmetric:
+            neg = (distinct[0] >> 31) == 1
+            sc = np.float16(np.float32(-2.0) * x if neg else np.float32(2.0) * x)
+            b = np.float32(-0.5) * np.float32(sc)
+            val = b if neg else np.float32(np.float32(sc) + b)
+            if _bits32(val) != distinct[0]:
+                return None
+            bits = np.full(v.shape, 0 if neg else 1, dtype=np.uint8)
+            return bits, sc, None
+        bias = np.float16(x)
+        if _bits32(np.float32(bias)) != distinct[0]:
+            return None
+        return np.zeros(v.shape, dtype=np.uint8), np.float16(0.0), bias
+    a, c = f
+    if a < c or (a == c and (distinct[0] >> 31) == 1):
+        lo, hi, hi_pat = a, c, distinct[1]
+    else:
+        lo, hi, hi_pat = c, a, distinct[0]
+    bits = (pats == hi_pat).astype(np.uint8)
+    if symmetric:
+        sc = np.float16(np.float32(-2.0) * lo)
+        b = np.float32(-0.5) * np.float32(sc)
+        one = np.float32(np.float32(sc) + b)
+        if _bits32(b) != _bits32(lo) or _bits32(one) != hi_pat:
+            return None
+        return bits, sc, None
+    bias = np.float16(lo)
+    if _bits32(np.float32(bias)) != _bits32(lo):
+        return None
+    c0 = np.float16(np.float32(hi - lo))
+    for k in SCALE_STEPS:
+        sc = _f16_step(c0, k)
+        if not np.isfinite(sc):
+            continue
+        if _bits32(np.float32(np.float32(sc) + np.float32(bias))) == hi_pat:
+            return bits, sc, bias
+    return None
+
+
+def pack_from_dense(dense, symmetric: bool):
+    """Repack a dense [N, K] tensor (bf16, f16 or f32) group by group.
+
+    Returns (words [N, K/32] uint32, scales [N, G] fp16, biases [N, G] fp16 or
+    None when symmetric, number of refused groups).  A refused group gets zero
+    words, scale and bias.  bf16 and f16 values widen to fp32 exactly, so
+    comparing fp32 bit patterns compares the input's bit patterns.
+    """
+    if isinstance(dense, torch.Tensor):
+        d32 = dense.detach().to(torch.float32).numpy()
+    else:
+        d32 = np.asarray(dense, dtype=np.float32)
+    N, K = d32.shape
+    G = K // GROUP_SIZE
+    bits = np.zeros((N, K), dtype=np.uint8)
+    scales = np.zeros((N, G), dtype=np.float16)
+    biases = None if symmetric else np.zeros((N, G), dtype=np.float16)
+    bad = 0
+    for n in range(N):
+        for g in range(G):
+            r = pack_group(d32[n, g * GROUP_SIZE:(g + 1) * GROUP_SIZE], symmetric)
+            if r is None:
+                bad += 1
+                continue
+            bits[n, g * GROUP_SIZE:(g + 1) * GROUP_SIZE] = r[0]
+            scales[n, g] = r[1]
+            if not symmetric:
+                biases[n, g] = r[2]
+    return pack(bits), scales, biases, bad
+
+
+# ---------------------------------------------------------------------------
 # Storage accounting (bytes per weight of the packed format)
 # ---------------------------------------------------------------------------
 def storage_bytes(N: int, K: int, symmetric: bool) -> dict:

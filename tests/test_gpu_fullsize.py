@@ -76,6 +76,35 @@ def test_dequantize_full_shape_bit_exact(q1):
     assert torch.equal(q1.pack(bits), W.words)
 
 
+def test_pack_from_dense_full_shape(q1):
+    """A 27B-class projection dequantized by the library, then repacked: fp32
+    dense gives back the very words and scales; bf16 dense (the halves of the
+    scales rounded to bf16) stays exactly representable and round-trips."""
+    t = synth.q1_tensor(D_FF, D_MODEL, seed=1011, affine=False)
+    W = q1.Q1Weight.from_host(t)
+    d32 = q1.dequantize(W, torch.float32)
+    W2, bad = q1.pack_from_dense(d32, symmetric=True)
+    assert int(bad.item()) == 0
+    assert torch.equal(W2.words, W.words) and torch.equal(W2.scales.view(torch.int16), W.scales.view(torch.int16))
+    d16 = q1.dequantize(W, torch.bfloat16)
+    W3, bad3 = q1.pack_from_dense(d16, symmetric=True)
+    assert int(bad3.item()) == 0 and torch.equal(W3.words, W.words)
+    assert torch.equal(q1.dequantize(W3, torch.bfloat16).view(torch.int16), d16.view(torch.int16))
+    rows = _rows(D_FF, 6, 1012)
+    wo, so, _, bado = O.pack_from_dense(d16[torch.from_numpy(rows).to(DEV)].cpu(), symmetric=True)
+    assert bado == 0
+    np.testing.assert_array_equal(W3.words[torch.from_numpy(rows).to(DEV)].cpu().numpy().view(np.uint32), wo)
+    np.testing.assert_array_equal(W3.scales[torch.from_numpy(rows).to(DEV)].cpu().numpy().view(np.uint16),
+                                  so.view(np.uint16))
+    # affine in fp32: the same words, and the repacked tensor dequantizes to the same bits
+    ta = synth.q1_tensor(D_MODEL, D_FF, seed=1013, affine=True)
+    Wa = q1.Q1Weight.from_host(ta)
+    da = q1.dequantize(Wa, torch.float32)
+    Wb, bada = q1.pack_from_dense(da, symmetric=False)
+    assert int(bada.item()) == 0 and torch.equal(Wb.words, Wa.words)
+    assert torch.equal(q1.dequantize(Wb, torch.float32).view(torch.int32), da.view(torch.int32))
+
+
 def test_embedding_gather_and_tied_head_full_vocab(q1):
     t = synth.q1_tensor(VOCAB, D_MODEL, seed=1003, affine=False)
     E = q1.Q1Weight.from_host(t)

@@ -322,6 +322,51 @@ def test_ffn_fused(q1, M, D, F):
     check_matmul(y, yo, ho, O.dequantize_f32(down.words, down.scales, None, F), f"ffn M={M}")
 
 
+# ------------------------------------------------------------------ exact repack from dense
+_TORCH = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}
+_INT = {"bf16": torch.int16, "f16": torch.int16, "f32": torch.int32}
+
+
+def _planted_dense(t, dtype):
+    """The dequantized tensor in `dtype` with edge-case groups planted (values
+    exact in every dtype): +-0 pairs, single values, a third value, NaN and
+    infinity."""
+    d = O.round_to(O.dequantize_f32(t.words, t.scales, t.biases, t.K), dtype).clone()
+    sign = torch.from_numpy(np.random.default_rng(5).integers(0, 2, 128).astype(bool))
+    d[0, 0:128] = torch.where(sign, torch.tensor(0.0), torch.tensor(-0.0)).to(d.dtype)
+    d[1, 128:256] = 0.5
+    d[2, 256:384] = -0.5
+    d[3, 5] = float("nan")
+    d[4, 130] = float("inf")
+    d[5, 7] = 3.0
+    d[6, 0:128] = 0.0
+    d[7, 128:256] = -0.0
+    d[8, 256:384] = torch.where(sign, torch.tensor(0.75), torch.tensor(0.25)).to(d.dtype)
+    return d
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("affine", [False, True])
+def test_pack_from_dense_bit_exact(q1, dtype, affine):
+    N, K = 37, 640
+    t = synth.q1_tensor(N, K, seed=501 + affine, affine=affine)
+    dense = _planted_dense(t, dtype)
+    W, bad = q1.pack_from_dense(dense.to(DEV), symmetric=not affine)
+    wo, so, bo, bado = O.pack_from_dense(dense, symmetric=not affine)
+    assert int(bad.item()) == bado and bado >= 3
+    np.testing.assert_array_equal(W.words.cpu().numpy().view(np.uint32), wo)
+    np.testing.assert_array_equal(W.scales.cpu().numpy().view(np.uint16), so.view(np.uint16))
+    if affine:
+        np.testing.assert_array_equal(W.biases.cpu().numpy().view(np.uint16), bo.view(np.uint16))
+    # every kept group dequantizes to exactly its input bits (the library's own dequantize)
+    back = q1.dequantize(W, _TORCH[dtype]).cpu().view(_INT[dtype]).reshape(N, K // 128, 128)
+    want = dense.view(_INT[dtype]).reshape(N, K // 128, 128)
+    kept = torch.tensor([[O.pack_group(dense[n, g * 128:(g + 1) * 128].float().numpy(), not affine) is not None
+                          for g in range(K // 128)] for n in range(N)])
+    assert int((~kept).sum()) == bado
+    assert torch.equal(back[kept], want[kept])
+
+
 # ------------------------------------------------------------------ decode chain
 def _scaled(t, factor):
     """The same bits with the metadata multiplied by `factor` (fp16): products

@@ -303,6 +303,95 @@ def test_decode_chain_on_selection_matrices():
     assert torch.equal(got.to(torch.float64), h)
 
 
+# ---------------------------------------------------------------- exact repack from dense
+def _group(lo, hi, pattern_seed=0):
+    rng = np.random.default_rng(pattern_seed)
+    q = rng.integers(0, 2, 128).astype(np.uint8)
+    q[0], q[1] = 0, 1
+    return np.where(q == 1, np.float32(hi), np.float32(lo)).astype(np.float32), q
+
+
+def test_pack_group_hand_built_cases():
+    # symmetric +-0.75: scale 1.5 (fp16 0x3E00), bit 1 for +0.75
+    v, q = _group(-0.75, 0.75)
+    bits, sc, b = O.pack_group(v, symmetric=True)
+    assert b is None and sc.view(np.uint16) == 0x3E00 and np.array_equal(bits, q)
+    # affine {0.25, 1.0}: bias 0.25, scale 0.75 (exact in fp16)
+    v, q = _group(0.25, 1.0)
+    bits, sc, b = O.pack_group(v, symmetric=False)
+    assert float(b) == 0.25 and float(sc) == 0.75 and np.array_equal(bits, q)
+    # {-0, +0}: bit 1 for +0; symmetric scale +0 (derived bias -0), affine bias -0
+    v, q = _group(-0.0, 0.0)
+    bits, sc, b = O.pack_group(v, symmetric=True)
+    assert sc.view(np.uint16) == 0x0000 and np.array_equal(bits, q)
+    bits, sc, b = O.pack_group(v, symmetric=False)
+    assert b.view(np.uint16) == 0x8000 and sc.view(np.uint16) == 0x0000 and np.array_equal(bits, q)
+    # one value: symmetric +0.5 -> scale 1.0, all bits 1; -0.5 -> scale 1.0, all bits 0
+    bits, sc, b = O.pack_group(np.full(128, 0.5, np.float32), symmetric=True)
+    assert float(sc) == 1.0 and bits.all()
+    bits, sc, b = O.pack_group(np.full(128, -0.5, np.float32), symmetric=True)
+    assert float(sc) == 1.0 and not bits.any()
+    # one value, affine: the bias is the value, all bits 0
+    bits, sc, b = O.pack_group(np.full(128, 3.0, np.float32), symmetric=False)
+    assert float(b) == 3.0 and not bits.any()
+    # refusals: three values, NaN, infinity, not +-m in symmetric mode, a bias
+    # that is not an fp16 value
+    v3 = _group(-0.5, 0.5)[0]
+    v3[5] = np.float32(0.25)
+    assert O.pack_group(v3, True) is None and O.pack_group(v3, False) is None
+    for bad in (np.nan, np.inf, -np.inf):
+        vb = _group(-0.5, 0.5)[0]
+        vb[7] = np.float32(bad)
+        assert O.pack_group(vb, True) is None and O.pack_group(vb, False) is None
+    assert O.pack_group(_group(-0.5, 0.75)[0], True) is None
+    assert O.pack_group(_group(1.0 + 2.0 ** -20, 2.0)[0], False) is None
+
+
+def test_pack_group_scale_rule_matches_exhaustive_search():
+    """An affine group {lo, hi} (lo an fp16 value) is kept iff some finite fp16
+    scale gives fl32(scale + lo) == hi; the chosen scale must be one of them."""
+    all16 = np.arange(0, 0x7C00, dtype=np.uint16).view(np.float16)
+    all16 = np.concatenate([all16, -all16[1:]]).astype(np.float32)
+    rng = np.random.default_rng(11)
+    kept = refused = 0
+    for _ in range(3000):
+        lo = np.float32(np.float16(rng.normal() * 10 ** rng.uniform(-6, 4)))
+        hi = np.float32(lo + np.float32(abs(rng.normal()) * 10 ** rng.uniform(-8, 3)))
+        if hi == lo:
+            continue
+        v = _group(lo, hi)[0]
+        r = O.pack_group(v, symmetric=False)
+        exists = np.any((all16 + lo).astype(np.float32).view(np.uint32) == np.float32(hi).view(np.uint32))
+        assert (r is not None) == bool(exists), (lo, hi)
+        if r is not None:
+            assert np.float32(np.float32(r[1]) + np.float32(r[2])) == hi
+            kept += 1
+        else:
+            refused += 1
+    assert kept > 300 and refused > 300
+
+
+@pytest.mark.parametrize("affine", [False, True])
+def test_pack_from_dense_round_trip(affine):
+    N, K = 24, 384
+    t = synth.q1_tensor(N, K, seed=141 + affine, affine=affine)
+    dense = O.dequantize_f32(t.words, t.scales, t.biases, K)    # pinned above
+    w, sc, b, bad = O.pack_from_dense(dense, symmetric=not affine)
+    assert bad == 0
+    # every bit comes back (no group of the random tensor is single-valued)
+    assert np.array_equal(w, t.words)
+    if not affine:
+        assert np.array_equal(sc.view(np.uint16), t.scales.view(np.uint16))
+    back = O.dequantize_f32(w, sc, b, K)
+    assert np.array_equal(back.view(np.uint32), dense.view(np.uint32))
+    # a group with a third value is refused and zeroed; the rest are untouched
+    dense2 = dense.copy()
+    dense2[3, 130] = np.float32(1234.5)
+    w2, sc2, b2, bad2 = O.pack_from_dense(dense2, symmetric=not affine)
+    assert bad2 == 1 and float(sc2[3, 1]) == 0.0 and not w2[3, 4:8].any()
+    assert np.array_equal(np.delete(w2, slice(4, 8), axis=1), np.delete(w, slice(4, 8), axis=1))
+
+
 # ---------------------------------------------------------------- gather
 def test_embed_gather_rows_and_out_of_range():
     V, K = 10, 256
