@@ -170,7 +170,7 @@ def cpu_baseline(seconds: float):
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
-def build_stack(q1, synth, torch, device, affine, seed0):
+def build_stack(q1, synth, torch, device, affine, seed0, meta_bf16=False):
     layers = []
     for li in range(LAYERS):
         ws = {}
@@ -179,6 +179,9 @@ def build_stack(q1, synth, torch, device, affine, seed0):
             w = synth.device_weight_words(N, K, sd, device)
             s = synth.device_scales(N, K, sd + 7919, device)
             b = synth.device_biases(N, K, sd + 15485863, device) if affine else None
+            if meta_bf16:  # the same draws rounded to bf16
+                s = s.to(torch.bfloat16)
+                b = None if b is None else b.to(torch.bfloat16)
             ws[name] = q1.Q1Weight(w, s, b, K)
         layers.append(ws)
     return layers
@@ -420,6 +423,14 @@ def gpu_arm(args):
         s_ = run_timed(torch, gm, n, stream)
         sub["affine_M1_GBps"] = round(step_bytes(1, True) * n / s_ / 1e9, 1)
         del gm, la
+        torch.cuda.empty_cache()
+        # bf16 scales (the Bonsai image checkpoint's metadata type), M = 1
+        lb = build_stack(q1, synth, torch, device, affine=False, seed0=9500, meta_bf16=True)
+        stp, _, _ = make_step(q1, torch, lb, 1, device)
+        gm = time_graph(torch, stp, 3, 3, stream)
+        s_ = run_timed(torch, gm, n, stream)
+        sub["bf16_meta_M1_GBps"] = round(step_bytes(1) * n / s_ / 1e9, 1)
+        del gm, lb
         torch.cuda.empty_cache()
         # exact repack of a dense bf16 projection (17408 x 5120) into Q1:
         # GB/s of the dense read plus the words and scales written

@@ -41,6 +41,7 @@ q1_status check_device() {
 q1_status check_weight(const q1_weight *W) {
   if (!W || !W->w || !W->scales) return Q1_ERR_NULL;
   if (W->group_size != 128) return Q1_ERR_GROUP;
+  if (W->meta_dtype != Q1_META_F16 && W->meta_dtype != Q1_META_BF16) return Q1_ERR_DTYPE;
   if (W->N < 1 || W->K < 128 || W->K % 128 != 0) return Q1_ERR_SHAPE;
   if (W->K > (int64_t)1 << 24 || W->N > ((int64_t)1 << 31) - 1) return Q1_ERR_SHAPE;
   if (!aligned(W->w, 16) || !aligned(W->scales, 2) || (W->biases && !aligned(W->biases, 2)))
@@ -64,7 +65,7 @@ q1_status matmul_common(const q1_weight *W, const void *x, int64_t M, q1_dtype d
   s = check_weight(W);
   if (s != Q1_OK) return s;
   if (!x || !y) return Q1_ERR_NULL;
-  if (dtype != Q1_BF16) return Q1_ERR_DTYPE;
+  if (dtype != Q1_BF16 && dtype != Q1_F16 && dtype != Q1_F32) return Q1_ERR_DTYPE;
   if (M < 1 || M > ((int64_t)1 << 24)) return Q1_ERR_SHAPE;
   if (!aligned(x, 16) || !aligned(y, 16)) return Q1_ERR_ALIGN;
   return Q1_OK;
@@ -126,7 +127,7 @@ q1_status q1_qmv(const q1_weight *W, const void *x, q1_dtype dtype, void *y, q1_
   q1_status s = matmul_common(W, x, 1, dtype, y);
   if (s != Q1_OK) return s;
   if (W->K > q1::kNarrowMaxK) return Q1_ERR_SHAPE;
-  return cuda_status(q1::launch_narrow(q1::view(W), x, 1, y, (cudaStream_t)stream, true));
+  return cuda_status(q1::launch_narrow(q1::view(W), x, 1, y, (cudaStream_t)stream, true, dtype, dtype));
 }
 
 q1_status q1_qmm_narrow(const q1_weight *W, const void *x, int64_t M, q1_dtype dtype, void *y,
@@ -134,7 +135,7 @@ q1_status q1_qmm_narrow(const q1_weight *W, const void *x, int64_t M, q1_dtype d
   q1_status s = matmul_common(W, x, M, dtype, y);
   if (s != Q1_OK) return s;
   if (M > q1::kNarrowMaxM || W->K > q1::kNarrowMaxK) return Q1_ERR_SHAPE;
-  return cuda_status(q1::launch_narrow(q1::view(W), x, M, y, (cudaStream_t)stream, true));
+  return cuda_status(q1::launch_narrow(q1::view(W), x, M, y, (cudaStream_t)stream, true, dtype, dtype));
 }
 
 size_t q1_qmm_workspace_size(int64_t M, int64_t N, int64_t K) {
@@ -148,10 +149,10 @@ q1_status q1_qmm(const q1_weight *W, const void *x, int64_t M, q1_dtype dtype, v
   q1_status s = matmul_common(W, x, M, dtype, y);
   if (s != Q1_OK) return s;
   if (M <= g_max_rows.load() && W->K <= q1::kNarrowMaxK)
-    return cuda_status(q1::launch_narrow(q1::view(W), x, M, y, (cudaStream_t)stream, true));
+    return cuda_status(q1::launch_narrow(q1::view(W), x, M, y, (cudaStream_t)stream, true, dtype, dtype));
   s = check_ws(workspace, workspace_bytes, q1::wide_workspace_bytes(M, W->K));
   if (s != Q1_OK) return s;
-  return cuda_status(q1::launch_wide(q1::view(W), x, M, y, workspace, (cudaStream_t)stream));
+  return cuda_status(q1::launch_wide(q1::view(W), x, M, y, workspace, (cudaStream_t)stream, dtype));
 }
 
 q1_status q1_embed_gather(const q1_weight *E, const int32_t *ids, int64_t T, q1_dtype out_t,
@@ -184,7 +185,7 @@ q1_status q1_ffn_fused(const q1_weight *gate, const q1_weight *up, const q1_weig
       (s = check_weight(down)) != Q1_OK)
     return s;
   if (!x || !y) return Q1_ERR_NULL;
-  if (dtype != Q1_BF16) return Q1_ERR_DTYPE;
+  if (dtype != Q1_BF16 && dtype != Q1_F16 && dtype != Q1_F32) return Q1_ERR_DTYPE;
   if (M < 1 || M > q1::kNarrowMaxM) return Q1_ERR_SHAPE;
   const int64_t D = gate->K, F = gate->N;
   if (up->K != D || up->N != F || down->K != F || down->N != D) return Q1_ERR_SHAPE;
@@ -197,8 +198,8 @@ q1_status q1_ffn_fused(const q1_weight *gate, const q1_weight *up, const q1_weig
   // two launches chained with programmatic dependent launch: the down
   // projection starts streaming its weights while gate/up drains, and waits
   // for h only before reading it
-  cudaError_t e = q1::launch_narrow_gate_up(q1::view(gate), q1::view(up), x, M, h, st, true);
-  if (e == cudaSuccess) e = q1::launch_narrow(q1::view(down), h, M, y, st, true);
+  cudaError_t e = q1::launch_narrow_gate_up(q1::view(gate), q1::view(up), x, M, h, st, true, dtype);
+  if (e == cudaSuccess) e = q1::launch_narrow(q1::view(down), h, M, y, st, true, Q1_BF16, dtype);
   return cuda_status(e);
 }
 

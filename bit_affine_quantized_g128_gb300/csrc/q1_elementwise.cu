@@ -86,10 +86,10 @@ __global__ void unpack_kernel(const uint32_t *__restrict__ w, uint8_t *__restric
 // fp32 dequantized pair for one (row, group): lo = bias (q = 0),
 // hi = fl32(scale + bias) (q = 1).  Symmetric: bias = -scale/2 in fp32 (exact).
 __device__ __forceinline__ void group_values(const uint16_t *__restrict__ s,
-                                             const uint16_t *__restrict__ b, int64_t idx,
+                                             const uint16_t *__restrict__ b, int64_t idx, bool mbf16,
                                              float &lo, float &hi) {
-  float sc = __half2float(__ushort_as_half(s[idx]));
-  float bi = b ? __half2float(__ushort_as_half(b[idx])) : __fmul_rn(-0.5f, sc);
+  float sc = meta_f32(s[idx], mbf16);
+  float bi = b ? meta_f32(b[idx], mbf16) : __fmul_rn(-0.5f, sc);
   lo = bi;
   hi = __fadd_rn(sc, bi);
 }
@@ -142,7 +142,7 @@ __device__ __forceinline__ void emit_word(float lo, float hi, uint32_t word, voi
 
 template <int OUT>
 __global__ void dequantize_kernel(const uint32_t *__restrict__ w, const uint16_t *__restrict__ s,
-                                  const uint16_t *__restrict__ b, int64_t N, int64_t K,
+                                  const uint16_t *__restrict__ b, int64_t N, int64_t K, bool mbf16,
                                   void *__restrict__ out) {
   const int64_t wpr = K / 32, G = K / 128, nwords = N * wpr;
   const int esz = OUT == 2 ? 4 : 2;
@@ -150,14 +150,14 @@ __global__ void dequantize_kernel(const uint32_t *__restrict__ w, const uint16_t
        i += (int64_t)gridDim.x * blockDim.x) {
     int64_t n = i / wpr, c = i - n * wpr;
     float lo, hi;
-    group_values(s, b, n * G + c / 4, lo, hi);
+    group_values(s, b, n * G + c / 4, mbf16, lo, hi);
     emit_word<OUT>(lo, hi, w[i], static_cast<char *>(out) + n * K * esz, c);
   }
 }
 
 template <int OUT>
 __global__ void gather_kernel(const uint32_t *__restrict__ w, const uint16_t *__restrict__ s,
-                              const uint16_t *__restrict__ b, int64_t V, int64_t K,
+                              const uint16_t *__restrict__ b, int64_t V, int64_t K, bool mbf16,
                               const int32_t *__restrict__ ids, int64_t T, void *__restrict__ out,
                               int32_t *__restrict__ bad) {
   const int64_t wpr = K / 32, G = K / 128, nwords = T * wpr;
@@ -175,7 +175,7 @@ __global__ void gather_kernel(const uint32_t *__restrict__ w, const uint16_t *__
       continue;
     }
     float lo, hi;
-    group_values(s, b, row * G + c / 4, lo, hi);
+    group_values(s, b, row * G + c / 4, mbf16, lo, hi);
     emit_word<OUT>(lo, hi, w[row * wpr + c], out_row, c);
   }
 }
@@ -183,13 +183,13 @@ __global__ void gather_kernel(const uint32_t *__restrict__ w, const uint16_t *__
 __global__ void set_flag_kernel(int32_t *flag, int32_t v) { *flag = v; }
 
 __global__ void check_symmetric_kernel(const uint16_t *__restrict__ s,
-                                       const uint16_t *__restrict__ b, int64_t count,
+                                       const uint16_t *__restrict__ b, int64_t count, bool mbf16,
                                        int32_t *__restrict__ result) {
   bool mismatch = false;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < count;
        i += (int64_t)gridDim.x * blockDim.x) {
-    float sc = __half2float(__ushort_as_half(s[i]));
-    float bi = __half2float(__ushort_as_half(b[i]));
+    float sc = meta_f32(s[i], mbf16);
+    float bi = meta_f32(b[i], mbf16);
     // exact fp32 equality: +0 == -0, NaN != anything
     if (!(bi == __fmul_rn(-0.5f, sc))) mismatch = true;
   }
@@ -398,9 +398,9 @@ cudaError_t launch_dequantize(const WeightView &W, q1_dtype t, void *out, cudaSt
   int64_t nwords = W.N * (W.K / 32);
   unsigned g = grid_for(nwords, 256);
   switch (t) {
-    case Q1_BF16: dequantize_kernel<0><<<g, 256, 0, st>>>(W.w, W.s, W.b, W.N, W.K, out); break;
-    case Q1_F16: dequantize_kernel<1><<<g, 256, 0, st>>>(W.w, W.s, W.b, W.N, W.K, out); break;
-    default: dequantize_kernel<2><<<g, 256, 0, st>>>(W.w, W.s, W.b, W.N, W.K, out); break;
+    case Q1_BF16: dequantize_kernel<0><<<g, 256, 0, st>>>(W.w, W.s, W.b, W.N, W.K, W.mbf16, out); break;
+    case Q1_F16: dequantize_kernel<1><<<g, 256, 0, st>>>(W.w, W.s, W.b, W.N, W.K, W.mbf16, out); break;
+    default: dequantize_kernel<2><<<g, 256, 0, st>>>(W.w, W.s, W.b, W.N, W.K, W.mbf16, out); break;
   }
   return cudaGetLastError();
 }
@@ -411,13 +411,13 @@ cudaError_t launch_gather(const WeightView &E, const int32_t *ids, int64_t T, q1
   unsigned g = grid_for(nwords, 256);
   switch (t) {
     case Q1_BF16:
-      gather_kernel<0><<<g, 256, 0, st>>>(E.w, E.s, E.b, E.N, E.K, ids, T, out, bad);
+      gather_kernel<0><<<g, 256, 0, st>>>(E.w, E.s, E.b, E.N, E.K, E.mbf16, ids, T, out, bad);
       break;
     case Q1_F16:
-      gather_kernel<1><<<g, 256, 0, st>>>(E.w, E.s, E.b, E.N, E.K, ids, T, out, bad);
+      gather_kernel<1><<<g, 256, 0, st>>>(E.w, E.s, E.b, E.N, E.K, E.mbf16, ids, T, out, bad);
       break;
     default:
-      gather_kernel<2><<<g, 256, 0, st>>>(E.w, E.s, E.b, E.N, E.K, ids, T, out, bad);
+      gather_kernel<2><<<g, 256, 0, st>>>(E.w, E.s, E.b, E.N, E.K, E.mbf16, ids, T, out, bad);
       break;
   }
   return cudaGetLastError();
@@ -428,7 +428,7 @@ cudaError_t launch_check_symmetric(const WeightView &W, int32_t *result, cudaStr
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   int64_t count = W.N * (W.K / 128);
-  check_symmetric_kernel<<<grid_for(count, 256), 256, 0, st>>>(W.s, W.b, count, result);
+  check_symmetric_kernel<<<grid_for(count, 256), 256, 0, st>>>(W.s, W.b, count, W.mbf16, result);
   return cudaGetLastError();
 }
 

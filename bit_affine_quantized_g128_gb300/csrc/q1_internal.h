@@ -2,6 +2,7 @@
 // Not part of the public ABI (include/q1.h is).
 #pragma once
 
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -21,11 +22,20 @@ struct WeightView {
   const uint16_t *s;
   const uint16_t *b;  // nullptr: symmetric
   int64_t N, K;
+  bool mbf16;         // scales/biases are bf16 (else fp16)
 };
 
 inline WeightView view(const q1_weight *W) {
-  return WeightView{W->w, W->scales, W->biases, W->N, W->K};
+  return WeightView{W->w, W->scales, W->biases, W->N, W->K, W->meta_dtype == Q1_META_BF16};
 }
+
+#ifdef __CUDACC__
+// One fp16 or bf16 metadata value (its 16 bits in the low half of h) -> fp32;
+// both widenings are exact.
+__device__ __forceinline__ float meta_f32(uint32_t h, bool bf16) {
+  return bf16 ? __uint_as_float((h & 0xFFFFu) << 16) : __half2float(__ushort_as_half((unsigned short)(h & 0xFFFFu)));
+}
+#endif
 
 // ---- elementwise kernels (q1_elementwise.cu)
 cudaError_t launch_pack(const uint8_t *bits, int64_t N, int64_t K, uint32_t *w, cudaStream_t st);
@@ -41,18 +51,20 @@ cudaError_t launch_pack_from_dense(const void *dense, q1_dtype t, int64_t N, int
                                    uint16_t *s, uint16_t *b, int32_t *bad, cudaStream_t st);
 
 // ---- narrow path (q1_narrow.cu): one launch, no scratch
-// y [M][N] bf16 = x . W^T (x [M][K] bf16).
+// y [M][N] (ydt) = x . W^T (x [M][K], xdt); fp16/fp32 x are rounded to bf16,
+// the tensor-core operand type, as they are loaded.
 cudaError_t launch_narrow(const WeightView &W, const void *x, int64_t M, void *y,
-                          cudaStream_t st, bool pdl);
-// h [M][F] bf16 = SiLU(x . G^T) * (x . U^T).
+                          cudaStream_t st, bool pdl, q1_dtype xdt = Q1_BF16, q1_dtype ydt = Q1_BF16);
+// h [M][F] bf16 = SiLU(x . G^T) * (x . U^T), x in xdt.
 cudaError_t launch_narrow_gate_up(const WeightView &G, const WeightView &U, const void *x,
-                                  int64_t M, void *h, cudaStream_t st, bool pdl);
+                                  int64_t M, void *h, cudaStream_t st, bool pdl, q1_dtype xdt = Q1_BF16);
 
 // ---- wide path (q1_wide.cu)
 // workspace: fp16 activation rows [M][K] and per-row scales [M]
 size_t wide_workspace_bytes(int64_t M, int64_t K);
+// x [M][K] and y [M][N] in dt (bf16, fp16 or fp32)
 cudaError_t launch_wide(const WeightView &W, const void *x, int64_t M, void *y, void *ws,
-                        cudaStream_t st);
+                        cudaStream_t st, q1_dtype dt = Q1_BF16);
 
 // ---- device error words (each translation unit with bounded waits owns one)
 unsigned int read_and_clear_wide_errors(cudaStream_t st, cudaError_t *err);

@@ -139,6 +139,18 @@ __device__ __forceinline__ uint32_t bmul2(uint32_t a, uint32_t b) {
   return d;
 }
 
+// (lo, hi) -> bf16x2, each rounded to nearest even
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t *>(&h);
+}
+// one output value in the activation dtype (one rounding for 16-bit types)
+__device__ __forceinline__ void store_act(void *out, size_t i, float v, int dt) {
+  if (dt == Q1_F32) static_cast<float *>(out)[i] = v;
+  else if (dt == Q1_F16) static_cast<__half *>(out)[i] = __float2half_rn(v);
+  else static_cast<__nv_bfloat16 *>(out)[i] = __float2bfloat16_rn(v);
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
@@ -222,12 +234,14 @@ struct NarrowArgs {
   int64_t N;
   int K;
   int M;
-  const __nv_bfloat16 *x;  // [M][K]
-  __nv_bfloat16 *out;      // y [M][N] or h [M][N]
+  const void *x;  // [M][K], xdt
+  void *out;      // y [M][N] or h [M][N], ydt
+  int xdt, ydt;   // q1_dtype of x and of the output
   Geo geo;
   // strides of the shared-memory layout, computed on the host so that the
   // tile loop reads them as constants
   int slot_words, slot_meta, part_tile;
+  int meta_bf16;  // bit m: matrix m's scales/biases are bf16 (else fp16)
 };
 
 // Tensor maps of the (up to two) matrices: packed words, scales, biases.
@@ -256,7 +270,7 @@ __device__ __forceinline__ void consumer_sync(int nthreads) {
 // the producer's lanes load them (zero past K) and store them before their
 // arrivals.  Either way a slot's metadata is [16 rows][meta_groups] fp16
 // starting at group 4 (q_lo & ~1).
-template <int NMAT, bool AFFINE, bool FASTMETA>
+template <int NMAT, bool AFFINE, bool FASTMETA, bool GEN>
 __global__ void __launch_bounds__(kMaxThreads, 1)
 narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -372,6 +386,9 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
   }
 
   // ================= consumers =================
+  // GEN: bf16 metadata, or fp16/fp32 activations or outputs, read at run time;
+  // otherwise (fp16 metadata, bf16 in and out) those choices are compiled in
+  const int xdt = GEN ? a.xdt : (int)Q1_BF16, ydt = GEN ? a.ydt : (int)Q1_BF16;
   const int qi = warp % QM, ri = warp / QM;
   const bool active = qi < QS;
   const int span = q_lo + qi;  // groups 4 span .. 4 span + 3
@@ -392,11 +409,31 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
     for (int u = 0; u < kQuad; ++u) {
       const int g = span * kQuad + u;
       if (gid < M && g < G) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(a.x + (size_t)gid * K + (size_t)g * 128 + 32 * t);
+        // this lane's 32 activations of the group as 16 bf16 pairs; fp16 and
+        // fp32 activations are rounded to bf16 (the MMA operand type) once here
+        const size_t e0 = (size_t)gid * K + (size_t)g * 128 + 32 * t;
+        if (xdt == Q1_F32) {
+          const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const float *>(a.x) + e0);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint4 v = __ldg(src + q);
-          xv[u][4 * q] = v.x; xv[u][4 * q + 1] = v.y; xv[u][4 * q + 2] = v.z; xv[u][4 * q + 3] = v.w;
+          for (int q = 0; q < 8; ++q) {
+            const uint4 v = __ldg(src + q);
+            xv[u][2 * q] = pack_bf16x2(__uint_as_float(v.x), __uint_as_float(v.y));
+            xv[u][2 * q + 1] = pack_bf16x2(__uint_as_float(v.z), __uint_as_float(v.w));
+          }
+        } else {
+          const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.x) + e0);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 v = __ldg(src + q);
+            xv[u][4 * q] = v.x; xv[u][4 * q + 1] = v.y; xv[u][4 * q + 2] = v.z; xv[u][4 * q + 3] = v.w;
+          }
+          if (xdt == Q1_F16) {
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+              const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&xv[u][q]));
+              xv[u][q] = pack_bf16x2(f.x, f.y);
+            }
+          }
         }
       } else {
 #pragma unroll
@@ -493,12 +530,13 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
         Q1_MMA(1) Q1_MMA(2) Q1_MMA(3) Q1_MMA(4) Q1_MMA(5) Q1_MMA(6) Q1_MMA(7)
 #undef Q1_MMA
         float acc[4];
+        const bool mbf = GEN && ((a.meta_bf16 >> ((NMAT == 2 && ((rb + lt) & 1)) ? 1 : 0)) & 1) != 0;
 #pragma unroll
         for (int u = 0; u < kQuad; ++u) {
           const uint32_t hs_a = (u < 2 ? sa.x : sa.y) >> (16 * (u & 1));
           const uint32_t hs_b = (u < 2 ? sb.x : sb.y) >> (16 * (u & 1));
-          const float s_a = __half2float(__ushort_as_half((uint16_t)hs_a));
-          const float s_b = __half2float(__ushort_as_half((uint16_t)hs_b));
+          const float s_a = meta_f32(hs_a, mbf);
+          const float s_b = meta_f32(hs_b, mbf);
           if (u == 0) {
             acc[0] = s_a * d[u][0]; acc[1] = s_a * d[u][1]; acc[2] = s_b * d[u][2]; acc[3] = s_b * d[u][3];
           } else {
@@ -508,8 +546,8 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
           if (AFFINE) {
             float b_a, b_b;
             if (has_b) {
-              b_a = __half2float(__ushort_as_half((uint16_t)((u < 2 ? ba.x : ba.y) >> (16 * (u & 1)))));
-              b_b = __half2float(__ushort_as_half((uint16_t)((u < 2 ? bb.x : bb.y) >> (16 * (u & 1)))));
+              b_a = meta_f32((u < 2 ? ba.x : ba.y) >> (16 * (u & 1)), mbf);
+              b_b = meta_f32((u < 2 ? bb.x : bb.y) >> (16 * (u & 1)), mbf);
             } else {  // matrix without stored biases: symmetric
               b_a = __fmul_rn(-0.5f, s_a);
               b_b = __fmul_rn(-0.5f, s_b);
@@ -559,7 +597,7 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
         }
         if (n < N) {
           const float o = NMAT == 2 ? v0 / (1.0f + expf(-v0)) * v1 : v0;  // SiLU(gate) * up
-          a.out[(size_t)m * N + n] = __float2bfloat16_rn(o);
+          store_act(a.out, (size_t)m * N + n, o, ydt);
         }
       }
       consumer_sync(nthreads);  // the next round rewrites the partials
@@ -589,7 +627,7 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
         }
         if (n < N) {
           const float o = NMAT == 2 ? v0 / (1.0f + expf(-v0)) * v1 : v0;
-          a.out[(size_t)m * N + n] = __float2bfloat16_rn(o);
+          store_act(a.out, (size_t)m * N + n, o, ydt);
         }
       }
       cluster.sync();  // every rank is done reading this round's partials
@@ -611,7 +649,7 @@ int sm_count_cached() {
   return n;
 }
 
-template <int NMAT, bool AFFINE, bool FASTMETA>
+template <int NMAT, bool AFFINE, bool FASTMETA, bool GEN>
 int max_clusters(int ks) {
   static int cache[9] = {0};
   if (cache[ks]) return cache[ks];
@@ -627,7 +665,7 @@ int max_clusters(int ks) {
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, narrow_kernel<NMAT, AFFINE, FASTMETA>, &cfg) != cudaSuccess || n < 1) {
+  if (cudaOccupancyMaxActiveClusters(&n, narrow_kernel<NMAT, AFFINE, FASTMETA, GEN>, &cfg) != cudaSuccess || n < 1) {
     cudaGetLastError();
     n = sm_count_cached() / ks;
   }
@@ -684,7 +722,7 @@ bool make_meta_map(CUtensorMap *map, const uint16_t *m, int64_t N, int64_t G, in
 // units: its tiles (spans x virtual row tiles of the widest cluster range),
 // about 0.7 tile per warp for the activation fragments, the cluster
 // exchange, and the extra rounds when the partial sums do not fit at once.
-template <int NMAT, bool AFFINE, bool FASTMETA>
+template <int NMAT, bool AFFINE, bool FASTMETA, bool GEN>
 bool choose_geo(int64_t N, int K, int M, Geo *out) {
   const int G = K / 128;
   const int QK = (G + kQuad - 1) / kQuad;
@@ -695,7 +733,7 @@ bool choose_geo(int64_t N, int K, int M, Geo *out) {
     if (ks > QK) break;
     const int qm = (QK + ks - 1) / ks;
     if (qm > kMaxWarps) continue;
-    int nclus = max_clusters<NMAT, AFFINE, FASTMETA>(ks);
+    int nclus = max_clusters<NMAT, AFFINE, FASTMETA, GEN>(ks);
     if (nclus > NT) nclus = NT;
     const int tv = ((NT + nclus - 1) / nclus) * NMAT;  // virtual row tiles of the widest range
     int R = kMaxWarps / qm;
@@ -739,9 +777,9 @@ bool choose_geo(int64_t N, int K, int M, Geo *out) {
   return best >= 0;
 }
 
-template <int NMAT, bool AFFINE, bool FASTMETA>
+template <int NMAT, bool AFFINE, bool FASTMETA, bool GEN>
 cudaError_t launch_impl(NarrowArgs args, const uint32_t *w0, const uint32_t *w1, cudaStream_t st, bool pdl) {
-  auto kern = narrow_kernel<NMAT, AFFINE, FASTMETA>;
+  auto kern = narrow_kernel<NMAT, AFFINE, FASTMETA, GEN>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
@@ -749,7 +787,7 @@ cudaError_t launch_impl(NarrowArgs args, const uint32_t *w0, const uint32_t *w1,
     attr_set = true;
   }
   Geo g;
-  if (!choose_geo<NMAT, AFFINE, FASTMETA>(args.N, args.K, args.M, &g)) return cudaErrorInvalidConfiguration;
+  if (!choose_geo<NMAT, AFFINE, FASTMETA, GEN>(args.N, args.K, args.M, &g)) return cudaErrorInvalidConfiguration;
   args.geo = g;
   {
     const SmemLayout L0 = smem_layout(g, AFFINE);
@@ -787,7 +825,7 @@ cudaError_t launch_impl(NarrowArgs args, const uint32_t *w0, const uint32_t *w1,
   return cudaLaunchKernelEx(&cfg, kern, maps, args);
 }
 
-template <int NMAT, bool AFFINE>
+template <int NMAT, bool AFFINE, bool GEN>
 cudaError_t launch_meta(NarrowArgs args, const uint32_t *w0, const uint32_t *w1, cudaStream_t st, bool pdl) {
   // metadata by TMA needs 16-byte rows (G % 8 == 0) and 16-byte aligned arrays
   bool fast = (args.K / 128) % 8 == 0;
@@ -795,41 +833,51 @@ cudaError_t launch_meta(NarrowArgs args, const uint32_t *w0, const uint32_t *w1,
     fast = fast && (reinterpret_cast<uintptr_t>(args.s[i]) & 15) == 0;
     fast = fast && (reinterpret_cast<uintptr_t>(args.b[i]) & 15) == 0;
   }
-  if (fast) return launch_impl<NMAT, AFFINE, true>(args, w0, w1, st, pdl);
-  return launch_impl<NMAT, AFFINE, false>(args, w0, w1, st, pdl);
+  if (fast) return launch_impl<NMAT, AFFINE, true, GEN>(args, w0, w1, st, pdl);
+  return launch_impl<NMAT, AFFINE, false, GEN>(args, w0, w1, st, pdl);
 }
 
-NarrowArgs make_args(const void *x, int64_t M, int64_t N, int64_t K, void *out) {
+NarrowArgs make_args(const void *x, int64_t M, int64_t N, int64_t K, void *out, q1_dtype xdt, q1_dtype ydt) {
   NarrowArgs a = {};
-  a.x = static_cast<const __nv_bfloat16 *>(x);
+  a.x = x;
   a.N = N;
   a.K = (int)K;
   a.M = (int)M;
-  a.out = static_cast<__nv_bfloat16 *>(out);
+  a.out = out;
+  a.xdt = (int)xdt;
+  a.ydt = (int)ydt;
   return a;
 }
 
 }  // namespace
 
 cudaError_t launch_narrow(const WeightView &W, const void *x, int64_t M, void *y,
-                          cudaStream_t st, bool pdl) {
-  NarrowArgs a = make_args(x, M, W.N, W.K, y);
+                          cudaStream_t st, bool pdl, q1_dtype xdt, q1_dtype ydt) {
+  NarrowArgs a = make_args(x, M, W.N, W.K, y, xdt, ydt);
   a.s[0] = a.s[1] = W.s;
   a.b[0] = a.b[1] = W.b;
-  return W.b ? launch_meta<1, true>(a, W.w, W.w, st, pdl) : launch_meta<1, false>(a, W.w, W.w, st, pdl);
+  a.meta_bf16 = W.mbf16 ? 3 : 0;
+  if (W.mbf16 || xdt != Q1_BF16 || ydt != Q1_BF16)
+    return W.b ? launch_meta<1, true, true>(a, W.w, W.w, st, pdl) : launch_meta<1, false, true>(a, W.w, W.w, st, pdl);
+  return W.b ? launch_meta<1, true, false>(a, W.w, W.w, st, pdl) : launch_meta<1, false, false>(a, W.w, W.w, st, pdl);
 }
 
 cudaError_t launch_narrow_gate_up(const WeightView &G, const WeightView &U, const void *x,
-                                  int64_t M, void *h, cudaStream_t st, bool pdl) {
-  NarrowArgs a = make_args(x, M, G.N, G.K, h);
+                                  int64_t M, void *h, cudaStream_t st, bool pdl, q1_dtype xdt) {
+  NarrowArgs a = make_args(x, M, G.N, G.K, h, xdt, Q1_BF16);
   a.s[0] = G.s;
   a.s[1] = U.s;
   a.b[0] = G.b;
   a.b[1] = U.b;
+  a.meta_bf16 = (G.mbf16 ? 1 : 0) | (U.mbf16 ? 2 : 0);
   // With mixed metadata the affine variant runs for both matrices; it derives
   // -scale/2 for the one whose biases pointer is null.
-  if (G.b || U.b) return launch_meta<2, true>(a, G.w, U.w, st, pdl);
-  return launch_meta<2, false>(a, G.w, U.w, st, pdl);
+  if (a.meta_bf16 || xdt != Q1_BF16) {
+    if (G.b || U.b) return launch_meta<2, true, true>(a, G.w, U.w, st, pdl);
+    return launch_meta<2, false, true>(a, G.w, U.w, st, pdl);
+  }
+  if (G.b || U.b) return launch_meta<2, true, false>(a, G.w, U.w, st, pdl);
+  return launch_meta<2, false, false>(a, G.w, U.w, st, pdl);
 }
 
 unsigned int read_and_clear_narrow_errors(cudaStream_t st, cudaError_t *err) {

@@ -200,6 +200,40 @@ __device__ __forceinline__ void expand_word(uint32_t w, uint32_t lo2, uint32_t h
   }
 }
 
+// Output stores in the activation dtype, one rounding for 16-bit types.
+__device__ __forceinline__ void store1(void *y, size_t i, float v, int dt) {
+  if (dt == Q1_F32) static_cast<float *>(y)[i] = v;
+  else if (dt == Q1_F16) static_cast<__half *>(y)[i] = __float2half_rn(v);
+  else static_cast<__nv_bfloat16 *>(y)[i] = __float2bfloat16_rn(v);
+}
+__device__ __forceinline__ uint32_t pack2(float a, float b, int dt) {
+  if (dt == Q1_F16) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h);
+  }
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t *>(&h);
+}
+// four values, y + i aligned to 8 bytes (16-bit types) or 16 bytes (fp32)
+__device__ __forceinline__ void store4(void *y, size_t i, const float (&f)[4], int dt) {
+  if (dt == Q1_F32) {
+    *reinterpret_cast<float4 *>(static_cast<float *>(y) + i) = make_float4(f[0], f[1], f[2], f[3]);
+  } else {
+    *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(y) + i) = make_uint2(pack2(f[0], f[1], dt), pack2(f[2], f[3], dt));
+  }
+}
+// eight values, y + i aligned to 16 bytes
+__device__ __forceinline__ void store8(void *y, size_t i, const float (&f)[8], int dt) {
+  if (dt == Q1_F32) {
+    float4 *d = reinterpret_cast<float4 *>(static_cast<float *>(y) + i);
+    d[0] = make_float4(f[0], f[1], f[2], f[3]);
+    d[1] = make_float4(f[4], f[5], f[6], f[7]);
+  } else {
+    *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(y) + i) =
+        make_uint4(pack2(f[0], f[1], dt), pack2(f[2], f[3], dt), pack2(f[4], f[5], dt), pack2(f[6], f[7], dt));
+  }
+}
+
 struct GroupData {
   uint4 w;
   uint16_t s, b;
@@ -213,7 +247,7 @@ template <int MT, bool SPLIT>
 __global__ void __launch_bounds__(kThreadsWide, 1)
 wide_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint32_t *__restrict__ W,
             const uint16_t *__restrict__ S, const uint16_t *__restrict__ Bv, int M, int N, int K,
-            const float *__restrict__ inv_scale, __nv_bfloat16 *__restrict__ y, int ksplit) {
+            const float *__restrict__ inv_scale, void *__restrict__ y, int ksplit, int mbf16, int ydt) {
   static_assert(!SPLIT || MT == 1, "split-K keeps one token tile per CTA");
   extern __shared__ unsigned char smem_raw[];
   unsigned char *base = reinterpret_cast<unsigned char *>(
@@ -316,8 +350,8 @@ wide_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint32_t *__restri
     };
     bool alive = true;
     auto process = [&](int g, const GroupData &gd) {
-      const float sc = __half2float(__ushort_as_half(gd.s));
-      const float bi = brow ? __half2float(__ushort_as_half(gd.b)) : __fmul_rn(-0.5f, sc);
+      const float sc = meta_f32(gd.s, mbf16 != 0);
+      const float bi = brow ? meta_f32(gd.b, mbf16 != 0) : __fmul_rn(-0.5f, sc);
       const uint32_t lo16 = __half_as_ushort(__float2half_rn(bi));
       const uint32_t hi16 = __half_as_ushort(__float2half_rn(__fadd_rn(sc, bi)));
       const uint32_t lo2 = lo16 | (lo16 << 16), hi2 = hi16 | (hi16 << 16);
@@ -408,24 +442,21 @@ wide_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint32_t *__restri
                             __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
         } else if (m < M) {
           const int n = n0 + col;
-          __nv_bfloat16 *dst = y + (size_t)m * N + n;
-          // 16-byte stores need 16-byte aligned rows: N % 8 == 0
-          if (n + 32 <= N && (N & 7) == 0) {
+          const size_t i0 = (size_t)m * N + n;
+          // 16-byte stores need 16-byte aligned rows: N % 8 == 0 (16-bit
+          // outputs) or N % 4 == 0 (fp32)
+          if (n + 32 <= N && (N & (ydt == Q1_F32 ? 3 : 7)) == 0) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              uint32_t p[4];
+              float f[8];
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                __nv_bfloat162 t2 = __floats2bfloat162_rn(__uint_as_float(v[8 * q + 2 * e]) * rs,
-                                                          __uint_as_float(v[8 * q + 2 * e + 1]) * rs);
-                p[e] = *reinterpret_cast<uint32_t *>(&t2);
-              }
-              reinterpret_cast<uint4 *>(dst)[q] = make_uint4(p[0], p[1], p[2], p[3]);
+              for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(v[8 * q + e]) * rs;
+              store8(y, i0 + 8 * q, f, ydt);
             }
           } else {
 #pragma unroll
             for (int e = 0; e < 32; ++e)
-              if (n + e < N) dst[e] = __float2bfloat16_rn(__uint_as_float(v[e]) * rs);
+              if (n + e < N) store1(y, i0 + e, __uint_as_float(v[e]) * rs, ydt);
           }
         }
       }
@@ -453,15 +484,12 @@ wide_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint32_t *__restri
       const int m = m0 + r, n = n0 + 4 * c4;
       if (m < M && n < N) {
         const float rs = inv_scale[m];
-        __nv_bfloat16 *dst = y + (size_t)m * N + n;
+        const size_t i0 = (size_t)m * N + n;
+        const float a4[4] = {acc.x * rs, acc.y * rs, acc.z * rs, acc.w * rs};
         if (n + 4 <= N && (N & 3) == 0) {
-          const __nv_bfloat162 p0 = __floats2bfloat162_rn(acc.x * rs, acc.y * rs);
-          const __nv_bfloat162 p1 = __floats2bfloat162_rn(acc.z * rs, acc.w * rs);
-          *reinterpret_cast<uint2 *>(dst) =
-              make_uint2(*reinterpret_cast<const uint32_t *>(&p0), *reinterpret_cast<const uint32_t *>(&p1));
+          store4(y, i0, a4, ydt);
         } else {
-          const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
-          for (int e = 0; e < 4 && n + e < N; ++e) dst[e] = __float2bfloat16_rn(a4[e] * rs);
+          for (int e = 0; e < 4 && n + e < N; ++e) store1(y, i0 + e, a4[e], ydt);
         }
       }
     }
@@ -475,26 +503,51 @@ wide_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint32_t *__restri
 }
 
 // x [M][K] bf16 -> x16 [M][K] fp16 = x * 2^e_m and inv_scale[m] = 2^-e_m, with
+// Eight activations x[m][8i .. 8i+7] as fp32 (bf16 and fp16 widen exactly).
+template <int XDT>
+__device__ __forceinline__ void load8(const void *__restrict__ row, int i, float (&f)[8]) {
+  if (XDT == Q1_F32) {
+    const uint4 *p = reinterpret_cast<const uint4 *>(row) + 2 * i;
+    const uint4 a = __ldg(p), b = __ldg(p + 1);
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) f[j] = __uint_as_float(w[j]);
+  } else {
+    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(row) + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (XDT == Q1_F16) {
+        const float2 t = __half22float2(*reinterpret_cast<const __half2 *>(&w[q]));
+        f[2 * q] = t.x;
+        f[2 * q + 1] = t.y;
+      } else {
+        f[2 * q] = __uint_as_float(w[q] << 16);
+        f[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
+      }
+    }
+  }
+}
+
 // e_m = 14 - floor(log2(max_k |x[m][k]|)) so that the row maximum lands in
 // [2^14, 2^15).  Multiplying by a power of two is exact; the fp16 rounding is
-// exact for every result that is a normal fp16 value.  One warp per row.
-__global__ void __launch_bounds__(256) x_to_f16_kernel(const __nv_bfloat16 *__restrict__ x, int M,
+// exact for every bf16 or fp16 activation whose scaled value is a normal fp16
+// number, and rounds fp32 activations once (2^-11).  One warp per row.
+template <int XDT>
+__global__ void __launch_bounds__(256) x_to_f16_kernel(const void *__restrict__ x, int M,
                                                        int K, __half *__restrict__ x16,
                                                        float *__restrict__ inv_scale) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (warp >= M) return;
-  const uint4 *row = reinterpret_cast<const uint4 *>(x + (size_t)warp * K);
-  const int n16 = K / 8;  // 16-byte chunks
+  const void *row = static_cast<const char *>(x) + (size_t)warp * K * (XDT == Q1_F32 ? 4 : 2);
+  const int n8 = K / 8;  // chunks of 8 activations
   float mx = 0.f;
-  for (int i = lane; i < n16; i += 32) {
-    uint4 v = __ldg(row + i);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  for (int i = lane; i < n8; i += 32) {
+    float f[8];
+    load8<XDT>(row, i, f);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      mx = fmaxf(mx, fabsf(__uint_as_float(w[q] << 16)));
-      mx = fmaxf(mx, fabsf(__uint_as_float(w[q] & 0xFFFF0000u)));
-    }
+    for (int j = 0; j < 8; ++j) mx = fmaxf(mx, fabsf(f[j]));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
@@ -508,14 +561,13 @@ __global__ void __launch_bounds__(256) x_to_f16_kernel(const __nv_bfloat16 *__re
   const float sc = __uint_as_float((uint32_t)(127 + e) << 23);   // 2^e, exact
   const float isc = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e, exact
   uint4 *out = reinterpret_cast<uint4 *>(x16 + (size_t)warp * K);
-  for (int i = lane; i < n16; i += 32) {
-    uint4 v = __ldg(row + i);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  for (int i = lane; i < n8; i += 32) {
+    float f[8];
+    load8<XDT>(row, i, f);
     uint32_t o[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const __half2 h = __floats2half2_rn(__uint_as_float(w[q] << 16) * sc,
-                                          __uint_as_float(w[q] & 0xFFFF0000u) * sc);
+      const __half2 h = __floats2half2_rn(f[2 * q] * sc, f[2 * q + 1] * sc);
       o[q] = *reinterpret_cast<const uint32_t *>(&h);
     }
     out[i] = make_uint4(o[0], o[1], o[2], o[3]);
@@ -538,7 +590,7 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 
 template <int MT, bool SPLIT>
 cudaError_t launch_wide_mma(const WeightView &W, const __half *x16, int64_t M, const float *inv_scale, void *y,
-                            int ksplit, cudaStream_t st) {
+                            int ksplit, cudaStream_t st, q1_dtype dt) {
   auto encode = get_encode();
   if (!encode) return cudaErrorNotSupported;
   CUtensorMap map;
@@ -573,7 +625,7 @@ cudaError_t launch_wide_mma(const WeightView &W, const __half *x16, int64_t M, c
   cfg.attrs = attrs;
   cfg.numAttrs = SPLIT ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, wide_kernel<MT, SPLIT>, map, W.w, W.s, W.b, (int)M, (int)W.N, (int)W.K,
-                            inv_scale, static_cast<__nv_bfloat16 *>(y), SPLIT ? ksplit : 1);
+                            inv_scale, y, SPLIT ? ksplit : 1, W.mbf16 ? 1 : 0, (int)dt);
 }
 
 // Clusters of `ks` split-K CTAs that can be resident at once (one per SM).
@@ -610,7 +662,7 @@ size_t wide_workspace_bytes(int64_t M, int64_t K) {
 }
 
 cudaError_t launch_wide(const WeightView &W, const void *x, int64_t M, void *y, void *ws,
-                        cudaStream_t st) {
+                        cudaStream_t st, q1_dtype dt) {
   auto encode = get_encode();
   if (!encode) return cudaErrorNotSupported;
   __half *x16 = static_cast<__half *>(ws);
@@ -619,8 +671,9 @@ cudaError_t launch_wide(const WeightView &W, const void *x, int64_t M, void *y, 
   // 1. fp16 rows with per-row power-of-two scales
   {
     const unsigned blocks = (unsigned)((M * 32 + 255) / 256);
-    x_to_f16_kernel<<<blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(x), (int)M, (int)W.K,
-                                            x16, inv_scale);
+    if (dt == Q1_F32) x_to_f16_kernel<Q1_F32><<<blocks, 256, 0, st>>>(x, (int)M, (int)W.K, x16, inv_scale);
+    else if (dt == Q1_F16) x_to_f16_kernel<Q1_F16><<<blocks, 256, 0, st>>>(x, (int)M, (int)W.K, x16, inv_scale);
+    else x_to_f16_kernel<Q1_BF16><<<blocks, 256, 0, st>>>(x, (int)M, (int)W.K, x16, inv_scale);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -660,9 +713,9 @@ cudaError_t launch_wide(const WeightView &W, const void *x, int64_t M, void *y, 
       best_split = ks;
     }
   }
-  if (mode == 2) return launch_wide_mma<2, false>(W, x16, M, inv_scale, y, 1, st);
-  if (mode == 3) return launch_wide_mma<1, true>(W, x16, M, inv_scale, y, best_split, st);
-  return launch_wide_mma<1, false>(W, x16, M, inv_scale, y, 1, st);
+  if (mode == 2) return launch_wide_mma<2, false>(W, x16, M, inv_scale, y, 1, st, dt);
+  if (mode == 3) return launch_wide_mma<1, true>(W, x16, M, inv_scale, y, best_split, st, dt);
+  return launch_wide_mma<1, false>(W, x16, M, inv_scale, y, 1, st, dt);
 }
 
 unsigned int read_and_clear_wide_errors(cudaStream_t st, cudaError_t *err) {

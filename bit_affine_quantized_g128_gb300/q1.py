@@ -37,7 +37,12 @@ class Q1Error(RuntimeError):
 
 class _CWeight(ctypes.Structure):
     _fields_ = [("w", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("biases", ctypes.c_void_p),
-                ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("group_size", ctypes.c_int32)]
+                ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("group_size", ctypes.c_int32),
+                ("meta_dtype", ctypes.c_int32)]
+
+
+# q1_meta_dtype of the scales/biases tensors
+_META = {torch.float16: 0, torch.bfloat16: 1}
 
 
 class _CLayer(ctypes.Structure):
@@ -111,17 +116,20 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
 
 class Q1Weight:
     """A packed Q1 weight on the GPU: words uint32 [N, K/32] (held as int32),
-    fp16 scales [N, K/128] and fp16 biases [N, K/128] or None (symmetric)."""
+    scales [N, K/128] and biases [N, K/128] or None (symmetric), the metadata
+    either fp16 or bf16 (both tensors the same dtype)."""
 
     def __init__(self, words: torch.Tensor, scales: torch.Tensor,
                  biases: Optional[torch.Tensor], K: int):
         self.words = words.contiguous()
         self.scales = scales.contiguous()
         self.biases = None if biases is None else biases.contiguous()
+        if self.scales.dtype not in _META or (self.biases is not None and self.biases.dtype != self.scales.dtype):
+            raise ValueError("Q1Weight: scales and biases must both be float16 or both bfloat16")
         self.N = int(words.shape[0])
         self.K = int(K)
         self._c = _CWeight(self.words.data_ptr(), self.scales.data_ptr(),
-                           _ptr(self.biases), self.N, self.K, 128)
+                           _ptr(self.biases), self.N, self.K, 128, _META[self.scales.dtype])
 
     @property
     def symmetric(self) -> bool:

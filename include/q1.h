@@ -23,8 +23,13 @@
  *   - Arguments are validated on the host before anything is launched; an
  *     invalid argument returns an error status and launches nothing.  A failed
  *     launch returns Q1_ERR_CUDA.  No exception crosses the ABI.
- *   - Activations/outputs of the matmul calls are bf16 (Q1_BF16); other dtypes
- *     return Q1_ERR_DTYPE.
+ *   - Activations and outputs of the matmul and FFN calls share one dtype:
+ *     Q1_BF16, Q1_F16 or Q1_F32 (q1_decode_chain: Q1_BF16 only).  The narrow
+ *     path's tensor-core operands are bf16, so fp16 and fp32 activations are
+ *     rounded once to bf16 as they are loaded (relative error <= 2^-9 per
+ *     activation); the prefill path scales them into fp16 rows (exact for bf16
+ *     and fp16 activations, one rounding at 2^-11 for fp32).  Accumulation is
+ *     fp32 and the output is rounded once to the dtype.
  *   - Calls that need scratch (q1_qmm on its prefill path, q1_ffn_fused for
  *     its intermediate activations) take a caller-owned device workspace and
  *     its size; q1_qmm_workspace_size / q1_ffn_workspace_size return the
@@ -67,9 +72,21 @@ typedef enum {
 
 typedef enum { Q1_BF16 = 0, Q1_F16 = 1, Q1_F32 = 2 } q1_dtype;
 
+/* Type of the scales and biases.  fp16 is the rMLX checkpoint's ("The good
+ * news - packing is standard": scales+biases F16); bf16 is the Bonsai image
+ * checkpoint's ("1-bit Bonsai Image support", MLX-Gen backlog, "Context": BF16
+ * scales/biases, bits 1, group_size 128).  Both widen to fp32 exactly, and all
+ * arithmetic on them is the same. */
+typedef enum { Q1_META_F16 = 0, Q1_META_BF16 = 1 } q1_meta_dtype;
+
 /* One packed Q1 weight.  All pointers are device pointers owned by the caller.
- *   w: 16-byte aligned.  scales/biases: 2-byte aligned.
- *   N >= 1, K >= 128, K % 128 == 0, group_size == 128. */
+ *   w: 16-byte aligned.  scales/biases: 2-byte aligned, meta_dtype each.
+ *   N >= 1, K >= 128, K % 128 == 0, group_size == 128.
+ *   meta_dtype: Q1_META_F16 (0, so a zero-initialised field means fp16) or
+ *   Q1_META_BF16; anything else returns Q1_ERR_DTYPE.
+ * The prefill path (q1_qmm above the narrow threshold) builds fp16 weight
+ * tiles: with bf16 metadata, dequantized values must lie within fp16's range
+ * (|value| <= 65504), as every fp16 checkpoint's do. */
 typedef struct {
   const uint32_t *w;
   const uint16_t *scales;
@@ -77,6 +94,7 @@ typedef struct {
   int64_t N;
   int64_t K;
   int32_t group_size;
+  int32_t meta_dtype;     /* q1_meta_dtype */
 } q1_weight;
 
 /* ---- pack / unpack (rMLX issue #207, "packing is standard") ------------- */
@@ -118,7 +136,8 @@ q1_status q1_pack_from_dense(const void *dense, q1_dtype in_t, int64_t N, int64_
                              q1_stream stream);
 
 /* ---- matmul: y[M][N] = x[M][K] . Wd^T ------------------------------------
- * fp32 accumulation, bf16 in and out.  x and y 16-byte aligned.
+ * fp32 accumulation; x and y in `dtype` (bf16, fp16 or fp32, see above).
+ * x and y 16-byte aligned.
  * q1_qmv: the M = 1 decode product (higgs PR #212, "What": the Q1 decode tile).
  * q1_qmm_narrow: 1 <= M <= 8 (speculative-verifier windows) with the weights
  *   kept packed and no dense temporary (higgs PR #212, "What": narrow Q1
@@ -160,7 +179,8 @@ q1_status q1_embed_gather(const q1_weight *E, const int32_t *ids, int64_t T, q1_
 
 /* ---- fused dense FFN (higgs PR #212, "What": fused dense-FFN operations) ---
  * y[M][D] = Down . (SiLU(Gate . x) * (Up . x)) with SiLU(g) = g / (1 + e^-g).
- * gate, up: [F][D]; down: [D][F].  1 <= M <= 8; D, F <= 40960.  x [M][D], y [M][D] bf16.
+ * gate, up: [F][D]; down: [D][F].  1 <= M <= 8; D, F <= 40960.  x [M][D], y [M][D]
+ * in `dtype` (bf16, fp16 or fp32).
  * The intermediate h [M][F] is kept in bf16 at the start of the workspace
  * (q1_ffn_workspace_size(M, D, F) bytes, 256-byte aligned); it is still
  * there when the call's work completes. */

@@ -74,17 +74,40 @@ def pack(bits: np.ndarray) -> np.ndarray:
 # ---------------------------------------------------------------------------
 # Metadata ("Support Bonsai-27B affine Q1", section "What": bias = -scale/2)
 # ---------------------------------------------------------------------------
-def resolve_metadata(scales: np.ndarray, biases: np.ndarray | None):
-    """fp16 scales/biases [N, G] -> (s, b) in fp32.
+def meta32(m) -> np.ndarray:
+    """Metadata values widened to fp32, exactly.
+
+    fp16 arrays (the rMLX checkpoint's F16 scales+biases) and bf16 tensors
+    (the Bonsai image checkpoint's BF16 scales/biases) both widen without
+    rounding; an fp32 array is taken as already widened (e.g. bf16 values
+    held in fp32).  Any other dtype is rounded to fp16 first.
+    """
+    if isinstance(m, torch.Tensor):
+        return m.detach().to(torch.float32).numpy()
+    m = np.asarray(m)
+    if m.dtype == np.float32:
+        return m
+    return m.astype(np.float16).astype(np.float32)
+
+
+def _take_rows(m, rows):
+    """Rows of a metadata array or tensor (fp16 array or bf16 tensor)."""
+    if isinstance(m, torch.Tensor):
+        return m[torch.as_tensor(rows)] if not isinstance(rows, slice) else m[rows]
+    return np.asarray(m)[rows]
+
+
+def resolve_metadata(scales, biases):
+    """Scales/biases [N, G] (fp16 or bf16, see meta32) -> (s, b) in fp32.
 
     Affine: b = fp32(bias).  Symmetric (biases is None): b = -0.5 * s in fp32,
-    which is exact (halving an fp16 value in fp32 never rounds).
+    which is exact (halving an fp16 or bf16 value in fp32 never rounds).
     """
-    s = np.asarray(scales, dtype=np.float16).astype(np.float32)
+    s = meta32(scales)
     if biases is None:
         b = np.float32(-0.5) * s
     else:
-        b = np.asarray(biases, dtype=np.float16).astype(np.float32)
+        b = meta32(biases)
     return s, b
 
 
@@ -148,8 +171,8 @@ def qmm(x, words, scales, biases, K: int, rows=None) -> np.ndarray:
     if rows is not None:
         rows = np.asarray(rows)
         words = np.asarray(words)[rows]
-        scales = np.asarray(scales)[rows]
-        biases = None if biases is None else np.asarray(biases)[rows]
+        scales = _take_rows(scales, rows)
+        biases = None if biases is None else _take_rows(biases, rows)
     wd = dequantize_f32(words, scales, biases, K).astype(np.float64)
     x64 = _x64(x)
     if x64.ndim == 1:
@@ -219,8 +242,8 @@ def embed_gather(ids, words, scales, biases, K: int, dtype: str = "bf16"):
         if r < 0 or r >= V:
             bad += 1
             continue
-        b_row = None if biases is None else np.asarray(biases)[r:r + 1]
-        out[t] = dequantize_f32(np.asarray(words)[r:r + 1], np.asarray(scales)[r:r + 1],
+        b_row = None if biases is None else _take_rows(biases, slice(r, r + 1))
+        out[t] = dequantize_f32(np.asarray(words)[r:r + 1], _take_rows(scales, slice(r, r + 1)),
                                 b_row, K)[0]
     return round_to(out, dtype), bad
 

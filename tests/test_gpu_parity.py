@@ -322,6 +322,135 @@ def test_ffn_fused(q1, M, D, F):
     check_matmul(y, yo, ho, O.dequantize_f32(down.words, down.scales, None, F), f"ffn M={M}")
 
 
+# ------------------------------------------------------------------ bf16 metadata
+def _bf16_meta(t):
+    """The same bits with the drawn metadata rounded to bf16 (torch tensors)."""
+    s = torch.from_numpy(t.scales.astype(np.float32)).to(torch.bfloat16)
+    b = None if t.biases is None else torch.from_numpy(t.biases.astype(np.float32)).to(torch.bfloat16)
+    return t.words, s, b
+
+
+def _dev_bf16(t):
+    w, s, b = _bf16_meta(t)
+    return q1_weight_from(w, s, b, t.K)
+
+
+def q1_weight_from(words, s, b, K):
+    from bit_affine_quantized_g128_gb300 import q1 as mod
+    return mod.Q1Weight(torch.from_numpy(words.view("<i4").copy()).to(DEV), s.to(DEV),
+                        None if b is None else b.to(DEV), K)
+
+
+@pytest.mark.parametrize("affine", [False, True])
+def test_bf16_metadata_dequantize_and_gather_bit_exact(q1, affine):
+    N, K = 300, 640
+    t = synth.q1_tensor(N, K, seed=601 + affine, affine=affine)
+    w, s, b = _bf16_meta(t)
+    # one scale beyond fp16's range: fine for dequantize and gather (fp32 math)
+    s[7, 2] = 65536.0
+    W = q1_weight_from(w, s, b, K)
+    for dt, name in ((torch.float32, "f32"), (torch.bfloat16, "bf16"), (torch.float16, "f16")):
+        got = q1.dequantize(W, dt).cpu()
+        want = O.dequantize(w, s, b, K, name)
+        it = torch.int32 if dt == torch.float32 else torch.int16
+        assert torch.equal(got.view(it), want.view(it)), name
+    ids = synth.token_ids(40, N, seed=603)
+    ids[3] = 7
+    out, bad = q1.embed_gather(W, torch.from_numpy(ids).to(DEV), torch.float32)
+    want, nbad = O.embed_gather(ids, w, s, b, K, "f32")
+    assert int(bad.item()) == nbad == 0
+    assert torch.equal(out.cpu().view(torch.int32), want.view(torch.int32))
+
+
+@pytest.mark.parametrize("affine", [False, True])
+@pytest.mark.parametrize("M", [1, 3, 8, 200])
+def test_bf16_metadata_matmul(q1, affine, M):
+    N, K = 777, 1536
+    t, x = _case(N, K, M, affine, seed=611 + M + affine)
+    w, s, b = _bf16_meta(t)
+    W = q1_weight_from(w, s, b, K)
+    y = q1.qmm(W, x.to(DEV))  # narrow for M <= 8, prefill for M = 200
+    check_matmul(y, O.qmm(x, w, s, b, K), x, O.dequantize_f32(w, s, b, K), f"bf16 meta M={M}")
+
+
+def test_bf16_metadata_ffn_mixed_with_fp16(q1):
+    # gate bf16, up fp16, down bf16: the gate/up launch reads each matrix's own type
+    M, D, F = 4, 512, 1408
+    gate = synth.q1_tensor(F, D, seed=621, affine=False)
+    up = synth.q1_tensor(F, D, seed=622, affine=False)
+    down = synth.q1_tensor(D, F, seed=623, affine=False)
+    x = synth.activations(M, D, seed=624)
+    gw, gs, _ = _bf16_meta(gate)
+    dw, ds, _ = _bf16_meta(down)
+    G, U, Dn = q1_weight_from(gw, gs, None, D), q1.Q1Weight.from_host(up), q1_weight_from(dw, ds, None, F)
+    ws = q1.ffn_workspace(M, D, F, DEV)
+    y = q1.ffn_fused(G, U, Dn, x.to(DEV), workspace=ws)
+    yo, ho = O.ffn(x, (gw, gs, None, D), (up.words, up.scales, None, D), (dw, ds, None, F))
+    check_matmul(y, yo, ho, O.dequantize_f32(dw, ds, None, F), "ffn bf16/fp16 metadata")
+
+
+def test_bf16_metadata_check_symmetric(q1):
+    t = synth.q1_tensor(64, 256, seed=631, affine=False)
+    s = torch.from_numpy(t.scales.astype(np.float32)).to(torch.bfloat16)
+    b = (s.float() * -0.5).to(torch.bfloat16)  # exact: halving a bf16 value
+    W = q1_weight_from(t.words, s, b, 256)
+    assert int(q1.check_symmetric(W).item()) == 1 == int(O.is_symmetric(s, b))
+    b2 = b.clone()
+    b2[5, 1] = 0.25
+    W2 = q1_weight_from(t.words, s, b2, 256)
+    assert int(q1.check_symmetric(W2).item()) == 0 == int(O.is_symmetric(s, b2))
+
+
+def test_meta_dtype_is_validated(q1):
+    t = synth.q1_tensor(16, 128, seed=641, affine=False)
+    W = q1.Q1Weight.from_host(t)
+    W._c.meta_dtype = 2
+    x = torch.zeros((1, 128), dtype=torch.bfloat16, device=DEV)
+    y = torch.empty((1, 16), dtype=torch.bfloat16, device=DEV)
+    st = q1.lib().q1_qmv(W.cref(), x.data_ptr(), 0, y.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert st == 4  # Q1_ERR_DTYPE
+
+
+# ------------------------------------------------------------------ fp16 / fp32 activations
+def _acts(M, K, seed, dtype):
+    """N(0, 1) activations drawn in fp32 (so that fp32 inputs carry more than
+    bf16's 8 bits), rounded to fp16 for the fp16 case."""
+    x = torch.from_numpy(np.random.default_rng(seed).standard_normal((M, K)).astype(np.float32))
+    return x.to(dtype)
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.float32])
+@pytest.mark.parametrize("affine", [False, True])
+@pytest.mark.parametrize("M", [1, 5, 8, 200])
+def test_fp16_fp32_activations(q1, dtype, affine, M):
+    N, K = 600, 1280
+    t = synth.q1_tensor(N, K, seed=651 + affine, affine=affine)
+    x = _acts(M, K, 652 + M, dtype)
+    W = q1.Q1Weight.from_host(t)
+    y = q1.qmm(W, x.to(DEV))  # narrow for M <= 8, prefill for M = 200
+    assert y.dtype == dtype and y.shape == (M, N)
+    check_matmul(y, O.qmm(x, t.words, t.scales, t.biases, K), x,
+                 O.dequantize_f32(t.words, t.scales, t.biases, K), f"{dtype} M={M}")
+    if M == 1:
+        yv = q1.qmv(W, x[0].to(DEV))
+        assert torch.equal(yv.reshape(1, N), y)
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.float32])
+def test_ffn_fp16_fp32_activations(q1, dtype):
+    M, D, F = 3, 512, 1408
+    gate = synth.q1_tensor(F, D, seed=661, affine=False)
+    up = synth.q1_tensor(F, D, seed=662, affine=False)
+    down = synth.q1_tensor(D, F, seed=663, affine=False)
+    x = _acts(M, D, 664, dtype)
+    G, U, Dn = (q1.Q1Weight.from_host(w) for w in (gate, up, down))
+    y = q1.ffn_fused(G, U, Dn, x.to(DEV))
+    assert y.dtype == dtype
+    yo, ho = O.ffn(x, (gate.words, gate.scales, None, D), (up.words, up.scales, None, D),
+                   (down.words, down.scales, None, F))
+    check_matmul(y, yo, ho, O.dequantize_f32(down.words, down.scales, None, F), f"ffn {dtype}")
+
+
 # ------------------------------------------------------------------ exact repack from dense
 _TORCH = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}
 _INT = {"bf16": torch.int16, "f16": torch.int16, "f32": torch.int32}

@@ -92,6 +92,23 @@ def test_dequant_golden_values():
         assert np.all(hf == int(f16h, 16)), (sh, bh, q, hex(hf[0, 0]))
 
 
+def test_dequant_bf16_metadata_golden():
+    """bf16 scales/biases widen exactly (hand-derived values in the fixture)."""
+    n = 0
+    for sc_h, b_h, want0, want1, _ in _rows("dequant_bf16_meta.txt"):
+        words = np.array([[0xAAAAAAAA, 0, 0, 0]], dtype=np.uint32)  # k = 1, 3, 5, ... set in word 0
+        sc = torch.tensor([[int(sc_h, 16)]], dtype=torch.int16).view(torch.bfloat16)
+        b = None if b_h == "sym" else torch.tensor([[int(b_h, 16) - (1 << 16) * (int(b_h, 16) >= 1 << 15)]],
+                                                   dtype=torch.int16).view(torch.bfloat16)
+        if int(sc_h, 16) >= 1 << 15:
+            raise AssertionError("fixture scales are positive")
+        d = O.dequantize_f32(words, sc, b, 128)
+        assert _bits32(d[0, 0]) == int(want0, 16), (sc_h, b_h)
+        assert _bits32(d[0, 1]) == int(want1, 16), (sc_h, b_h)
+        n += 1
+    assert n == 7
+
+
 def test_bf16_rounding_golden():
     for f32h, bf16h in _rows("bf16_rounding.txt"):
         v = np.frombuffer(struct.pack("<I", int(f32h, 16)), dtype=np.float32)
