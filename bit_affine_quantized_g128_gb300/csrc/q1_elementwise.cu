@@ -143,14 +143,14 @@ __device__ __forceinline__ void emit_word(float lo, float hi, uint32_t word, voi
 template <int OUT>
 __global__ void dequantize_kernel(const uint32_t *__restrict__ w, const uint16_t *__restrict__ s,
                                   const uint16_t *__restrict__ b, int64_t N, int64_t K, bool mbf16,
-                                  void *__restrict__ out) {
-  const int64_t wpr = K / 32, G = K / 128, nwords = N * wpr;
+                                  int gshift, void *__restrict__ out) {
+  const int64_t wpr = K / 32, G = wpr >> gshift, nwords = N * wpr;  // G: metadata groups per row
   const int esz = OUT == 2 ? 4 : 2;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nwords;
        i += (int64_t)gridDim.x * blockDim.x) {
     int64_t n = i / wpr, c = i - n * wpr;
     float lo, hi;
-    group_values(s, b, n * G + c / 4, mbf16, lo, hi);
+    group_values(s, b, n * G + (c >> gshift), mbf16, lo, hi);
     emit_word<OUT>(lo, hi, w[i], static_cast<char *>(out) + n * K * esz, c);
   }
 }
@@ -158,9 +158,9 @@ __global__ void dequantize_kernel(const uint32_t *__restrict__ w, const uint16_t
 template <int OUT>
 __global__ void gather_kernel(const uint32_t *__restrict__ w, const uint16_t *__restrict__ s,
                               const uint16_t *__restrict__ b, int64_t V, int64_t K, bool mbf16,
-                              const int32_t *__restrict__ ids, int64_t T, void *__restrict__ out,
-                              int32_t *__restrict__ bad) {
-  const int64_t wpr = K / 32, G = K / 128, nwords = T * wpr;
+                              int gshift, const int32_t *__restrict__ ids, int64_t T,
+                              void *__restrict__ out, int32_t *__restrict__ bad) {
+  const int64_t wpr = K / 32, G = wpr >> gshift, nwords = T * wpr;
   const int esz = OUT == 2 ? 4 : 2;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nwords;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -175,7 +175,7 @@ __global__ void gather_kernel(const uint32_t *__restrict__ w, const uint16_t *__
       continue;
     }
     float lo, hi;
-    group_values(s, b, row * G + c / 4, mbf16, lo, hi);
+    group_values(s, b, row * G + (c >> gshift), mbf16, lo, hi);
     emit_word<OUT>(lo, hi, w[row * wpr + c], out_row, c);
   }
 }
@@ -398,9 +398,9 @@ cudaError_t launch_dequantize(const WeightView &W, q1_dtype t, void *out, cudaSt
   int64_t nwords = W.N * (W.K / 32);
   unsigned g = grid_for(nwords, 256);
   switch (t) {
-    case Q1_BF16: dequantize_kernel<0><<<g, 256, 0, st>>>(W.w, W.s, W.b, W.N, W.K, W.mbf16, out); break;
-    case Q1_F16: dequantize_kernel<1><<<g, 256, 0, st>>>(W.w, W.s, W.b, W.N, W.K, W.mbf16, out); break;
-    default: dequantize_kernel<2><<<g, 256, 0, st>>>(W.w, W.s, W.b, W.N, W.K, W.mbf16, out); break;
+    case Q1_BF16: dequantize_kernel<0><<<g, 256, 0, st>>>(W.w, W.s, W.b, W.N, W.K, W.mbf16, W.gshift, out); break;
+    case Q1_F16: dequantize_kernel<1><<<g, 256, 0, st>>>(W.w, W.s, W.b, W.N, W.K, W.mbf16, W.gshift, out); break;
+    default: dequantize_kernel<2><<<g, 256, 0, st>>>(W.w, W.s, W.b, W.N, W.K, W.mbf16, W.gshift, out); break;
   }
   return cudaGetLastError();
 }
@@ -411,13 +411,13 @@ cudaError_t launch_gather(const WeightView &E, const int32_t *ids, int64_t T, q1
   unsigned g = grid_for(nwords, 256);
   switch (t) {
     case Q1_BF16:
-      gather_kernel<0><<<g, 256, 0, st>>>(E.w, E.s, E.b, E.N, E.K, E.mbf16, ids, T, out, bad);
+      gather_kernel<0><<<g, 256, 0, st>>>(E.w, E.s, E.b, E.N, E.K, E.mbf16, E.gshift, ids, T, out, bad);
       break;
     case Q1_F16:
-      gather_kernel<1><<<g, 256, 0, st>>>(E.w, E.s, E.b, E.N, E.K, E.mbf16, ids, T, out, bad);
+      gather_kernel<1><<<g, 256, 0, st>>>(E.w, E.s, E.b, E.N, E.K, E.mbf16, E.gshift, ids, T, out, bad);
       break;
     default:
-      gather_kernel<2><<<g, 256, 0, st>>>(E.w, E.s, E.b, E.N, E.K, E.mbf16, ids, T, out, bad);
+      gather_kernel<2><<<g, 256, 0, st>>>(E.w, E.s, E.b, E.N, E.K, E.mbf16, E.gshift, ids, T, out, bad);
       break;
   }
   return cudaGetLastError();
@@ -427,7 +427,7 @@ cudaError_t launch_check_symmetric(const WeightView &W, int32_t *result, cudaStr
   set_flag_kernel<<<1, 1, 0, st>>>(result, 1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  int64_t count = W.N * (W.K / 128);
+  int64_t count = W.N * ((W.K / 32) >> W.gshift);
   check_symmetric_kernel<<<grid_for(count, 256), 256, 0, st>>>(W.s, W.b, count, W.mbf16, result);
   return cudaGetLastError();
 }

@@ -23,10 +23,12 @@ struct WeightView {
   const uint16_t *b;  // nullptr: symmetric
   int64_t N, K;
   bool mbf16;         // scales/biases are bf16 (else fp16)
+  int gshift;         // log2(group_size / 32): 0, 1 or 2
 };
 
 inline WeightView view(const q1_weight *W) {
-  return WeightView{W->w, W->scales, W->biases, W->N, W->K, W->meta_dtype == Q1_META_BF16};
+  return WeightView{W->w, W->scales, W->biases, W->N, W->K, W->meta_dtype == Q1_META_BF16,
+                    W->group_size == 32 ? 0 : (W->group_size == 64 ? 1 : 2)};
 }
 
 #ifdef __CUDACC__

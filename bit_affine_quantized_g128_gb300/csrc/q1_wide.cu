@@ -234,20 +234,24 @@ __device__ __forceinline__ void store8(void *y, size_t i, const float (&f)[8], i
   }
 }
 
+// One thread's share of a 128-k unit: its row's four words, and the metadata
+// of the two words it expands (k-steps 0 and 1); the same group for both
+// unless the group size is 32 or 64.
 struct GroupData {
   uint4 w;
-  uint16_t s, b;
+  uint16_t s[2], b[2];
 };
 
 // SPLIT: a thread-block cluster of `ksplit` CTAs shares one output tile, each
 // taking a contiguous range of the 128-k groups; the fp32 partial tiles are
 // summed through distributed shared memory in rank order (deterministic, no
 // workspace).  Only with MT = 1.
-template <int MT, bool SPLIT>
+template <int MT, bool SPLIT, bool G128>
 __global__ void __launch_bounds__(kThreadsWide, 1)
 wide_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint32_t *__restrict__ W,
             const uint16_t *__restrict__ S, const uint16_t *__restrict__ Bv, int M, int N, int K,
-            const float *__restrict__ inv_scale, void *__restrict__ y, int ksplit, int mbf16, int ydt) {
+            const float *__restrict__ inv_scale, void *__restrict__ y, int ksplit, int mbf16, int ydt,
+            int gshift) {
   static_assert(!SPLIT || MT == 1, "split-K keeps one token tile per CTA");
   extern __shared__ unsigned char smem_raw[];
   unsigned char *base = reinterpret_cast<unsigned char *>(
@@ -333,60 +337,114 @@ wide_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint32_t *__restri
     const int d = (tid - kDeqWarp0 * 32) >> 1, wh = tid & 1;
     const int n = n0 + d;
     const bool ok_row = n < N;
-    const int wpr = K / 32, G = K / 128;
+    const int wpr = K / 32, G = wpr >> gshift;  // G: metadata groups per row
     const uint4 *wrow = reinterpret_cast<const uint4 *>(W + (size_t)(ok_row ? n : 0) * wpr);
     const uint16_t *srow = S + (size_t)(ok_row ? n : 0) * G;
     const uint16_t *brow = Bv ? Bv + (size_t)(ok_row ? n : 0) * G : nullptr;
-    auto load = [&](int g, GroupData &gd) {
+    auto load = [&](int g, GroupData &gd) {  // g: 128-k unit
       if (g < g_hi && ok_row) {
         gd.w = __ldg(wrow + g);
-        gd.s = srow[g];
-        gd.b = brow ? brow[g] : (uint16_t)0;
+        if constexpr (G128) {  // one group per 128-k unit
+          gd.s[0] = gd.s[1] = srow[g];
+          gd.b[0] = gd.b[1] = brow ? brow[g] : (uint16_t)0;
+        } else {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int mi = (4 * g + 2 * h + wh) >> gshift;  // group of word 2h + wh
+            gd.s[h] = srow[mi];
+            gd.b[h] = brow ? brow[mi] : (uint16_t)0;
+          }
+        }
       } else {
         gd.w = make_uint4(0, 0, 0, 0);
-        gd.s = 0;
-        gd.b = 0;
+        gd.s[0] = gd.s[1] = gd.b[0] = gd.b[1] = 0;
       }
     };
     bool alive = true;
-    auto process = [&](int g, const GroupData &gd) {
-      const float sc = meta_f32(gd.s, mbf16 != 0);
-      const float bi = brow ? meta_f32(gd.b, mbf16 != 0) : __fmul_rn(-0.5f, sc);
+    // fp16x2 patterns of the two dequantized values (q = 0, q = 1) of a group
+    auto pair_of = [&](uint16_t s16, uint16_t b16, uint32_t &lo2, uint32_t &hi2) {
+      const float sc = meta_f32(s16, mbf16 != 0);
+      const float bi = brow ? meta_f32(b16, mbf16 != 0) : __fmul_rn(-0.5f, sc);
       const uint32_t lo16 = __half_as_ushort(__float2half_rn(bi));
       const uint32_t hi16 = __half_as_ushort(__float2half_rn(__fadd_rn(sc, bi)));
-      const uint32_t lo2 = lo16 | (lo16 << 16), hi2 = hi16 | (hi16 << 16);
-      // both k-steps of the group: wait for both stages, write both, then one
-      // proxy fence and the two arrivals (halves the fence/arrive hand-offs)
-      const int ks0 = 2 * (g - g_lo);  // this CTA's k-step
-      const int s0 = ks0 % STAGES, s1 = (ks0 + 1) % STAGES;
-      const uint32_t ph0 = (uint32_t)(ks0 / STAGES) & 1u, ph1 = (uint32_t)((ks0 + 1) / STAGES) & 1u;
-      // one lane waits, the warp follows its verdict (keeps the warp converged)
-      int okw = 0;
-      if (lane == 0)
-        okw = alive && mbar_wait(&sh->empty[s0], ph0 ^ 1u, sh) && mbar_wait(&sh->empty[s1], ph1 ^ 1u, sh);
-      okw = __shfl_sync(0xffffffffu, okw, 0);
-      if (!okw) {
-        alive = false;
-        return;
+      lo2 = lo16 | (lo16 << 16);
+      hi2 = hi16 | (hi16 << 16);
+    };
+    auto process = [&](int g, const GroupData &gd) {
+      uint32_t lo2v[2], hi2v[2];
+      pair_of(gd.s[0], gd.b[0], lo2v[0], hi2v[0]);
+      if constexpr (G128) {
+        lo2v[1] = lo2v[0];
+        hi2v[1] = hi2v[0];
+      } else {
+        pair_of(gd.s[1], gd.b[1], lo2v[1], hi2v[1]);
       }
+      if constexpr (MT == 2) {
+        // the group's two k-steps, one stage at a time: each stage is handed to
+        // the MMA as soon as it is written, so that the dequantizers can run up
+        // to STAGES stages ahead
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        unsigned char *rowp = sb + (h == 0 ? s0 : s1) * B_BYTES + d * 128;
-        const uint32_t word = h == 0 ? (wh == 0 ? gd.w.x : gd.w.y) : (wh == 0 ? gd.w.z : gd.w.w);
-        uint32_t out[16];
-        expand_word(word, lo2, hi2, out);
+        for (int h = 0; h < 2; ++h) {
+          const int ks = 2 * (g - g_lo) + h;  // this CTA's k-step
+          const int st = ks % STAGES;
+          const uint32_t ph = (uint32_t)(ks / STAGES) & 1u;
+          // one lane waits, the warp follows its verdict (keeps the warp converged)
+          int okw = 0;
+          if (lane == 0) okw = alive && mbar_wait(&sh->empty[st], ph ^ 1u, sh);
+          okw = __shfl_sync(0xffffffffu, okw, 0);
+          if (!okw) {
+            alive = false;
+            return;
+          }
+          unsigned char *rowp = sb + st * B_BYTES + d * 128;
+          const uint32_t word = h == 0 ? (wh == 0 ? gd.w.x : gd.w.y) : (wh == 0 ? gd.w.z : gd.w.w);
+          uint32_t out[16];
+          expand_word(word, lo2v[h], hi2v[h], out);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int c = wh * 4 + q;  // 16-byte chunk: k = 8c .. 8c+7 of this stage
-          *reinterpret_cast<uint4 *>(rowp + ((c ^ (d & 7)) << 4)) =
-              make_uint4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
+          for (int q = 0; q < 4; ++q) {
+            const int c = wh * 4 + q;  // 16-byte chunk: k = 8c .. 8c+7 of this stage
+            *reinterpret_cast<uint4 *>(rowp + ((c ^ (d & 7)) << 4)) =
+                make_uint4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh->full_b[st]);
         }
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&sh->full_b[s0]);
-        mbar_arrive(&sh->full_b[s1]);
+      } else {
+        // four stages: wait for both of the group's stages, write both, then
+        // one proxy fence and the two arrivals (halves the hand-offs; with four
+        // stages the dequantizers still run a stage ahead)
+        const int ks0 = 2 * (g - g_lo);  // this CTA's k-step
+        const int s0 = ks0 % STAGES, s1 = (ks0 + 1) % STAGES;
+        const uint32_t ph0 = (uint32_t)(ks0 / STAGES) & 1u, ph1 = (uint32_t)((ks0 + 1) / STAGES) & 1u;
+        // one lane waits, the warp follows its verdict (keeps the warp converged)
+        int okw = 0;
+        if (lane == 0)
+          okw = alive && mbar_wait(&sh->empty[s0], ph0 ^ 1u, sh) && mbar_wait(&sh->empty[s1], ph1 ^ 1u, sh);
+        okw = __shfl_sync(0xffffffffu, okw, 0);
+        if (!okw) {
+          alive = false;
+          return;
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          unsigned char *rowp = sb + (h == 0 ? s0 : s1) * B_BYTES + d * 128;
+          const uint32_t word = h == 0 ? (wh == 0 ? gd.w.x : gd.w.y) : (wh == 0 ? gd.w.z : gd.w.w);
+          uint32_t out[16];
+          expand_word(word, lo2v[h], hi2v[h], out);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int c = wh * 4 + q;  // 16-byte chunk: k = 8c .. 8c+7 of this stage
+            *reinterpret_cast<uint4 *>(rowp + ((c ^ (d & 7)) << 4)) =
+                make_uint4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
+          }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&sh->full_b[s0]);
+          mbar_arrive(&sh->full_b[s1]);
+        }
       }
     };
     GroupData r0, r1, r2;
@@ -588,8 +646,8 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
-template <int MT, bool SPLIT>
-cudaError_t launch_wide_mma(const WeightView &W, const __half *x16, int64_t M, const float *inv_scale, void *y,
+template <int MT, bool SPLIT, bool G128>
+cudaError_t launch_wide_mma_g(const WeightView &W, const __half *x16, int64_t M, const float *inv_scale, void *y,
                             int ksplit, cudaStream_t st, q1_dtype dt) {
   auto encode = get_encode();
   if (!encode) return cudaErrorNotSupported;
@@ -604,7 +662,7 @@ cudaError_t launch_wide_mma(const WeightView &W, const __half *x16, int64_t M, c
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(wide_kernel<MT, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(wide_kernel<MT, SPLIT, G128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes<MT>);
     if (e != cudaSuccess) return e;
     attr = true;
@@ -624,8 +682,17 @@ cudaError_t launch_wide_mma(const WeightView &W, const __half *x16, int64_t M, c
   attrs[1].val.clusterDim.z = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = SPLIT ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, wide_kernel<MT, SPLIT>, map, W.w, W.s, W.b, (int)M, (int)W.N, (int)W.K,
-                            inv_scale, y, SPLIT ? ksplit : 1, W.mbf16 ? 1 : 0, (int)dt);
+  return cudaLaunchKernelEx(&cfg, wide_kernel<MT, SPLIT, G128>, map, W.w, W.s, W.b, (int)M, (int)W.N, (int)W.K,
+                            inv_scale, y, SPLIT ? ksplit : 1, W.mbf16 ? 1 : 0, (int)dt, W.gshift);
+}
+
+// 128-groups (one scale per 128-k unit) compile to their own kernel: the
+// per-word metadata of 32- and 64-groups costs the dequantizers ~5 %.
+template <int MT, bool SPLIT>
+cudaError_t launch_wide_mma(const WeightView &W, const __half *x16, int64_t M, const float *inv_scale, void *y,
+                            int ksplit, cudaStream_t st, q1_dtype dt) {
+  if (W.gshift == 2) return launch_wide_mma_g<MT, SPLIT, true>(W, x16, M, inv_scale, y, ksplit, st, dt);
+  return launch_wide_mma_g<MT, SPLIT, false>(W, x16, M, inv_scale, y, ksplit, st, dt);
 }
 
 // Clusters of `ks` split-K CTAs that can be resident at once (one per SM).
@@ -644,9 +711,9 @@ int wide_split_clusters(int ks) {
   attr.val.clusterDim.z = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  cudaFuncSetAttribute(wide_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes<1>);
+  cudaFuncSetAttribute(wide_kernel<1, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes<1>);
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, wide_kernel<1, true>, &cfg) != cudaSuccess || n < 1) {
+  if (cudaOccupancyMaxActiveClusters(&n, wide_kernel<1, true, true>, &cfg) != cudaSuccess || n < 1) {
     cudaGetLastError();
     n = 0;
   }

@@ -128,8 +128,10 @@ class Q1Weight:
             raise ValueError("Q1Weight: scales and biases must both be float16 or both bfloat16")
         self.N = int(words.shape[0])
         self.K = int(K)
+        # weights per scale along K, from the metadata's shape [N, K / group_size]
+        self.group_size = self.K // max(int(self.scales.shape[-1]), 1)
         self._c = _CWeight(self.words.data_ptr(), self.scales.data_ptr(),
-                           _ptr(self.biases), self.N, self.K, 128, _META[self.scales.dtype])
+                           _ptr(self.biases), self.N, self.K, self.group_size, _META[self.scales.dtype])
 
     @property
     def symmetric(self) -> bool:
@@ -203,13 +205,14 @@ def qmm_narrow(W: Q1Weight, x: torch.Tensor, out=None) -> torch.Tensor:
 def qmm(W: Q1Weight, x: torch.Tensor, workspace: Optional[torch.Tensor] = None,
         out=None) -> torch.Tensor:
     """x [..., K] -> y [..., N]; narrow path up to the row threshold, tcgen05 beyond
-    (which needs a workspace; one is allocated when none is given)."""
+    and for group sizes 32 and 64 (which needs a workspace; one is allocated
+    when none is given)."""
     lead = x.shape[:-1]
     x2 = _flat(x, W.K)
     M = x2.shape[0]
     y = out if out is not None else torch.empty((M, W.N), dtype=x.dtype, device=x.device)
     ws = workspace
-    if ws is None and (M > get_qmm_max_rows() or W.K > NARROW_MAX_K):
+    if ws is None and (M > get_qmm_max_rows() or W.K > NARROW_MAX_K or W.group_size != 128):
         ws = qmm_workspace(M, W.N, W.K, x.device)
     wp, wn = (ws.data_ptr(), ws.numel()) if ws is not None else (None, 0)
     _check("q1_qmm", lib().q1_qmm(W.cref(), x2.data_ptr(), M, _DT[x.dtype], y.data_ptr(), wp, wn,

@@ -40,15 +40,15 @@ def weight_words(N: int, K: int, seed: int) -> np.ndarray:
     return _rng(seed).integers(0, 2**32, size=(N, K // BITS_PER_WORD), dtype=np.uint32)
 
 
-def scales(N: int, K: int, seed: int) -> np.ndarray:
-    """fp16 [N, K/128]: |N(0, 0.02)| + 1e-4, rounded to fp16."""
-    g = _rng(seed).standard_normal((N, K // GROUP), dtype=np.float32)
+def scales(N: int, K: int, seed: int, group: int = GROUP) -> np.ndarray:
+    """fp16 [N, K/group]: |N(0, 0.02)| + 1e-4, rounded to fp16."""
+    g = _rng(seed).standard_normal((N, K // group), dtype=np.float32)
     return (np.abs(g * np.float32(0.02)) + np.float32(1e-4)).astype(np.float16)
 
 
-def biases(N: int, K: int, seed: int) -> np.ndarray:
-    """fp16 [N, K/128]: N(0, 0.01), rounded to fp16 (affine metadata)."""
-    g = _rng(seed).standard_normal((N, K // GROUP), dtype=np.float32)
+def biases(N: int, K: int, seed: int, group: int = GROUP) -> np.ndarray:
+    """fp16 [N, K/group]: N(0, 0.01), rounded to fp16 (affine metadata)."""
+    g = _rng(seed).standard_normal((N, K // group), dtype=np.float32)
     return (g * np.float32(0.01)).astype(np.float16)
 
 
@@ -88,12 +88,12 @@ class Q1Tensor:
         return self.biases is None
 
 
-def q1_tensor(N: int, K: int, seed: int, affine: bool) -> Q1Tensor:
-    """A full synthetic Q1 weight.  Sub-streams: seed (words), seed+7919
-    (scales), seed+15485863 (biases)."""
+def q1_tensor(N: int, K: int, seed: int, affine: bool, group: int = GROUP) -> Q1Tensor:
+    """A full synthetic Q1 weight (metadata per `group` weights along K).
+    Sub-streams: seed (words), seed+7919 (scales), seed+15485863 (biases)."""
     w = weight_words(N, K, seed)
-    s = scales(N, K, seed + 7919)
-    b = biases(N, K, seed + 15485863) if affine else None
+    s = scales(N, K, seed + 7919, group)
+    b = biases(N, K, seed + 15485863, group) if affine else None
     return Q1Tensor(w, s, b, K)
 
 

@@ -63,7 +63,7 @@ typedef enum {
   Q1_ERR_SHAPE = 2,      /* N < 1, K < 128, K % 128 != 0, M out of range, ...   */
   Q1_ERR_ALIGN = 3,      /* a pointer is not aligned as documented              */
   Q1_ERR_DTYPE = 4,      /* unsupported dtype for this call                     */
-  Q1_ERR_GROUP = 5,      /* group_size != 128                                   */
+  Q1_ERR_GROUP = 5,      /* group_size not 32, 64 or 128, or not 128 where needed */
   Q1_ERR_WORKSPACE = 6,  /* workspace missing, too small or misaligned          */
   Q1_ERR_CUDA = 7,       /* a CUDA runtime call or launch failed                */
   Q1_ERR_TIMEOUT = 8,    /* a bounded device-side wait ran out                  */
@@ -81,7 +81,15 @@ typedef enum { Q1_META_F16 = 0, Q1_META_BF16 = 1 } q1_meta_dtype;
 
 /* One packed Q1 weight.  All pointers are device pointers owned by the caller.
  *   w: 16-byte aligned.  scales/biases: 2-byte aligned, meta_dtype each.
- *   N >= 1, K >= 128, K % 128 == 0, group_size == 128.
+ *   N >= 1, K >= 128, K % 128 == 0.
+ *   group_size: 128 (every checkpoint on the pages), or 32 or 64 (MLX's affine
+ *   format allows them; "1-bit affine weight support", rMLX issue #207, lists
+ *   "group_size=32 occupancy" among mlx#3161's edge cases).  scales/biases are
+ *   then [N][K/group_size].  Every call takes 128; q1_dequantize,
+ *   q1_embed_gather, q1_check_symmetric and q1_qmm also take 32 and 64 (q1_qmm
+ *   runs them on its prefill path for every M, so it needs its workspace);
+ *   the narrow-only calls (q1_qmv, q1_qmm_narrow, q1_ffn_fused*,
+ *   q1_decode_chain) return Q1_ERR_GROUP for them.
  *   meta_dtype: Q1_META_F16 (0, so a zero-initialised field means fp16) or
  *   Q1_META_BF16; anything else returns Q1_ERR_DTYPE.
  * The prefill path (q1_qmm above the narrow threshold) builds fp16 weight

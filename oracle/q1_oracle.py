@@ -97,6 +97,17 @@ def _take_rows(m, rows):
     return np.asarray(m)[rows]
 
 
+def group_size_of(K: int, s) -> int:
+    """Weights per scale along K, from the metadata's shape [N, K / group]:
+    128 for every checkpoint on the pages; MLX's affine format also has 32 and
+    64 ("1-bit affine weight support", rMLX issue #207: mlx#3161's
+    "group_size=32 occupancy" edge case)."""
+    G = np.asarray(s.shape)[1]
+    if G < 1 or K % G or (K // G) not in (32, 64, 128):
+        raise ValueError(f"metadata of {G} groups does not fit K = {K}")
+    return K // G
+
+
 def resolve_metadata(scales, biases):
     """Scales/biases [N, G] (fp16 or bf16, see meta32) -> (s, b) in fp32.
 
@@ -135,8 +146,9 @@ def dequantize_f32(words: np.ndarray, scales: np.ndarray, biases: np.ndarray | N
     """
     q = unpack(words, K)
     s, b = resolve_metadata(scales, biases)
-    s_k = np.repeat(s, GROUP_SIZE, axis=1)          # [N, K]
-    b_k = np.repeat(b, GROUP_SIZE, axis=1)
+    gs = group_size_of(K, s)
+    s_k = np.repeat(s, gs, axis=1)                  # [N, K]
+    b_k = np.repeat(b, gs, axis=1)
     one = (s_k + b_k).astype(np.float32)            # fl32(s + b)
     return np.where(q == 1, one, b_k).astype(np.float32)
 

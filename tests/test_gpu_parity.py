@@ -451,6 +451,48 @@ def test_ffn_fp16_fp32_activations(q1, dtype):
     check_matmul(y, yo, ho, O.dequantize_f32(down.words, down.scales, None, F), f"ffn {dtype}")
 
 
+# ------------------------------------------------------------------ group sizes 32 and 64
+@pytest.mark.parametrize("group", [32, 64])
+@pytest.mark.parametrize("affine", [False, True])
+def test_small_groups(q1, group, affine):
+    N, K = 300, 640
+    t = synth.q1_tensor(N, K, seed=671 + group + affine, affine=affine, group=group)
+    W = q1.Q1Weight.from_host(t)
+    assert W.group_size == group
+    for dt, name in ((torch.float32, "f32"), (torch.bfloat16, "bf16"), (torch.float16, "f16")):
+        it = torch.int32 if dt == torch.float32 else torch.int16
+        got = q1.dequantize(W, dt).cpu()
+        assert torch.equal(got.view(it), O.dequantize(t.words, t.scales, t.biases, K, name).view(it)), name
+    ids = synth.token_ids(24, N, seed=672)
+    out, bad = q1.embed_gather(W, torch.from_numpy(ids).to(DEV), torch.bfloat16)
+    want, _ = O.embed_gather(ids, t.words, t.scales, t.biases, K, "bf16")
+    assert int(bad.item()) == 0 and torch.equal(out.cpu().view(torch.int16), want.view(torch.int16))
+    wd = O.dequantize_f32(t.words, t.scales, t.biases, K)
+    for M in (1, 8, 200):  # every M runs on the prefill path
+        x = synth.activations(M, K, seed=673 + M)
+        y = q1.qmm(W, x.to(DEV))
+        check_matmul(y, O.qmm(x, t.words, t.scales, t.biases, K), x, wd, f"group {group} M={M}")
+    # the narrow-only calls refuse these group sizes
+    x1 = torch.zeros((K,), dtype=torch.bfloat16, device=DEV)
+    y1 = torch.empty((N,), dtype=torch.bfloat16, device=DEV)
+    st = torch.cuda.current_stream().cuda_stream
+    assert q1.lib().q1_qmv(W.cref(), x1.data_ptr(), 0, y1.data_ptr(), st) == 5
+    assert q1.lib().q1_qmm_narrow(W.cref(), x1.data_ptr(), 1, 0, y1.data_ptr(), st) == 5
+
+
+def test_small_groups_check_symmetric(q1):
+    t = synth.q1_tensor(64, 256, seed=681, affine=False, group=32)
+    s = t.scales
+    b = (-(s.astype(np.float32) / 2)).astype(np.float16)
+    W = q1.Q1Weight.from_host(synth.Q1Tensor(t.words, s, b, 256))
+    assert W.group_size == 32
+    assert int(q1.check_symmetric(W).item()) == 1 == int(O.is_symmetric(s, b))
+    b2 = b.copy()
+    b2[63, 7] = np.float16(0.25)  # the last group of the last row
+    W2 = q1.Q1Weight.from_host(synth.Q1Tensor(t.words, s, b2, 256))
+    assert int(q1.check_symmetric(W2).item()) == 0 == int(O.is_symmetric(s, b2))
+
+
 # ------------------------------------------------------------------ exact repack from dense
 _TORCH = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}
 _INT = {"bf16": torch.int16, "f16": torch.int16, "f32": torch.int32}

@@ -157,7 +157,7 @@ def test_symmetric_equals_affine_when_bias_is_exactly_minus_half_scale():
 
 
 # ---------------------------------------------------------------- matmul
-def _exact_qmm(x_bf16, words, scales, biases, K):
+def _exact_qmm(x_bf16, words, scales, biases, K, group=128):
     """Exact rational brute force: dequant with Python Fractions of the fp32
     values (derived independently of the oracle: bit test per weight, fp32
     add done by numpy scalar), then exact sums."""
@@ -167,8 +167,8 @@ def _exact_qmm(x_bf16, words, scales, biases, K):
     for n in range(N):
         for k in range(K):
             q = (int(words[n, k // 32]) >> (k % 32)) & 1
-            s = np.float32(scales[n, k // 128])
-            b = np.float32(biases[n, k // 128]) if biases is not None else np.float32(-0.5) * s
+            s = np.float32(scales[n, k // group])
+            b = np.float32(biases[n, k // group]) if biases is not None else np.float32(-0.5) * s
             w = np.float32(s + b) if q else b
             fw = Fraction(float(w))
             for m in range(M):
@@ -253,6 +253,49 @@ def test_affine_with_exact_minus_half_bias_close_to_symmetric():
     b = (-(s.astype(np.float32) / 2)).astype(np.float16)
     x = synth.activations(3, K, seed=122)
     np.testing.assert_array_equal(O.qmm(x, t.words, s, b, K), O.qmm(x, t.words, s, None, K))
+
+
+# ---------------------------------------------------------------- group sizes 32 and 64
+def test_dequant_group_32_hand_built():
+    """K = 128 in four groups of 32: each word takes its own scale."""
+    words = np.array([[0xFFFFFFFF, 0x00000000, 0x00000001, 0x80000000]], dtype=np.uint32)
+    scales = np.array([[1.0, 2.0, 0.5, 4.0]], dtype=np.float16)
+    d = O.dequantize_f32(words, scales, None, 128)[0]
+    want = np.concatenate([np.full(32, 0.5), np.full(32, -1.0), [0.25], np.full(31, -0.25),
+                           np.full(31, -2.0), [2.0]]).astype(np.float32)
+    assert np.array_equal(d, want)
+
+
+def test_dequant_group_64_affine_hand_built():
+    """K = 128 in two groups of 64: {0, 1} then {-1.5, fl32(3 - 1.5) = 1.5}."""
+    words = np.array([[0x0000FFFF, 0xFFFF0000, 0x00000000, 0xFFFFFFFF]], dtype=np.uint32)
+    scales = np.array([[1.0, 3.0]], dtype=np.float16)
+    biases = np.array([[0.0, -1.5]], dtype=np.float16)
+    d = O.dequantize_f32(words, scales, biases, 128)[0]
+    want = np.concatenate([np.full(16, 1.0), np.full(32, 0.0), np.full(16, 1.0),
+                           np.full(32, -1.5), np.full(32, 1.5)]).astype(np.float32)
+    assert np.array_equal(d, want)
+
+
+@pytest.mark.parametrize("group", [32, 64])
+@pytest.mark.parametrize("affine", [False, True])
+def test_qmm_brute_force_small_groups(group, affine):
+    K, N, M = 128, 3, 2
+    t = synth.q1_tensor(N, K, seed=71 + group + affine, affine=affine, group=group)
+    x = synth.activations(M, K, seed=72)
+    want = _exact_qmm(x, t.words, t.scales, t.biases, K, group)
+    got = O.qmm(x, t.words, t.scales, t.biases, K)
+    for m in range(M):
+        for n in range(N):
+            assert got[m, n] == pytest.approx(float(want[m][n]), rel=1e-12, abs=1e-12)
+
+
+def test_group_size_from_metadata_shape():
+    assert O.group_size_of(512, np.zeros((2, 16))) == 32
+    assert O.group_size_of(512, np.zeros((2, 8))) == 64
+    assert O.group_size_of(512, np.zeros((2, 4))) == 128
+    with pytest.raises(ValueError):
+        O.group_size_of(512, np.zeros((2, 2)))  # 256 per group
 
 
 # ---------------------------------------------------------------- FFN
