@@ -270,7 +270,7 @@ __device__ __forceinline__ void consumer_sync(int nthreads) {
 // the producer's lanes load them (zero past K) and store them before their
 // arrivals.  Either way a slot's metadata is [16 rows][meta_groups] fp16
 // starting at group 4 (q_lo & ~1).
-template <int NMAT, bool AFFINE, bool FASTMETA, bool GEN>
+template <int NMAT, bool AFFINE, bool FASTMETA, int VAR>
 __global__ void __launch_bounds__(kMaxThreads, 1)
 narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -386,9 +386,10 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
   }
 
   // ================= consumers =================
-  // GEN: bf16 metadata, or fp16/fp32 activations or outputs, read at run time;
-  // otherwise (fp16 metadata, bf16 in and out) those choices are compiled in
-  const int xdt = GEN ? a.xdt : (int)Q1_BF16, ydt = GEN ? a.ydt : (int)Q1_BF16;
+  // VAR 0: fp16 metadata, bf16 in and out, all compiled in; 1: the metadata
+  // type of each matrix read at run time, bf16 in and out; 2: metadata type
+  // and the dtypes of x and y all read at run time
+  const int xdt = VAR == 2 ? a.xdt : (int)Q1_BF16, ydt = VAR == 2 ? a.ydt : (int)Q1_BF16;
   const int qi = warp % QM, ri = warp / QM;
   const bool active = qi < QS;
   const int span = q_lo + qi;  // groups 4 span .. 4 span + 3
@@ -530,7 +531,7 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
         Q1_MMA(1) Q1_MMA(2) Q1_MMA(3) Q1_MMA(4) Q1_MMA(5) Q1_MMA(6) Q1_MMA(7)
 #undef Q1_MMA
         float acc[4];
-        const bool mbf = GEN && ((a.meta_bf16 >> ((NMAT == 2 && ((rb + lt) & 1)) ? 1 : 0)) & 1) != 0;
+        const bool mbf = VAR >= 1 && ((a.meta_bf16 >> ((NMAT == 2 && ((rb + lt) & 1)) ? 1 : 0)) & 1) != 0;
 #pragma unroll
         for (int u = 0; u < kQuad; ++u) {
           const uint32_t hs_a = (u < 2 ? sa.x : sa.y) >> (16 * (u & 1));
@@ -649,7 +650,7 @@ int sm_count_cached() {
   return n;
 }
 
-template <int NMAT, bool AFFINE, bool FASTMETA, bool GEN>
+template <int NMAT, bool AFFINE, bool FASTMETA, int VAR>
 int max_clusters(int ks) {
   static int cache[9] = {0};
   if (cache[ks]) return cache[ks];
@@ -665,7 +666,7 @@ int max_clusters(int ks) {
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, narrow_kernel<NMAT, AFFINE, FASTMETA, GEN>, &cfg) != cudaSuccess || n < 1) {
+  if (cudaOccupancyMaxActiveClusters(&n, narrow_kernel<NMAT, AFFINE, FASTMETA, VAR>, &cfg) != cudaSuccess || n < 1) {
     cudaGetLastError();
     n = sm_count_cached() / ks;
   }
@@ -722,7 +723,7 @@ bool make_meta_map(CUtensorMap *map, const uint16_t *m, int64_t N, int64_t G, in
 // units: its tiles (spans x virtual row tiles of the widest cluster range),
 // about 0.7 tile per warp for the activation fragments, the cluster
 // exchange, and the extra rounds when the partial sums do not fit at once.
-template <int NMAT, bool AFFINE, bool FASTMETA, bool GEN>
+template <int NMAT, bool AFFINE, bool FASTMETA, int VAR>
 bool choose_geo(int64_t N, int K, int M, Geo *out) {
   const int G = K / 128;
   const int QK = (G + kQuad - 1) / kQuad;
@@ -733,7 +734,7 @@ bool choose_geo(int64_t N, int K, int M, Geo *out) {
     if (ks > QK) break;
     const int qm = (QK + ks - 1) / ks;
     if (qm > kMaxWarps) continue;
-    int nclus = max_clusters<NMAT, AFFINE, FASTMETA, GEN>(ks);
+    int nclus = max_clusters<NMAT, AFFINE, FASTMETA, VAR>(ks);
     if (nclus > NT) nclus = NT;
     const int tv = ((NT + nclus - 1) / nclus) * NMAT;  // virtual row tiles of the widest range
     int R = kMaxWarps / qm;
@@ -777,9 +778,9 @@ bool choose_geo(int64_t N, int K, int M, Geo *out) {
   return best >= 0;
 }
 
-template <int NMAT, bool AFFINE, bool FASTMETA, bool GEN>
+template <int NMAT, bool AFFINE, bool FASTMETA, int VAR>
 cudaError_t launch_impl(NarrowArgs args, const uint32_t *w0, const uint32_t *w1, cudaStream_t st, bool pdl) {
-  auto kern = narrow_kernel<NMAT, AFFINE, FASTMETA, GEN>;
+  auto kern = narrow_kernel<NMAT, AFFINE, FASTMETA, VAR>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
@@ -787,7 +788,7 @@ cudaError_t launch_impl(NarrowArgs args, const uint32_t *w0, const uint32_t *w1,
     attr_set = true;
   }
   Geo g;
-  if (!choose_geo<NMAT, AFFINE, FASTMETA, GEN>(args.N, args.K, args.M, &g)) return cudaErrorInvalidConfiguration;
+  if (!choose_geo<NMAT, AFFINE, FASTMETA, VAR>(args.N, args.K, args.M, &g)) return cudaErrorInvalidConfiguration;
   args.geo = g;
   {
     const SmemLayout L0 = smem_layout(g, AFFINE);
@@ -825,7 +826,7 @@ cudaError_t launch_impl(NarrowArgs args, const uint32_t *w0, const uint32_t *w1,
   return cudaLaunchKernelEx(&cfg, kern, maps, args);
 }
 
-template <int NMAT, bool AFFINE, bool GEN>
+template <int NMAT, bool AFFINE, int VAR>
 cudaError_t launch_meta(NarrowArgs args, const uint32_t *w0, const uint32_t *w1, cudaStream_t st, bool pdl) {
   // metadata by TMA needs 16-byte rows (G % 8 == 0) and 16-byte aligned arrays
   bool fast = (args.K / 128) % 8 == 0;
@@ -833,8 +834,8 @@ cudaError_t launch_meta(NarrowArgs args, const uint32_t *w0, const uint32_t *w1,
     fast = fast && (reinterpret_cast<uintptr_t>(args.s[i]) & 15) == 0;
     fast = fast && (reinterpret_cast<uintptr_t>(args.b[i]) & 15) == 0;
   }
-  if (fast) return launch_impl<NMAT, AFFINE, true, GEN>(args, w0, w1, st, pdl);
-  return launch_impl<NMAT, AFFINE, false, GEN>(args, w0, w1, st, pdl);
+  if (fast) return launch_impl<NMAT, AFFINE, true, VAR>(args, w0, w1, st, pdl);
+  return launch_impl<NMAT, AFFINE, false, VAR>(args, w0, w1, st, pdl);
 }
 
 NarrowArgs make_args(const void *x, int64_t M, int64_t N, int64_t K, void *out, q1_dtype xdt, q1_dtype ydt) {
@@ -857,9 +858,11 @@ cudaError_t launch_narrow(const WeightView &W, const void *x, int64_t M, void *y
   a.s[0] = a.s[1] = W.s;
   a.b[0] = a.b[1] = W.b;
   a.meta_bf16 = W.mbf16 ? 3 : 0;
-  if (W.mbf16 || xdt != Q1_BF16 || ydt != Q1_BF16)
-    return W.b ? launch_meta<1, true, true>(a, W.w, W.w, st, pdl) : launch_meta<1, false, true>(a, W.w, W.w, st, pdl);
-  return W.b ? launch_meta<1, true, false>(a, W.w, W.w, st, pdl) : launch_meta<1, false, false>(a, W.w, W.w, st, pdl);
+  if (xdt != Q1_BF16 || ydt != Q1_BF16)
+    return W.b ? launch_meta<1, true, 2>(a, W.w, W.w, st, pdl) : launch_meta<1, false, 2>(a, W.w, W.w, st, pdl);
+  if (W.mbf16)
+    return W.b ? launch_meta<1, true, 1>(a, W.w, W.w, st, pdl) : launch_meta<1, false, 1>(a, W.w, W.w, st, pdl);
+  return W.b ? launch_meta<1, true, 0>(a, W.w, W.w, st, pdl) : launch_meta<1, false, 0>(a, W.w, W.w, st, pdl);
 }
 
 cudaError_t launch_narrow_gate_up(const WeightView &G, const WeightView &U, const void *x,
@@ -872,12 +875,16 @@ cudaError_t launch_narrow_gate_up(const WeightView &G, const WeightView &U, cons
   a.meta_bf16 = (G.mbf16 ? 1 : 0) | (U.mbf16 ? 2 : 0);
   // With mixed metadata the affine variant runs for both matrices; it derives
   // -scale/2 for the one whose biases pointer is null.
-  if (a.meta_bf16 || xdt != Q1_BF16) {
-    if (G.b || U.b) return launch_meta<2, true, true>(a, G.w, U.w, st, pdl);
-    return launch_meta<2, false, true>(a, G.w, U.w, st, pdl);
+  if (xdt != Q1_BF16) {
+    if (G.b || U.b) return launch_meta<2, true, 2>(a, G.w, U.w, st, pdl);
+    return launch_meta<2, false, 2>(a, G.w, U.w, st, pdl);
   }
-  if (G.b || U.b) return launch_meta<2, true, false>(a, G.w, U.w, st, pdl);
-  return launch_meta<2, false, false>(a, G.w, U.w, st, pdl);
+  if (a.meta_bf16) {
+    if (G.b || U.b) return launch_meta<2, true, 1>(a, G.w, U.w, st, pdl);
+    return launch_meta<2, false, 1>(a, G.w, U.w, st, pdl);
+  }
+  if (G.b || U.b) return launch_meta<2, true, 0>(a, G.w, U.w, st, pdl);
+  return launch_meta<2, false, 0>(a, G.w, U.w, st, pdl);
 }
 
 unsigned int read_and_clear_narrow_errors(cudaStream_t st, cudaError_t *err) {
