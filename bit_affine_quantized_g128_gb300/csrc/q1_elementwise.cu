@@ -17,14 +17,15 @@ namespace q1 {
 namespace {
 
 int sm_count() {
-  static int cached = 0;
-  if (cached == 0) {
-    int dev = 0, n = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    cached = n > 0 ? n : 148;
-  }
-  return cached;
+  static std::atomic<int> cached[kMaxDevices];
+  const int dev = current_device();
+  if (dev < kMaxDevices && cached[dev].load(std::memory_order_relaxed) > 0)
+    return cached[dev].load(std::memory_order_relaxed);
+  int n = 0;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (n <= 0) n = 148;
+  if (dev < kMaxDevices) cached[dev].store(n, std::memory_order_relaxed);
+  return n;
 }
 
 unsigned grid_for(int64_t items, int threads) {

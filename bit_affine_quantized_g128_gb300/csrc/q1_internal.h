@@ -6,9 +6,29 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "q1.h"
 
 namespace q1 {
+
+// One-time host state is kept per device: a process may drive several GPUs,
+// and function attributes, SM counts and occupancy are per device.  Devices
+// beyond kMaxDevices are served without caching.
+constexpr int kMaxDevices = 64;
+inline int current_device() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0) d = 0;
+  return d;
+}
+// True once per (flag, device): the caller then does the one-time work and,
+// if it succeeded, calls mark_done.  Concurrent first calls may both do it.
+inline bool not_done(const std::atomic<uint64_t> &flag, int dev) {
+  return dev >= kMaxDevices || !(flag.load(std::memory_order_relaxed) & (1ull << dev));
+}
+inline void mark_done(std::atomic<uint64_t> &flag, int dev) {
+  if (dev < kMaxDevices) flag.fetch_or(1ull << dev, std::memory_order_relaxed);
+}
 
 constexpr int kGroup = 128;      // weights per scale/bias group
 constexpr int kWordBits = 32;    // weights per packed word

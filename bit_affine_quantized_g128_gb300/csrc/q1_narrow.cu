@@ -640,20 +640,23 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
 // host: geometry
 // ---------------------------------------------------------------------------
 int sm_count_cached() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
+  static std::atomic<int> cached[kMaxDevices];
+  const int dev = current_device();
+  if (dev < kMaxDevices && cached[dev].load(std::memory_order_relaxed) > 0)
+    return cached[dev].load(std::memory_order_relaxed);
+  int n = 0;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (n <= 0) n = 148;
+  if (dev < kMaxDevices) cached[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
 template <int NMAT, bool AFFINE, bool FASTMETA, int VAR>
 int max_clusters(int ks) {
-  static int cache[9] = {0};
-  if (cache[ks]) return cache[ks];
+  static std::atomic<int> cache[kMaxDevices][9];
+  const int dev = current_device();
+  if (dev < kMaxDevices && cache[dev][ks].load(std::memory_order_relaxed) > 0)
+    return cache[dev][ks].load(std::memory_order_relaxed);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(ks * 64), 1, 1);
   cfg.blockDim = dim3(kMaxThreads, 1, 1);
@@ -671,7 +674,7 @@ int max_clusters(int ks) {
     n = sm_count_cached() / ks;
   }
   if (n < 1) n = 1;
-  cache[ks] = n;
+  if (dev < kMaxDevices) cache[dev][ks].store(n, std::memory_order_relaxed);
   return n;
 }
 
@@ -781,11 +784,12 @@ bool choose_geo(int64_t N, int K, int M, Geo *out) {
 template <int NMAT, bool AFFINE, bool FASTMETA, int VAR>
 cudaError_t launch_impl(NarrowArgs args, const uint32_t *w0, const uint32_t *w1, cudaStream_t st, bool pdl) {
   auto kern = narrow_kernel<NMAT, AFFINE, FASTMETA, VAR>;
-  static bool attr_set = false;
-  if (!attr_set) {
+  static std::atomic<uint64_t> attr_set{0};
+  const int dev = current_device();
+  if (not_done(attr_set, dev)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    mark_done(attr_set, dev);
   }
   Geo g;
   if (!choose_geo<NMAT, AFFINE, FASTMETA, VAR>(args.N, args.K, args.M, &g)) return cudaErrorInvalidConfiguration;

@@ -660,12 +660,13 @@ cudaError_t launch_wide_mma_g(const WeightView &W, const __half *x16, int64_t M,
                       estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  static bool attr = false;
-  if (!attr) {
+  static std::atomic<uint64_t> attr{0};
+  const int dev = current_device();
+  if (not_done(attr, dev)) {
     cudaError_t e = cudaFuncSetAttribute(wide_kernel<MT, SPLIT, G128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes<MT>);
     if (e != cudaSuccess) return e;
-    attr = true;
+    mark_done(attr, dev);
   }
   const unsigned ntn = (unsigned)((W.N + BN - 1) / BN);
   cudaLaunchConfig_t cfg = {};
@@ -697,9 +698,11 @@ cudaError_t launch_wide_mma(const WeightView &W, const __half *x16, int64_t M, c
 
 // Clusters of `ks` split-K CTAs that can be resident at once (one per SM).
 int wide_split_clusters(int ks) {
-  static int cache[9] = {0};
+  static std::atomic<int> cache[kMaxDevices][9];
   if (ks < 2 || ks > 8) return 0;
-  if (cache[ks]) return cache[ks];
+  const int dev = current_device();
+  if (dev < kMaxDevices && cache[dev][ks].load(std::memory_order_relaxed) > 0)
+    return cache[dev][ks].load(std::memory_order_relaxed);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(ks * 32), 1, 1);
   cfg.blockDim = dim3(kThreadsWide, 1, 1);
@@ -717,7 +720,7 @@ int wide_split_clusters(int ks) {
     cudaGetLastError();
     n = 0;
   }
-  cache[ks] = n;
+  if (dev < kMaxDevices && n > 0) cache[dev][ks].store(n, std::memory_order_relaxed);
   return n;
 }
 
