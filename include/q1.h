@@ -8,6 +8,7 @@
  *   w       uint32 [N][K/32]  weight (n, k) is bit (k % 32) of word [n][k / 32]
  *   scales  fp16   [N][K/128] one per row and group of 128 along K
  *   biases  fp16   [N][K/128] or NULL
+ *   (bf16 metadata and group sizes 32 / 64 are variants: see q1_weight)
  * Value ("Support Bonsai-27B affine Q1", higgs PR #212, section "What"):
  *   w(n,k) = scale * q + bias, q in {0,1}.  With biases == NULL the tensor is
  *   symmetric: bias = -scale/2, derived in fp32 and never stored.  So bit 0
@@ -30,9 +31,10 @@
  *     activation); the prefill path scales them into fp16 rows (exact for bf16
  *     and fp16 activations, one rounding at 2^-11 for fp32).  Accumulation is
  *     fp32 and the output is rounded once to the dtype.
- *   - Calls that need scratch (q1_qmm on its prefill path, q1_ffn_fused for
- *     its intermediate activations) take a caller-owned device workspace and
- *     its size; q1_qmm_workspace_size / q1_ffn_workspace_size return the
+ *   - Calls that need scratch (q1_qmm on its prefill path, q1_ffn_fused and
+ *     q1_decode_chain for their intermediate activations) take a caller-owned
+ *     device workspace and its size; q1_qmm_workspace_size,
+ *     q1_ffn_workspace_size and q1_decode_chain_workspace_size return the
  *     bytes needed.  A workspace must be 256-byte aligned and must not be used
  *     by another call that may run concurrently.
  *   - Device-side waits in the kernels are bounded; one that runs out sets a
