@@ -436,6 +436,21 @@ def test_fp16_fp32_activations(q1, dtype, affine, M):
         assert torch.equal(yv.reshape(1, N), y)
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])
+@pytest.mark.parametrize("M", [9, 300])
+def test_prefill_ragged_rows_every_output_dtype(q1, dtype, M):
+    # N % 8 != 0: the epilogues' element-wise tails (split-K clusters for M = 9,
+    # whole tiles for M = 300) in every output dtype
+    N, K = 601, 768
+    t = synth.q1_tensor(N, K, seed=691, affine=True)
+    x = _acts(M, K, 692 + M, dtype)
+    W = q1.Q1Weight.from_host(t)
+    y = q1.qmm(W, x.to(DEV))
+    assert y.dtype == dtype
+    check_matmul(y, O.qmm(x, t.words, t.scales, t.biases, K), x,
+                 O.dequantize_f32(t.words, t.scales, t.biases, K), f"prefill N={N} M={M} {dtype}")
+
+
 @pytest.mark.parametrize("dtype", [torch.float16, torch.float32])
 def test_ffn_fp16_fp32_activations(q1, dtype):
     M, D, F = 3, 512, 1408
