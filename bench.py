@@ -37,6 +37,7 @@ if ROOT not in sys.path:
 
 LAYERS = 64
 D_MODEL, D_FF = 5120, 17408
+VOCAB = 152064  # 27B-class vocabulary: embedding table and tied head [VOCAB x D_MODEL]
 SHAPES = (("gate", D_FF, D_MODEL), ("up", D_FF, D_MODEL), ("down", D_MODEL, D_FF),
           ("attn", D_MODEL, D_MODEL))
 WORKLOAD = "q1 decode QMV M=1, 64 layers x {gate,up 17408x5120; down 5120x17408; attn 5120x5120}, symmetric g128"
@@ -236,6 +237,62 @@ def run_timed(torch, graph, steps, stream, dist=None):
     if dist is not None:
         dist.barrier()
     return e0.elapsed_time(e1) / 1e3  # seconds
+
+
+def graph_time(torch, fns, stream, per=10, reps=5):
+    """Seconds per call: `per` calls (cycling over `fns`) captured in one CUDA
+    graph, replayed `reps` times after 3 warm-up replays."""
+    gm = time_graph(torch, lambda: [fns[i % len(fns)]() for i in range(per)], 3, 3, stream)
+    t = run_timed(torch, gm, reps, stream) / (reps * per)
+    del gm
+    return t
+
+
+def elementwise_and_head(q1, synth, torch, device, stream):
+    """GB/s of algorithmic bytes for the tied head (QMV over the vocabulary),
+    dequantize, pack, unpack and the symmetric check, and the time of a 64-id
+    embedding gather.  Inputs rotate over more than the 129 MB L2 where the
+    work is a stream."""
+    out = {}
+    G = D_MODEL // 128
+    # tied head: two vocabulary matrices in turn (2 x 109.5 MB)
+    heads = [q1.Q1Weight(synth.device_weight_words(VOCAB, D_MODEL, 4400 + i, device),
+                         synth.device_scales(VOCAB, D_MODEL, 4410 + i, device), None, D_MODEL) for i in range(2)]
+    xh = torch.randn(D_MODEL, device=device).to(torch.bfloat16)
+    yh = torch.empty(VOCAB, dtype=torch.bfloat16, device=device)
+    t = graph_time(torch, [lambda W=W: q1.qmv(W, xh, out=yh) for W in heads], stream)
+    out["tied_head_152064x5120_GBps"] = round((weight_bytes(VOCAB, D_MODEL, False) + D_MODEL * 2 + VOCAB * 2) / t / 1e9, 1)
+    # embedding gather: 64 ids into the table (latency-bound: 46 KB read, 655 KB written)
+    ids = torch.randint(0, VOCAB, (64,), device=device, dtype=torch.int32)
+    t = graph_time(torch, [lambda: q1.embed_gather(heads[0], ids)], stream)
+    out["embed_gather_T64_us"] = round(t * 1e6, 2)
+    out["embed_gather_T64_GBps"] = round(64 * (D_MODEL // 8 + G * 2 + D_MODEL * 2) / t / 1e9, 1)
+    # dequantize a 17408 x 5120 projection to bf16 (178 MB written)
+    W1 = q1.Q1Weight(synth.device_weight_words(D_FF, D_MODEL, 4420, device),
+                     synth.device_scales(D_FF, D_MODEL, 4421, device), None, D_MODEL)
+    t = graph_time(torch, [lambda: q1.dequantize(W1, torch.bfloat16)], stream)
+    out["dequantize_bf16_17408x5120_GBps"] = round((weight_bytes(D_FF, D_MODEL, False) + D_FF * D_MODEL * 2) / t / 1e9, 1)
+    # unpack / pack of two stacked projections (2 x 17408 rows: 178 MB of bits)
+    words = torch.cat([W1.words, heads[1].words[:D_FF]])
+    bits = q1.unpack(words, D_MODEL)
+    nbytes = words.numel() * 4 + bits.numel()
+    t = graph_time(torch, [lambda: q1.unpack(words, D_MODEL)], stream)
+    out["unpack_34816x5120_GBps"] = round(nbytes / t / 1e9, 1)
+    t = graph_time(torch, [lambda: q1.pack(bits)], stream)
+    out["pack_34816x5120_GBps"] = round(nbytes / t / 1e9, 1)
+    del bits, words, W1
+    # symmetric check of stored biases: six vocabulary-sized metadata sets in
+    # turn (6 x 24 MB of scales and biases)
+    metas = []
+    for i in range(6):
+        # scales >= 2^-13 so that -scale/2 is a normal fp16 value (exact)
+        sc = synth.device_scales(VOCAB, D_MODEL, 4430 + i, device).clamp(min=2.0 ** -13)
+        metas.append(q1.Q1Weight(heads[0].words, sc, (sc.float() * -0.5).to(torch.float16), D_MODEL))
+    t = graph_time(torch, [lambda W=W: q1.check_symmetric(W) for W in metas], stream, per=12)
+    out["check_symmetric_152064x5120_GBps"] = round(VOCAB * G * 4 / t / 1e9, 1)
+    assert all(int(q1.check_symmetric(W).item()) == 1 for W in metas)
+    del metas, heads
+    return out
 
 
 def time_prefill(q1, synth, torch, device, M, shape, affine, reps=20):
@@ -448,7 +505,9 @@ def gpu_arm(args):
         del gm
         rp_bytes = D_FF * D_MODEL * 2 + weight_bytes(D_FF, D_MODEL, False)
         sub["repack_bf16_17408x5120_GBps"] = round(rp_bytes / t_rp / 1e9, 1)
-        del W0, dense
+        del W0, dense, Wr
+        torch.cuda.empty_cache()
+        sub.update(elementwise_and_head(q1, synth, torch, device, stream))
         torch.cuda.empty_cache()
         # prefill on the tensor cores
         for M in (128, 2048):

@@ -183,17 +183,33 @@ __global__ void gather_kernel(const uint32_t *__restrict__ w, const uint16_t *__
 
 __global__ void set_flag_kernel(int32_t *flag, int32_t v) { *flag = v; }
 
+// exact fp32 equality of a stored bias with -scale/2: +0 == -0, NaN != anything
+__device__ __forceinline__ bool sym_pair(uint32_t sh, uint32_t bh, bool mbf16) {
+  return meta_f32(bh, mbf16) == __fmul_rn(-0.5f, meta_f32(sh, mbf16));
+}
+
+// Eight groups per thread with 16-byte loads when both arrays are 16-byte
+// aligned (vec), one group per thread otherwise.
 __global__ void check_symmetric_kernel(const uint16_t *__restrict__ s,
                                        const uint16_t *__restrict__ b, int64_t count, bool mbf16,
-                                       int32_t *__restrict__ result) {
+                                       bool vec, int32_t *__restrict__ result) {
   bool mismatch = false;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < count;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    float sc = meta_f32(s[i], mbf16);
-    float bi = meta_f32(b[i], mbf16);
-    // exact fp32 equality: +0 == -0, NaN != anything
-    if (!(bi == __fmul_rn(-0.5f, sc))) mismatch = true;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  int64_t done = 0;
+  if (vec) {
+    const int64_t n8 = count / 8;
+    const uint4 *s8 = reinterpret_cast<const uint4 *>(s), *b8 = reinterpret_cast<const uint4 *>(b);
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8; i += stride) {
+      const uint4 sv = __ldg(s8 + i), bv = __ldg(b8 + i);
+      const uint32_t sw[4] = {sv.x, sv.y, sv.z, sv.w}, bw[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (!sym_pair(sw[q], bw[q], mbf16) || !sym_pair(sw[q] >> 16, bw[q] >> 16, mbf16)) mismatch = true;
+    }
+    done = n8 * 8;
   }
+  for (int64_t i = done + blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < count; i += stride)
+    if (!sym_pair(s[i], b[i], mbf16)) mismatch = true;
   if (__syncthreads_or(mismatch) && threadIdx.x == 0) *result = 0;
 }
 
@@ -429,7 +445,9 @@ cudaError_t launch_check_symmetric(const WeightView &W, int32_t *result, cudaStr
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   int64_t count = W.N * ((W.K / 32) >> W.gshift);
-  check_symmetric_kernel<<<grid_for(count, 256), 256, 0, st>>>(W.s, W.b, count, W.mbf16, result);
+  const bool vec = (reinterpret_cast<uintptr_t>(W.s) & 15) == 0 && (reinterpret_cast<uintptr_t>(W.b) & 15) == 0;
+  check_symmetric_kernel<<<grid_for(vec ? count / 8 + 1 : count, 256), 256, 0, st>>>(W.s, W.b, count, W.mbf16, vec,
+                                                                                   result);
   return cudaGetLastError();
 }
 

@@ -645,5 +645,26 @@ def test_check_symmetric(q1):
     assert int(q1.check_symmetric(W2).item()) == 0 == int(O.is_symmetric(s, b2))
 
 
+def test_check_symmetric_tail_and_unaligned_metadata(q1):
+    # 3 x 3 groups: one 8-group vector and a scalar tail; then the same
+    # metadata 2 bytes past a 16-byte boundary (the element-wise path)
+    N, K = 3, 384
+    t = synth.q1_tensor(N, K, seed=701, affine=False)
+    s = np.maximum(t.scales, np.float16(2.0 ** -13))
+    b = (-(s.astype(np.float32) / 2)).astype(np.float16)
+    for bad in (None, (2, 2), (0, 1)):  # (2, 2) is the tail element
+        b2 = b.copy()
+        if bad:
+            b2[bad] = np.float16(0.5)
+        W = q1.Q1Weight.from_host(synth.Q1Tensor(t.words, s, b2, K))
+        want = int(O.is_symmetric(s, b2))
+        assert int(q1.check_symmetric(W).item()) == want == (0 if bad else 1)
+        sd = torch.from_numpy(np.concatenate([[np.float16(1)], s.reshape(-1)])).to(DEV)[1:].reshape(N, 3)
+        bd = torch.from_numpy(np.concatenate([[np.float16(1)], b2.reshape(-1)])).to(DEV)[1:].reshape(N, 3)
+        Wu = q1.Q1Weight(W.words, sd, bd, K)
+        assert Wu.scales.data_ptr() % 16 != 0
+        assert int(q1.check_symmetric(Wu).item()) == want
+
+
 def test_no_device_errors_after_suite(q1):
     assert q1.device_errors() == 0
