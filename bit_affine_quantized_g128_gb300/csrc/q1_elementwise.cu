@@ -64,23 +64,31 @@ __global__ void pack_kernel(const uint8_t *__restrict__ bits, uint32_t *__restri
   }
 }
 
+// The warp's 32 consecutive words: a lane's own word is word `lane` of the
+// run starting at the warp's base.  The outputs of the run are contiguous, and
+// every store instruction of the emitters below writes one contiguous 512
+// bytes: store j puts chunk 32 j + lane (16 bytes) of the run, taking the word
+// (and its values) from the lane that owns it.
+constexpr unsigned kFull = 0xFFFFFFFFu;
+
 __global__ void unpack_kernel(const uint32_t *__restrict__ w, uint8_t *__restrict__ bits,
                               int64_t nwords) {
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nwords;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    uint32_t v = w[i];
-    uint4 a, b;
-    a.x = nibble_to_bytes(v);
-    a.y = nibble_to_bytes(v >> 4);
-    a.z = nibble_to_bytes(v >> 8);
-    a.w = nibble_to_bytes(v >> 12);
-    b.x = nibble_to_bytes(v >> 16);
-    b.y = nibble_to_bytes(v >> 20);
-    b.z = nibble_to_bytes(v >> 24);
-    b.w = nibble_to_bytes(v >> 28);
-    uint4 *dst = reinterpret_cast<uint4 *>(bits + i * 32);
-    dst[0] = a;
-    dst[1] = b;
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarp = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t base = (((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * 32; base < nwords;
+       base += nwarp * 32) {
+    const bool valid = base + lane < nwords;
+    const uint32_t v = valid ? w[base + lane] : 0u;
+    const unsigned vmask = __ballot_sync(kFull, valid);
+    uint4 *dst = reinterpret_cast<uint4 *>(bits + base * 32);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {  // 32 bytes per word: 2 chunks of 16 bits
+      const int c = 32 * j + lane, src = c >> 1;
+      const uint32_t x = __shfl_sync(kFull, v, src) >> (16 * (c & 1));
+      if ((vmask >> src) & 1u)
+        dst[c] = make_uint4(nibble_to_bytes(x), nibble_to_bytes(x >> 4), nibble_to_bytes(x >> 8),
+                            nibble_to_bytes(x >> 12));
+    }
   }
 }
 
@@ -95,49 +103,36 @@ __device__ __forceinline__ void group_values(const uint16_t *__restrict__ s,
   hi = __fadd_rn(sc, bi);
 }
 
-// 32 outputs of one word, as 16-bit patterns lo16 / hi16 selected by the bits.
-__device__ __forceinline__ void store_word_16(uint16_t lo16, uint16_t hi16, uint32_t word,
-                                              uint4 *dst) {
-  uint32_t out[16];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    uint32_t a = (word >> (2 * j)) & 1u ? hi16 : lo16;
-    uint32_t c = (word >> (2 * j + 1)) & 1u ? hi16 : lo16;
-    out[j] = a | (c << 16);
-  }
-#pragma unroll
-  for (int j = 0; j < 4; ++j) dst[j] = make_uint4(out[4 * j], out[4 * j + 1], out[4 * j + 2], out[4 * j + 3]);
-}
-
-__device__ __forceinline__ void store_word_f32(float lo, float hi, uint32_t word, uint4 *dst) {
-  uint32_t lo32 = __float_as_uint(lo), hi32 = __float_as_uint(hi);
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    uint4 v;
-    v.x = (word >> (4 * j + 0)) & 1u ? hi32 : lo32;
-    v.y = (word >> (4 * j + 1)) & 1u ? hi32 : lo32;
-    v.z = (word >> (4 * j + 2)) & 1u ? hi32 : lo32;
-    v.w = (word >> (4 * j + 3)) & 1u ? hi32 : lo32;
-    dst[j] = v;
-  }
-}
-
+// Output bit patterns of the dequantized pair (lo, hi) in the output dtype.
 template <int OUT>  // 0 = bf16, 1 = f16, 2 = f32
-__device__ __forceinline__ void emit_word(float lo, float hi, uint32_t word, void *out_row,
-                                          int64_t c) {
-  if (OUT == 2) {
-    store_word_f32(lo, hi, word, reinterpret_cast<uint4 *>(static_cast<float *>(out_row) + c * 32));
-  } else {
-    uint16_t l16, h16;
-    if (OUT == 0) {
-      l16 = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
-      h16 = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
-    } else {
-      l16 = __half_as_ushort(__float2half_rn(lo));
-      h16 = __half_as_ushort(__float2half_rn(hi));
+__device__ __forceinline__ uint32_t out_bits(float v) {
+  if (OUT == 2) return __float_as_uint(v);
+  if (OUT == 0) return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  return __half_as_ushort(__float2half_rn(v));
+}
+
+// The warp's run of 32 words (lane: word `wd`, its values' patterns lo/hi,
+// `valid` if inside the tensor) -> 32 x 32 outputs at `dst`, as contiguous
+// 512-byte stores (see unpack_kernel).
+template <int OUT>
+__device__ __forceinline__ void warp_emit(uint32_t wd, uint32_t lo, uint32_t hi, bool valid, uint4 *dst) {
+  constexpr int CPW = OUT == 2 ? 8 : 4;  // 16-byte chunks per word
+  constexpr int VPC = 32 / CPW;          // values per chunk
+  const int lane = threadIdx.x & 31;
+  const unsigned vmask = __ballot_sync(kFull, valid);
+#pragma unroll
+  for (int j = 0; j < CPW; ++j) {
+    const int c = 32 * j + lane, src = c / CPW;
+    const uint32_t x = __shfl_sync(kFull, wd, src) >> (VPC * (c % CPW));
+    const uint32_t l = __shfl_sync(kFull, lo, src), h = __shfl_sync(kFull, hi, src);
+    if (!((vmask >> src) & 1u)) continue;
+    uint32_t q[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (OUT == 2) q[e] = (x >> e) & 1u ? h : l;
+      else q[e] = ((x >> (2 * e)) & 1u ? h : l) | (((x >> (2 * e + 1)) & 1u ? h : l) << 16);
     }
-    store_word_16(l16, h16, word,
-                  reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out_row) + c * 32));
+    dst[c] = make_uint4(q[0], q[1], q[2], q[3]);
   }
 }
 
@@ -147,12 +142,23 @@ __global__ void dequantize_kernel(const uint32_t *__restrict__ w, const uint16_t
                                   int gshift, void *__restrict__ out) {
   const int64_t wpr = K / 32, G = wpr >> gshift, nwords = N * wpr;  // G: metadata groups per row
   const int esz = OUT == 2 ? 4 : 2;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nwords;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    int64_t n = i / wpr, c = i - n * wpr;
-    float lo, hi;
-    group_values(s, b, n * G + (c >> gshift), mbf16, lo, hi);
-    emit_word<OUT>(lo, hi, w[i], static_cast<char *>(out) + n * K * esz, c);
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarp = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t base = (((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * 32; base < nwords;
+       base += nwarp * 32) {
+    const int64_t i = base + lane;
+    const bool valid = i < nwords;
+    uint32_t wd = 0u, lo = 0u, hi = 0u;
+    if (valid) {
+      const int64_t n = i / wpr, c = i - n * wpr;
+      float lf, hf;
+      group_values(s, b, n * G + (c >> gshift), mbf16, lf, hf);
+      wd = w[i];
+      lo = out_bits<OUT>(lf);
+      hi = out_bits<OUT>(hf);
+    }
+    // word i's 32 outputs start at element 32 i ([N][K] row-major, K = 32 wpr)
+    warp_emit<OUT>(wd, lo, hi, valid, reinterpret_cast<uint4 *>(static_cast<char *>(out) + base * 32 * esz));
   }
 }
 
@@ -163,21 +169,28 @@ __global__ void gather_kernel(const uint32_t *__restrict__ w, const uint16_t *__
                               void *__restrict__ out, int32_t *__restrict__ bad) {
   const int64_t wpr = K / 32, G = wpr >> gshift, nwords = T * wpr;
   const int esz = OUT == 2 ? 4 : 2;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nwords;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    int64_t t = i / wpr, c = i - t * wpr;
-    int64_t row = ids[t];
-    char *out_row = static_cast<char *>(out) + t * K * esz;
-    if (row < 0 || row >= V) {
-      uint4 *dst = reinterpret_cast<uint4 *>(out_row + c * 32 * esz);
-      const int n16 = 32 * esz / 16;
-      for (int j = 0; j < n16; ++j) dst[j] = make_uint4(0, 0, 0, 0);
-      if (c == 0 && bad) atomicAdd(bad, 1);
-      continue;
+  const int lane = threadIdx.x & 31;
+  const int64_t nwarp = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t base = (((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * 32; base < nwords;
+       base += nwarp * 32) {
+    const int64_t i = base + lane;
+    const bool valid = i < nwords;
+    uint32_t wd = 0u, lo = 0u, hi = 0u;  // an out-of-range id gives a zero row
+    if (valid) {
+      const int64_t t = i / wpr, c = i - t * wpr;
+      const int64_t row = ids[t];
+      if (row < 0 || row >= V) {
+        if (c == 0 && bad) atomicAdd(bad, 1);
+      } else {
+        float lf, hf;
+        group_values(s, b, row * G + (c >> gshift), mbf16, lf, hf);
+        wd = w[row * wpr + c];
+        lo = out_bits<OUT>(lf);
+        hi = out_bits<OUT>(hf);
+      }
     }
-    float lo, hi;
-    group_values(s, b, row * G + (c >> gshift), mbf16, lo, hi);
-    emit_word<OUT>(lo, hi, w[row * wpr + c], out_row, c);
+    // output word i (row t, word c) starts at element t K + 32 c = 32 i
+    warp_emit<OUT>(wd, lo, hi, valid, reinterpret_cast<uint4 *>(static_cast<char *>(out) + base * 32 * esz));
   }
 }
 
@@ -407,7 +420,7 @@ cudaError_t launch_pack(const uint8_t *bits, int64_t N, int64_t K, uint32_t *w, 
 cudaError_t launch_unpack(const uint32_t *w, int64_t N, int64_t K, uint8_t *bits,
                           cudaStream_t st) {
   int64_t nwords = N * (K / 32);
-  unpack_kernel<<<grid_for(nwords, 256), 256, 0, st>>>(w, bits, nwords);
+  unpack_kernel<<<grid_for((nwords + 31) / 32 * 32, 256), 256, 0, st>>>(w, bits, nwords);
   return cudaGetLastError();
 }
 
