@@ -242,11 +242,15 @@ struct NarrowArgs {
   // tile loop reads them as constants
   int slot_words, slot_meta, part_tile;
   int meta_bf16;  // bit m: matrix m's scales/biases are bf16 (else fp16)
+  int w3;         // the w3 maps are set: one TMA per slot for the words
 };
 
 // Tensor maps of the (up to two) matrices: packed words, scales, biases.
+// w3[m][v]: the same words as a 3-D tensor (16 words of a span, rows, spans),
+// so that one box of 16 rows x (qm - v) spans fills a whole ring slot.
 struct Maps {
   CUtensorMap w[2], s[2], b[2];
+  CUtensorMap w3[2][2];
 };
 
 __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint32_t bar) {
@@ -340,7 +344,18 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb), "r"(bytes) : "memory");
         const CUtensorMap *wm = mat ? &maps.w[1] : &maps.w[0];
         const uint32_t wdst = ring_s + slot * L.slot_words;
-        for (int qs = 0; qs < QS; ++qs) tma_2d(wdst + qs * kTileBytes, wm, (q_lo + qs) * 16, rt * 16, fb);
+        if (a.w3) {
+          // one box: 16 words x 16 rows x QS spans, laid out span by span as
+          // the per-span boxes would be
+          const CUtensorMap *wm3 = &maps.w3[mat][QS == QM ? 0 : 1];
+          asm volatile(
+              "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+              "[%5];" ::"r"(wdst),
+              "l"(wm3), "r"(0), "r"(rt * 16), "r"(q_lo), "r"(fb)
+              : "memory");
+        } else {
+          for (int qs = 0; qs < QS; ++qs) tma_2d(wdst + qs * kTileBytes, wm, (q_lo + qs) * 16, rt * 16, fb);
+        }
         if (FASTMETA) {
           tma_2d(mdst, mat ? &maps.s[1] : &maps.s[0], q_base * kQuad, rt * 16, fb);
           if (has_b) tma_2d(mdst + 16 * MROW, mat ? &maps.b[1] : &maps.b[0], q_base * kQuad, rt * 16, fb);
@@ -706,6 +721,24 @@ bool make_word_map(CUtensorMap *map, const uint32_t *w, int64_t N, int64_t K) {
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Packed words [N][K/32] as a 3-D uint32 tensor (16 words of a span, rows,
+// spans), boxes of 16 words x 16 rows x `spans` spans with the 64-byte
+// swizzle: the smem image of one box is the per-span boxes of make_word_map
+// back to back.  Only for K % 512 == 0, where every span is whole and the
+// three dimensions tile each row exactly (nothing outside the array is ever
+// addressed); rows >= N read as zero.
+bool make_word_map3(CUtensorMap *map, const uint32_t *w, int64_t N, int64_t K, int spans) {
+  auto encode = encode_fn();
+  if (!encode || K % 512 != 0 || spans < 1) return false;
+  cuuint64_t gdim[3] = {16, (cuuint64_t)N, (cuuint64_t)(K / 512)};
+  cuuint64_t gstride[2] = {(cuuint64_t)(K / 32) * 4, 64};
+  cuuint32_t box[3] = {16, 16, (cuuint32_t)spans};
+  cuuint32_t estride[3] = {1, 1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint32_t *>(w), gdim, gstride, box, estride,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Scales or biases [N][G] fp16 as a 2-D uint16 tensor; boxes of box_groups
 // (a multiple of 8) groups x 16 rows, no swizzle; rows >= N and groups >= G
 // read as zero.  Needs G % 8 == 0 (16-byte rows) and a 16-byte aligned base.
@@ -804,6 +837,11 @@ cudaError_t launch_impl(NarrowArgs args, const uint32_t *w0, const uint32_t *w1,
   memset(&maps, 0, sizeof(maps));
   if (!make_word_map(&maps.w[0], w0, args.N, args.K)) return cudaErrorInvalidValue;
   if (!make_word_map(&maps.w[1], w1, args.N, args.K)) return cudaErrorInvalidValue;
+  // one TMA per slot when every span is whole; a CTA holds qm or qm - 1 spans
+  args.w3 = args.K % 512 == 0;
+  for (int m = 0; m < 2 && args.w3; ++m)
+    for (int v = 0; v < 2 && args.w3; ++v)
+      if (g.qm - v >= 1 && !make_word_map3(&maps.w3[m][v], m ? w1 : w0, args.N, args.K, g.qm - v)) args.w3 = 0;
   if (FASTMETA) {
     const int64_t G = args.K / 128;
     for (int i = 0; i < 2; ++i) {
