@@ -42,11 +42,12 @@
 //   * the clusters split the 16-row tiles of W into contiguous ranges; the
 //     R warps that own the same span take every R-th row tile of the range;
 //   * the producer warp streams the CTA's row tiles, in order, through a
-//     ring of row-tile slots: per slot one 1 KB TMA box per span (16 rows x
-//     16 words, 64-byte swizzle: conflict-free reads) and one box with the
-//     16 rows' scales (and biases) of the whole K-slice, all completing on
-//     the slot's mbarrier; the consumers hand the slot back through a second
-//     mbarrier;
+//     ring of row-tile slots: per slot the words as 1 KB per span (16 rows x
+//     16 words, 64-byte swizzle: conflict-free reads), one 3-D TMA box for
+//     all the CTA's spans when K % 512 == 0 (else one 2-D box per span), and
+//     one box with the 16 rows' scales (and biases) of the whole K-slice, all
+//     completing on the slot's mbarrier; the consumers hand the slot back
+//     through a second mbarrier;
 //   * the four groups' MMA chains of a tile are interleaved, so that a warp
 //     always has four independent MMAs in flight;
 //   * per-tile partial sums go to shared memory and are combined over the
@@ -265,7 +266,7 @@ __device__ __forceinline__ void consumer_sync(int nthreads) {
 
 // One CTA: NC = qm * R consumer warps and one producer warp (the last).
 // The producer streams the CTA's row tiles in order through a ring of
-// row-tile slots: per slot one 1 KB TMA box per span of the CTA (16 rows x
+// row-tile slots: per slot 1 KB of words per span of the CTA (16 rows x
 // 16 words, 64-byte swizzle) and the rows' metadata.  Consumer warp
 // (qi, ri) owns span q_lo + qi and takes the row tiles ri, ri + R, ... of
 // each round.
