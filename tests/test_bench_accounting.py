@@ -1,0 +1,35 @@
+"""The benchmark's algorithmic byte counts (the denominators of its GB/s
+figures), checked against per-matrix counts derived by hand from the packed
+format: N*K/8 bytes of words, N*(K/128)*2 bytes per fp16 metadata array, and
+the bf16 activations in and out once.  CPU only."""
+import bench
+
+
+def test_weight_bytes_per_matrix():
+    # 17408 x 5120: 11,141,120 B of words + 1,392,640 B of scales (+ the same of biases)
+    assert bench.weight_bytes(17408, 5120, False) == 11_141_120 + 1_392_640
+    assert bench.weight_bytes(17408, 5120, True) == 11_141_120 + 2 * 1_392_640
+    # 5120 x 5120: 3,276,800 B of words + 409,600 B of scales
+    assert bench.weight_bytes(5120, 5120, False) == 3_686_400
+
+
+def test_decode_step_bytes():
+    # per layer, x [K] in and y [N] out in bf16 for each of the four matrices
+    gate = 12_533_760 + 5120 * 2 + 17408 * 2    # 12,578,816
+    down = 12_533_760 + 17408 * 2 + 5120 * 2
+    attn = 3_686_400 + 5120 * 2 + 5120 * 2      # 3,706,880
+    assert gate == 12_578_816 and attn == 3_706_880
+    assert bench.step_bytes(1) == 64 * (2 * gate + down + attn)
+    # M tokens move M times the activations, the weights once
+    assert bench.step_bytes(8) - bench.step_bytes(1) == 64 * 7 * 2 * (2 * (5120 + 17408) + (17408 + 5120) + 2 * 5120)
+    # affine: one more metadata array per matrix
+    assert bench.step_bytes(1, True) - bench.step_bytes(1) == 64 * (3 * 1_392_640 + 409_600)
+
+
+def test_decode_chain_bytes():
+    # per layer: all four matrices once; h and a in/out of the attention
+    # product, a in and the FFN intermediate out of gate/up, the intermediate
+    # in and h out of the down product (bf16, M = 1)
+    w = 2 * 12_533_760 + 12_533_760 + 3_686_400
+    act = 2 * (5120 + 5120) + 2 * (5120 + 17408) + 2 * (17408 + 5120)
+    assert bench.chain_bytes(1) == 64 * (w + act)
