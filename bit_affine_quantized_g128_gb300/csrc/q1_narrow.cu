@@ -74,6 +74,7 @@ namespace {
 constexpr int kMaxWarps = 10;                     // consumer warps
 constexpr int kMaxThreads = (kMaxWarps + 1) * 32;  // + the producer warp
 constexpr int kQuad = 4;                          // groups per span
+constexpr int kMaxKS = 8;                         // CTAs per cluster (K slices)
 constexpr int kTileBytes = 16 * 64;               // 16 rows x 16 words
 constexpr int kSmemMax = 227 * 1024;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
@@ -260,6 +261,13 @@ __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int
       ::"r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(bar)
       : "memory");
 }
+// Cluster barrier without release semantics.  It closes a round of remote
+// reads: those values are already in registers (every one has been summed
+// and stored), so nothing needs to become visible, and the arrival does not
+// wait for this thread's outstanding global stores as a releasing one would.
+__device__ __forceinline__ void cluster_sync_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void consumer_sync(int nthreads) {
   asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }
@@ -395,7 +403,7 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
       while (j < target) issue_next();
       if (KS > 1) {
         cluster.sync();
-        cluster.sync();
+        cluster_sync_relaxed();
       }
     }
     return;
@@ -607,10 +615,17 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
         const int r = i & 15, lp = (i >> 4) % npairs, m = (i >> 4) / npairs;
         const int lt = lp * NMAT;
         const int64_t n = (int64_t)((rb + lt) / NMAT) * 16 + r;
+        // unrolled to the most spans a CTA holds, so that the loads need not
+        // wait for the sums before them; the sums stay in span order
+        const float *p0 = part + ((size_t)lt * QM * 16 + r) * MST + m;
+        const float *p1 = p0 + (size_t)QM * 16 * MST;
         float v0 = 0.f, v1 = 0.f;
-        for (int q = 0; q < QS; ++q) {
-          v0 += part[((size_t)(lt * QM + q) * 16 + r) * MST + m];
-          if (NMAT == 2) v1 += part[((size_t)((lt + 1) * QM + q) * 16 + r) * MST + m];
+#pragma unroll
+        for (int q = 0; q < kMaxWarps; ++q) {
+          if (q < QS) {
+            v0 += p0[(size_t)q * 16 * MST];
+            if (NMAT == 2) v1 += p1[(size_t)q * 16 * MST];
+          }
         }
         if (n < N) {
           const float o = NMAT == 2 ? v0 / (1.0f + expf(-v0)) * v1 : v0;  // SiLU(gate) * up
@@ -622,8 +637,11 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
       const int cnt = trc * 16 * M;
       for (int i = tid; i < cnt; i += nthreads) {
         const int m = i % M, r = (i / M) & 15, lt = i / (16 * M);
+        const float *p0 = part + ((size_t)lt * QM * 16 + r) * MST + m;
         float v = 0.f;
-        for (int q = 0; q < QS; ++q) v += part[((size_t)(lt * QM + q) * 16 + r) * MST + m];
+#pragma unroll
+        for (int q = 0; q < kMaxWarps; ++q)
+          if (q < QS) v += p0[(size_t)q * 16 * MST];
         red[((size_t)lt * 16 + r) * MST + m] = v;
       }
       cluster.sync();
@@ -636,18 +654,24 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
         const int r = i & 15, lp = lo + (i >> 4) % (hi - lo), m = (i >> 4) / (hi - lo);
         const int lt = lp * NMAT;
         const int64_t n = (int64_t)((rb + lt) / NMAT) * 16 + r;
+        // every rank's value is requested before the first one is added: the
+        // remote reads overlap instead of queueing one behind the other
+        const size_t o0 = ((size_t)lt * 16 + r) * MST + m, o1 = o0 + (size_t)16 * MST;
         float v0 = 0.f, v1 = 0.f;
-        for (int q = 0; q < KS; ++q) {
-          const float *rq = cluster.map_shared_rank(red, q);
-          v0 += rq[((size_t)lt * 16 + r) * MST + m];
-          if (NMAT == 2) v1 += rq[((size_t)(lt + 1) * 16 + r) * MST + m];
+#pragma unroll
+        for (int q = 0; q < kMaxKS; ++q) {
+          if (q < KS) {
+            const float *rq = cluster.map_shared_rank(red, q);
+            v0 += rq[o0];
+            if (NMAT == 2) v1 += rq[o1];
+          }
         }
         if (n < N) {
           const float o = NMAT == 2 ? v0 / (1.0f + expf(-v0)) * v1 : v0;
           store_act(a.out, (size_t)m * N + n, o, ydt);
         }
       }
-      cluster.sync();  // every rank is done reading this round's partials
+      cluster_sync_relaxed();  // every rank is done reading this round's partials
     }
   }
 }
@@ -767,7 +791,7 @@ bool choose_geo(int64_t N, int K, int M, Geo *out) {
   const int NT = (int)((N + 15) / 16);
   const int mst = M <= 1 ? 1 : (M <= 2 ? 2 : (M <= 4 ? 4 : 8));
   double best = -1.0;
-  for (int ks = 1; ks <= 8; ks *= 2) {
+  for (int ks = 1; ks <= kMaxKS; ks *= 2) {
     if (ks > QK) break;
     const int qm = (QK + ks - 1) / ks;
     if (qm > kMaxWarps) continue;
