@@ -32,13 +32,15 @@
 // pattern and rows 8..15 hold d_p / 2 (all exact in bf16); -E_g (or -C_g) is
 // then the accumulator that the group's MMA chain starts from.
 //
-// Work decomposition (one CTA per SM: up to 10 consumer warps and one
+// Work decomposition (one CTA per SM: up to 8 consumer warps and one
 // producer warp):
 //   * K is cut into spans of 4 groups (512 k).  A thread-block cluster of KS
 //     CTAs splits the spans into KS contiguous slices; inside a CTA every
-//     consumer warp owns one span for the whole launch and keeps its
-//     activation fragments (64 registers) and the span's C/E terms in
-//     registers;
+//     consumer warp owns one span for the whole launch, and with 9 or 10
+//     spans on 8 warps (5 on 4) also one group of the remaining spans, so
+//     that the SM's four sub-partitions get equal work; a warp keeps the
+//     activation fragments of its 4 or 5 groups (16 registers each) and their
+//     C/E terms in registers;
 //   * the clusters split the 16-row tiles of W into contiguous ranges; the
 //     R warps that own the same span take every R-th row tile of the range;
 //   * the producer warp streams the CTA's row tiles, in order, through a
@@ -48,13 +50,14 @@
 //     one box with the 16 rows' scales (and biases) of the whole K-slice, all
 //     completing on the slot's mbarrier; the consumers hand the slot back
 //     through a second mbarrier;
-//   * the four groups' MMA chains of a tile are interleaved, so that a warp
-//     always has four independent MMAs in flight;
+//   * the groups' MMA chains of a tile are interleaved, so that a warp
+//     always has four or five independent MMAs in flight;
 //   * per-tile partial sums go to shared memory and are combined over the
 //     spans in a fixed order, then over the cluster's CTAs in rank order
 //     through distributed shared memory (deterministic, no atomics).
 // Every mbarrier wait is bounded: one that runs out sets a device error word.
 #include <cooperative_groups.h>
+#include <type_traits>
 #include <cstring>
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -71,13 +74,25 @@ __device__ unsigned int g_narrow_err = 0;
 
 namespace {
 
-constexpr int kMaxWarps = 10;                     // consumer warps
+constexpr int kMaxSpans = 10;                     // spans per CTA
+constexpr int kMaxWarps = 8;                      // consumer warps
 constexpr int kMaxThreads = (kMaxWarps + 1) * 32;  // + the producer warp
 constexpr int kQuad = 4;                          // groups per span
 constexpr int kMaxKS = 8;                         // CTAs per cluster (K slices)
 constexpr int kTileBytes = 16 * 64;               // 16 rows x 16 words
 constexpr int kSmemMax = 227 * 1024;
+constexpr int kRingBytes = 24 * 1024;             // ring slots per SM, in bytes (about)
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+
+// Consumer warps along K for a CTA of qs spans.  Each warp owns one span,
+// except that 9 or 10 spans go to 8 warps and 5 spans to 4 warps; the spans
+// past the warps are then dealt out one group per warp (warp w also takes
+// group w % 4 of span nw + w / 4).  The warps are spread round-robin over the
+// SM's four sub-partitions, whose tensor and integer pipes bound the tile
+// loop: 10 one-span warps would load two sub-partitions with three warps
+// (12 groups) while the other two carry 8; 8 warps of 5 groups load each
+// with 10.
+__host__ __device__ inline int kwarps(int qs) { return qs > 8 ? 8 : (qs == 5 ? 4 : qs); }
 
 __host__ __device__ constexpr int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
@@ -161,6 +176,11 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
   return v;
 }
+__device__ __forceinline__ uint32_t lds16(uint32_t addr) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
 __device__ __forceinline__ uint2 lds64(uint32_t addr) {
   uint2 v;
   asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
@@ -224,7 +244,7 @@ __host__ __device__ inline SmemLayout smem_layout(const Geo &g, bool affine) {
   L.ring = off; off += g.ring * L.slot_words;
   L.meta = off; off += g.ring * L.slot_meta;
   L.bars = off; off += align_up(2 * g.ring * 8, 128);
-  L.part = off; off += g.tr * g.qm * 16 * (g.mst < 2 ? 2 : g.mst) * 4;
+  L.part = off; off += g.tr * kwarps(g.qm) * 16 * (g.mst < 2 ? 2 : g.mst) * 4;
   L.red = off; off += g.ks > 1 ? g.tr * 16 * (g.mst < 2 ? 2 : g.mst) * 4 : 0;
   L.total = off + 1024;  // slack for aligning the dynamic shared memory base
   return L;
@@ -272,12 +292,13 @@ __device__ __forceinline__ void consumer_sync(int nthreads) {
   asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }
 
-// One CTA: NC = qm * R consumer warps and one producer warp (the last).
-// The producer streams the CTA's row tiles in order through a ring of
-// row-tile slots: per slot 1 KB of words per span of the CTA (16 rows x
+// One CTA: NC = kwarps(qm) * R consumer warps and one producer warp (the
+// last).  The producer streams the CTA's row tiles in order through a ring
+// of row-tile slots: per slot 1 KB of words per span of the CTA (16 rows x
 // 16 words, 64-byte swizzle) and the rows' metadata.  Consumer warp
-// (qi, ri) owns span q_lo + qi and takes the row tiles ri, ri + R, ... of
-// each round.
+// (qi, ri) owns span q_lo + qi, plus one group of a span past the K-warps
+// when the CTA has more spans than K-warps, and takes the row tiles ri,
+// ri + R, ... of each round.
 // FASTMETA: G % 8 == 0 and 16-byte aligned metadata, so the scales (and
 // biases) come as one TMA box of meta_groups(qm) groups x 16 rows; otherwise
 // the producer's lanes load them (zero past K) and store them before their
@@ -298,7 +319,8 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
   const int KS = geo.ks, RING = geo.ring, QM = geo.qm, R = geo.R, TR = geo.tr;
   const int MST = geo.mst < 2 ? 2 : geo.mst;  // tokens stored per partial row (a lane stores a pair)
   const SmemLayout L = smem_layout(geo, AFFINE);
-  const int NC = QM * R;                    // consumer warps
+  const int NWM = kwarps(QM);               // K-warps of the widest slice
+  const int NC = NWM * R;                   // consumer warps
   const int MROW = meta_groups(QM) * 2;     // bytes per metadata row
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -308,6 +330,7 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
   const int QK = (G + kQuad - 1) / kQuad;  // spans in K
   const int q_lo = (int)(((int64_t)QK * rank) / KS), q_hi = (int)(((int64_t)QK * (rank + 1)) / KS);
   const int QS = q_hi - q_lo;               // spans of this CTA
+  const int NW = kwarps(QS);                // K-warps of this CTA
   const int q_base = q_lo & ~1;             // first span of the metadata rows
   const int NT = (int)((N + 15) / 16);
   const int v_lo = (int)(((int64_t)NT * clus) / geo.nclus) * NMAT;
@@ -322,10 +345,10 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
 
   if (warp == NC && lane < RING) {
     // full: the producer's expect_tx (plus, without metadata TMA, the 32
-    // producer lanes' arrivals); empty: one arrival per consumer warp
+    // producer lanes' arrivals); empty: one arrival per K-warp
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(full_s + 8 * lane), "r"(FASTMETA ? 1 : 33)
                  : "memory");
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(empty_s + 8 * lane), "r"(QS) : "memory");
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(empty_s + 8 * lane), "r"(NW) : "memory");
   }
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   __syncthreads();
@@ -414,25 +437,33 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
   // type of each matrix read at run time, bf16 in and out; 2: metadata type
   // and the dtypes of x and y all read at run time
   const int xdt = VAR == 2 ? a.xdt : (int)Q1_BF16, ydt = VAR == 2 ? a.ydt : (int)Q1_BF16;
-  const int qi = warp % QM, ri = warp / QM;
-  const bool active = qi < QS;
+  const int qi = warp % NWM, ri = warp / NWM;
+  const bool active = qi < NW;
   const int span = q_lo + qi;  // groups 4 span .. 4 span + 3
+  // the extra group of the first 4 (QS - NW) K-warps: group xu of span xspan
+  const bool has_ex = active && qi < 4 * (QS - NW);
+  const int xspan = q_lo + NW + (qi >> 2), xu = qi & 3;
   const int nthreads = NC * 32;
 
   // x may be the output of the preceding kernel: wait for it before reading
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  // ---- activation fragments of this warp's span (token gid, word t of each
+  // The rest is compiled twice, for warps of 4 groups and of 5 (the body is
+  // the same; only the loops over the warp's groups get longer).
+  auto consume = [&](auto ex) {
+  constexpr int NG = decltype(ex)::value ? kQuad + 1 : kQuad;  // groups of this warp
+
+  // ---- activation fragments of this warp's groups (token gid, word t of each
   //      group) and the per-group accumulator seeds: all loads first, then
-  //      the fragments, then the four groups' C/E chains interleaved
-  uint32_t bfr[kQuad][16];
-  float seed[kQuad][4];
-  float sx[kQuad][2];
+  //      the fragments, then the groups' C/E chains interleaved
+  uint32_t bfr[NG][16];
+  float seed[NG][4];
+  float sx[NG][2];
   if (active) {
-    uint32_t xv[kQuad][16];
+    uint32_t xv[NG][16];
 #pragma unroll
-    for (int u = 0; u < kQuad; ++u) {
-      const int g = span * kQuad + u;
+    for (int u = 0; u < NG; ++u) {
+      const int g = u < kQuad ? span * kQuad + u : xspan * kQuad + xu;
       if (gid < M && g < G) {
         // this lane's 32 activations of the group as 16 bf16 pairs; fp16 and
         // fp32 activations are rounded to bf16 (the MMA operand type) once here
@@ -466,7 +497,7 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
       }
     }
 #pragma unroll
-    for (int u = 0; u < kQuad; ++u) {
+    for (int u = 0; u < NG; ++u) {
 #define Q1_PAIR(P) \
   bfr[u][P] = bmul2(prmt(xv[u][(P) >> 1], xv[u][8 + ((P) >> 1)], ((P) & 1) ? 0x7632u : 0x5410u), inv_d_bits(P));
       Q1_PAIR(0) Q1_PAIR(1) Q1_PAIR(2) Q1_PAIR(3) Q1_PAIR(4) Q1_PAIR(5) Q1_PAIR(6) Q1_PAIR(7)
@@ -474,17 +505,17 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
 #undef Q1_PAIR
     }
     // rows 0..7: C_g = sum a_p x'; rows 8..15: Sx_g / 2 = sum (d_p / 2) x'
-    float d[kQuad][4];
+    float d[NG][4];
 #pragma unroll
-    for (int u = 0; u < kQuad; ++u) d[u][0] = d[u][1] = d[u][2] = d[u][3] = 0.f;
+    for (int u = 0; u < NG; ++u) d[u][0] = d[u][1] = d[u][2] = d[u][3] = 0.f;
 #define Q1_CE(JJ)                                                                                           \
-  _Pragma("unroll") for (int u = 0; u < kQuad; ++u)                                                         \
+  _Pragma("unroll") for (int u = 0; u < NG; ++u)                                                            \
       mma_acc(d[u], a_bits(2 * (JJ)), halfd_bits(2 * (JJ)), a_bits(2 * (JJ) + 1), halfd_bits(2 * (JJ) + 1), \
               bfr[u][2 * (JJ)], bfr[u][2 * (JJ) + 1]);
     Q1_CE(0) Q1_CE(1) Q1_CE(2) Q1_CE(3) Q1_CE(4) Q1_CE(5) Q1_CE(6) Q1_CE(7)
 #undef Q1_CE
 #pragma unroll
-    for (int u = 0; u < kQuad; ++u) {
+    for (int u = 0; u < NG; ++u) {
       // tokens 2t, 2t+1
       const float e0 = AFFINE ? d[u][0] : d[u][0] + d[u][2], e1 = AFFINE ? d[u][1] : d[u][1] + d[u][3];
       seed[u][0] = -e0; seed[u][1] = -e1; seed[u][2] = -e0; seed[u][3] = -e1;
@@ -502,8 +533,11 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
   const int swz = (gid >> 1) & 3;
   const uint32_t wlane = ring_s + qi * kTileBytes + gid * 64 + 4 * t;
   const uint32_t mlane = meta_s + gid * MROW + (span - q_base) * 8;
+  // the extra group's words and metadata, relative to those of the span
+  const uint32_t xw = (uint32_t)((xspan - span) * kTileBytes + ((xu ^ swz) << 4));
+  const uint32_t xm = (uint32_t)((xspan - span) * 8 + 2 * xu);
 
-  // this lane's partial sums (rows gid, gid + 8 of span qi; tokens 2t, 2t+1)
+  // this lane's partial sums (rows gid, gid + 8 of K-warp qi; tokens 2t, 2t+1)
   const uint32_t plane = smem_u32(part) + (uint32_t)(((qi * 16 + gid) * MST + 2 * t) * 4);
   const bool pstore = 2 * t < MST;
   const uint32_t SW = (uint32_t)a.slot_words, SM = (uint32_t)a.slot_meta, PT = (uint32_t)a.part_tile;
@@ -521,34 +555,44 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
         // a wait that ran out has set the device error word; the results of
         // this call are then undefined, but the CTA still reaches its barriers
         mbar_wait(fb, ph);
-        uint32_t wa[kQuad], wb[kQuad];
+        uint32_t wa[NG], wb[NG];
 #pragma unroll
-        for (int u = 0; u < kQuad; ++u) {
-          wa[u] = lds32(tb + ((u ^ swz) << 4));
-          wb[u] = lds32(tb + ((u ^ swz) << 4) + 8 * 64);
+        for (int u = 0; u < NG; ++u) {
+          const uint32_t o = u < kQuad ? (uint32_t)((u ^ swz) << 4) : xw;
+          wa[u] = lds32(tb + o);
+          wb[u] = lds32(tb + o + 8 * 64);
         }
         const uint2 sa = lds64(mb), sb = lds64(mb + 8 * MROW);
+        uint32_t xsa = 0u, xsb = 0u, xba = 0u, xbb = 0u;
+        if (NG > kQuad) {
+          xsa = lds16(mb + xm);
+          xsb = lds16(mb + xm + 8 * MROW);
+        }
         uint2 ba = make_uint2(0, 0), bb = make_uint2(0, 0);
         const bool has_b = AFFINE && ((NMAT == 2 && ((rb + lt) & 1)) ? a.b[1] : a.b[0]) != nullptr;
         if (AFFINE && has_b) {
           ba = lds64(mb + 16 * MROW);
           bb = lds64(mb + 24 * MROW);
+          if (NG > kQuad) {
+            xba = lds16(mb + xm + 16 * MROW);
+            xbb = lds16(mb + xm + 24 * MROW);
+          }
         }
-        uint32_t wa8[kQuad], wb8[kQuad];
+        uint32_t wa8[NG], wb8[NG];
 #pragma unroll
-        for (int u = 0; u < kQuad; ++u) {
+        for (int u = 0; u < NG; ++u) {
           wa8[u] = wa[u] >> 8;
           wb8[u] = wb[u] >> 8;
         }
-        // four independent chains (one per group), interleaved step by step
-        float d[kQuad][4];
+        // independent chains (one per group), interleaved step by step
+        float d[NG][4];
 #pragma unroll
-        for (int u = 0; u < kQuad; ++u)
+        for (int u = 0; u < NG; ++u)
           mma_from(d[u], pair_reg<0>(wa[u], wa8[u], kbase), pair_reg<0>(wb[u], wb8[u], kbase),
                    pair_reg<1>(wa[u], wa8[u], kbase), pair_reg<1>(wb[u], wb8[u], kbase), bfr[u][0], bfr[u][1],
                    seed[u]);
 #define Q1_MMA(JJ)                                                                                          \
-  _Pragma("unroll") for (int u = 0; u < kQuad; ++u)                                                         \
+  _Pragma("unroll") for (int u = 0; u < NG; ++u)                                                            \
       mma_acc(d[u], pair_reg<2 * (JJ)>(wa[u], wa8[u], kbase), pair_reg<2 * (JJ)>(wb[u], wb8[u], kbase),       \
               pair_reg<2 * (JJ) + 1>(wa[u], wa8[u], kbase), pair_reg<2 * (JJ) + 1>(wb[u], wb8[u], kbase),     \
               bfr[u][2 * (JJ)], bfr[u][2 * (JJ) + 1]);
@@ -557,9 +601,9 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
         float acc[4];
         const bool mbf = VAR >= 1 && ((a.meta_bf16 >> ((NMAT == 2 && ((rb + lt) & 1)) ? 1 : 0)) & 1) != 0;
 #pragma unroll
-        for (int u = 0; u < kQuad; ++u) {
-          const uint32_t hs_a = (u < 2 ? sa.x : sa.y) >> (16 * (u & 1));
-          const uint32_t hs_b = (u < 2 ? sb.x : sb.y) >> (16 * (u & 1));
+        for (int u = 0; u < NG; ++u) {
+          const uint32_t hs_a = u < kQuad ? (u < 2 ? sa.x : sa.y) >> (16 * (u & 1)) : xsa;
+          const uint32_t hs_b = u < kQuad ? (u < 2 ? sb.x : sb.y) >> (16 * (u & 1)) : xsb;
           const float s_a = meta_f32(hs_a, mbf);
           const float s_b = meta_f32(hs_b, mbf);
           if (u == 0) {
@@ -571,8 +615,8 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
           if (AFFINE) {
             float b_a, b_b;
             if (has_b) {
-              b_a = meta_f32((u < 2 ? ba.x : ba.y) >> (16 * (u & 1)), mbf);
-              b_b = meta_f32((u < 2 ? bb.x : bb.y) >> (16 * (u & 1)), mbf);
+              b_a = meta_f32(u < kQuad ? (u < 2 ? ba.x : ba.y) >> (16 * (u & 1)) : xba, mbf);
+              b_b = meta_f32(u < kQuad ? (u < 2 ? bb.x : bb.y) >> (16 * (u & 1)) : xbb, mbf);
             } else {  // matrix without stored biases: symmetric
               b_a = __fmul_rn(-0.5f, s_a);
               b_b = __fmul_rn(-0.5f, s_b);
@@ -615,14 +659,14 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
         const int r = i & 15, lp = (i >> 4) % npairs, m = (i >> 4) / npairs;
         const int lt = lp * NMAT;
         const int64_t n = (int64_t)((rb + lt) / NMAT) * 16 + r;
-        // unrolled to the most spans a CTA holds, so that the loads need not
-        // wait for the sums before them; the sums stay in span order
-        const float *p0 = part + ((size_t)lt * QM * 16 + r) * MST + m;
-        const float *p1 = p0 + (size_t)QM * 16 * MST;
+        // unrolled to the most K-warps a CTA holds, so that the loads need
+        // not wait for the sums before them; the sums stay in K-warp order
+        const float *p0 = part + ((size_t)lt * NWM * 16 + r) * MST + m;
+        const float *p1 = p0 + (size_t)NWM * 16 * MST;
         float v0 = 0.f, v1 = 0.f;
 #pragma unroll
         for (int q = 0; q < kMaxWarps; ++q) {
-          if (q < QS) {
+          if (q < NW) {
             v0 += p0[(size_t)q * 16 * MST];
             if (NMAT == 2) v1 += p1[(size_t)q * 16 * MST];
           }
@@ -637,11 +681,11 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
       const int cnt = trc * 16 * M;
       for (int i = tid; i < cnt; i += nthreads) {
         const int m = i % M, r = (i / M) & 15, lt = i / (16 * M);
-        const float *p0 = part + ((size_t)lt * QM * 16 + r) * MST + m;
+        const float *p0 = part + ((size_t)lt * NWM * 16 + r) * MST + m;
         float v = 0.f;
 #pragma unroll
         for (int q = 0; q < kMaxWarps; ++q)
-          if (q < QS) v += p0[(size_t)q * 16 * MST];
+          if (q < NW) v += p0[(size_t)q * 16 * MST];
         red[((size_t)lt * 16 + r) * MST + m] = v;
       }
       cluster.sync();
@@ -674,6 +718,11 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
       cluster_sync_relaxed();  // every rank is done reading this round's partials
     }
   }
+  };
+  if (has_ex)
+    consume(std::true_type{});
+  else
+    consume(std::false_type{});
 }
 
 // ---------------------------------------------------------------------------
@@ -779,11 +828,12 @@ bool make_meta_map(CUtensorMap *map, const uint16_t *m, int64_t N, int64_t G, in
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Pick the geometry: among cluster sizes KS (K slices) whose consumer warps
-// fit, the one with the least estimated work on the busiest SM, in tile
-// units: its tiles (spans x virtual row tiles of the widest cluster range),
-// about 0.7 tile per warp for the activation fragments, the cluster
-// exchange, and the extra rounds when the partial sums do not fit at once.
+// Pick the geometry: among cluster sizes KS (K slices) whose spans fit, the
+// one with the least estimated work on the busiest SM, in span-tile units:
+// the group-tiles of its busiest sub-partition (a quarter of the SM's when
+// balanced) or the producer's per-slot cost if that is larger, about 0.7
+// tile per warp for the activation fragments, the cluster exchange, and the
+// extra rounds when the partial sums do not fit at once.
 template <int NMAT, bool AFFINE, bool FASTMETA, int VAR>
 bool choose_geo(int64_t N, int K, int M, Geo *out) {
   const int G = K / 128;
@@ -794,20 +844,29 @@ bool choose_geo(int64_t N, int K, int M, Geo *out) {
   for (int ks = 1; ks <= kMaxKS; ks *= 2) {
     if (ks > QK) break;
     const int qm = (QK + ks - 1) / ks;
-    if (qm > kMaxWarps) continue;
+    if (qm > kMaxSpans) continue;
+    const int nw = kwarps(qm);
     int nclus = max_clusters<NMAT, AFFINE, FASTMETA, VAR>(ks);
     if (nclus > NT) nclus = NT;
     const int tv = ((NT + nclus - 1) / nclus) * NMAT;  // virtual row tiles of the widest range
-    int R = kMaxWarps / qm;
+    int R = kMaxWarps / nw;
     if (R > tv) R = tv;
     if (R < 1) R = 1;
-    const int W = qm * R;
-    // ring: row tiles in flight; at least R + 1 so that every consumer warp
-    // can have its next tile loading
-    int ring = tv < 8 ? tv : 8;
+    const int W = nw * R;
+    // ring: row tiles in flight.  About kRingBytes of slots per SM keeps
+    // enough requests in flight for this kernel, whose tile loop consumes a
+    // few TB/s across the GPU; a deeper ring only lengthens the memory queues
+    // that the activation loads wait in.  At least R + 1 slots, so that every
+    // consumer warp can have its next tile loading.
+    Geo g{ks, nclus, qm, R, tv, 2, mst};
+    const SmemLayout L0 = smem_layout(g, AFFINE);
+    const int slot = L0.slot_words + L0.slot_meta;
+    int ring = (kRingBytes + slot - 1) / slot;
+    if (ring > 8) ring = 8;
+    if (ring > tv) ring = tv;
     if (ring < R + 1) ring = R + 1 < tv ? R + 1 : tv;
     if (ring < 2) ring = 2;
-    Geo g{ks, nclus, qm, R, tv, ring, mst};
+    g.ring = ring;
     // shrink the round, then the ring, until shared memory fits
     while (smem_layout(g, AFFINE).total > kSmemMax) {
       if (g.tr > 16 * NMAT) {
@@ -828,8 +887,21 @@ bool choose_geo(int64_t N, int K, int M, Geo *out) {
     // per span, a ring shorter than R + 1 could starve a warp
     if (g.ring < (R + 1 < tv ? R + 1 : tv)) continue;
     const int rounds = (tv + g.tr - 1) / g.tr;
-    double tiles = (double)qm * tv;
-    if (W < 8) tiles *= 8.0 / W;  // too few warps to keep the pipes busy
+    // group-tiles of the busiest SM sub-partition (warp w runs on w % 4 and
+    // takes its groups of every R-th row tile); qm x tv when all four carry
+    // the same, more when they do not
+    double load[4] = {0.0, 0.0, 0.0, 0.0};
+    for (int w = 0; w < W; ++w) {
+      const int q = w % nw, r = w / nw;
+      const int groups = kQuad + (q < kQuad * (qm - nw) ? 1 : 0);
+      load[w % 4] += (double)groups * ((tv - r + R - 1) / R);
+    }
+    double tiles = load[0];
+    for (int i = 1; i < 4; ++i) tiles = load[i] > tiles ? load[i] : tiles;
+    if (W < 8) tiles *= 1.25;  // a sub-partition with one warp hides less latency
+    // the producer spends a few hundred clocks on every slot (about 3 units)
+    // however small: with thin K-slices and long row ranges it sets the pace
+    if (3.0 * tv > tiles) tiles = 3.0 * tv;
     const double cost = tiles + 0.7 * W + (ks > 1 ? 20.0 : 0.0) + 20.0 * (rounds - 1);
     if (best < 0 || cost < best) {
       best = cost;
@@ -856,7 +928,7 @@ cudaError_t launch_impl(NarrowArgs args, const uint32_t *w0, const uint32_t *w1,
     const SmemLayout L0 = smem_layout(g, AFFINE);
     args.slot_words = L0.slot_words;
     args.slot_meta = L0.slot_meta;
-    args.part_tile = g.qm * 16 * (g.mst < 2 ? 2 : g.mst) * 4;
+    args.part_tile = kwarps(g.qm) * 16 * (g.mst < 2 ? 2 : g.mst) * 4;
   }
   Maps maps;
   memset(&maps, 0, sizeof(maps));
@@ -878,7 +950,7 @@ cudaError_t launch_impl(NarrowArgs args, const uint32_t *w0, const uint32_t *w1,
   const SmemLayout L = smem_layout(g, AFFINE);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(g.nclus * g.ks), 1, 1);
-  cfg.blockDim = dim3((unsigned)((g.qm * g.R + 1) * 32), 1, 1);
+  cfg.blockDim = dim3((unsigned)((kwarps(g.qm) * g.R + 1) * 32), 1, 1);
   cfg.dynamicSmemBytes = (size_t)L.total;
   cfg.stream = st;
   cudaLaunchAttribute attrs[2];
