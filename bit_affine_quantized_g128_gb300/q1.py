@@ -114,13 +114,52 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
     return None if t is None else t.data_ptr()
 
 
+# The library takes raw device pointers and cannot tell a host pointer, a
+# tensor on another GPU or a short output buffer from a good one: the kernels
+# would fault or write past the end.  These checks turn such calls into a
+# ValueError before anything is launched.
+def _cuda(t, name: str, device=None) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    return t
+
+
+def _out(out: Optional[torch.Tensor], shape, dtype, device, name: str = "out") -> torch.Tensor:
+    """`out` checked against what the call writes (or a new tensor of that shape)."""
+    if out is None:
+        return torch.empty(shape, dtype=dtype, device=device)
+    _cuda(out, name, device)
+    n = 1
+    for d in shape:
+        n *= int(d)
+    if out.dtype != dtype or not out.is_contiguous() or out.numel() != n:
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor of {n} elements "
+                         f"(got {out.dtype}, {tuple(out.shape)}, contiguous={out.is_contiguous()})")
+    return out
+
+
+def _x_dtype(x: torch.Tensor, name: str = "x") -> int:
+    if x.dtype not in _DT:
+        raise ValueError(f"{name} must be bfloat16, float16 or float32 (got {x.dtype})")
+    return _DT[x.dtype]
+
+
 class Q1Weight:
     """A packed Q1 weight on the GPU: words uint32 [N, K/32] (held as int32),
-    scales [N, K/128] and biases [N, K/128] or None (symmetric), the metadata
-    either fp16 or bf16 (both tensors the same dtype)."""
+    scales [N, K/group_size] and biases of the same shape or None
+    (symmetric), the metadata either fp16 or bf16 (both tensors the same
+    dtype); all on one CUDA device."""
 
     def __init__(self, words: torch.Tensor, scales: torch.Tensor,
                  biases: Optional[torch.Tensor], K: int):
+        _cuda(words, "Q1Weight words")
+        _cuda(scales, "Q1Weight scales", words.device)
+        if biases is not None:
+            _cuda(biases, "Q1Weight biases", words.device)
+        if words.dtype not in (torch.int32, torch.uint32):
+            raise ValueError(f"Q1Weight words must be int32 or uint32 (the packed words), got {words.dtype}")
         self.words = words.contiguous()
         self.scales = scales.contiguous()
         self.biases = None if biases is None else biases.contiguous()
@@ -157,6 +196,9 @@ def _flat(x: torch.Tensor, K: int) -> torch.Tensor:
 
 def pack(bits: torch.Tensor) -> torch.Tensor:
     """bits uint8 [N, K] -> words int32 [N, K/32] (LSB first)."""
+    _cuda(bits, "bits")
+    if bits.dtype != torch.uint8 or bits.dim() != 2:
+        raise ValueError(f"bits must be a 2-D uint8 tensor (got {bits.dtype}, {tuple(bits.shape)})")
     bits = bits.contiguous()
     N, K = bits.shape
     w = torch.empty((N, K // 32), dtype=torch.int32, device=bits.device)
@@ -165,6 +207,10 @@ def pack(bits: torch.Tensor) -> torch.Tensor:
 
 
 def unpack(words: torch.Tensor, K: int) -> torch.Tensor:
+    """words int32 [N, K/32] -> bits uint8 [N, K]."""
+    _cuda(words, "words")
+    if words.dim() != 2 or words.shape[1] * 32 != K:
+        raise ValueError(f"words must be [N, K/32] for K = {K} (got {tuple(words.shape)})")
     words = words.contiguous()
     N = words.shape[0]
     out = torch.empty((N, K), dtype=torch.uint8, device=words.device)
@@ -173,6 +219,8 @@ def unpack(words: torch.Tensor, K: int) -> torch.Tensor:
 
 
 def dequantize(W: Q1Weight, dtype=torch.bfloat16) -> torch.Tensor:
+    if dtype not in _DT:
+        raise ValueError(f"dtype must be bfloat16, float16 or float32 (got {dtype})")
     out = torch.empty((W.N, W.K), dtype=dtype, device=W.words.device)
     _check("q1_dequantize", lib().q1_dequantize(W.cref(), _DT[dtype], out.data_ptr(), _stream()))
     return out
@@ -180,24 +228,29 @@ def dequantize(W: Q1Weight, dtype=torch.bfloat16) -> torch.Tensor:
 
 def qmv(W: Q1Weight, x: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
     """x [K] -> y [N] (M = 1 decode)."""
+    _cuda(x, "x", W.words.device)
+    xdt = _x_dtype(x)
     x = x.reshape(W.K).contiguous()
-    y = out if out is not None else torch.empty((W.N,), dtype=x.dtype, device=x.device)
-    _check("q1_qmv", lib().q1_qmv(W.cref(), x.data_ptr(), _DT[x.dtype], y.data_ptr(), _stream()))
+    y = _out(out, (W.N,), x.dtype, x.device)
+    _check("q1_qmv", lib().q1_qmv(W.cref(), x.data_ptr(), xdt, y.data_ptr(), _stream()))
     return y
 
 
 def qmm_workspace(M: int, N: int, K: int, device) -> torch.Tensor:
+    """A byte buffer of the size q1_qmm needs for M x N x K (at least 256 B)."""
     n = lib().q1_qmm_workspace_size(M, N, K)
     return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
 
 
 def qmm_narrow(W: Q1Weight, x: torch.Tensor, out=None) -> torch.Tensor:
     """x [..., K] with prod(leading dims) <= 8 -> y [..., N]; weights stay packed."""
+    _cuda(x, "x", W.words.device)
+    xdt = _x_dtype(x)
     lead = x.shape[:-1]
     x2 = _flat(x, W.K)
     M = x2.shape[0]
-    y = out if out is not None else torch.empty((M, W.N), dtype=x.dtype, device=x.device)
-    _check("q1_qmm_narrow", lib().q1_qmm_narrow(W.cref(), x2.data_ptr(), M, _DT[x.dtype],
+    y = _out(out, (M, W.N), x.dtype, x.device)
+    _check("q1_qmm_narrow", lib().q1_qmm_narrow(W.cref(), x2.data_ptr(), M, xdt,
                                                 y.data_ptr(), _stream()))
     return y.reshape(*lead, W.N)
 
@@ -207,15 +260,19 @@ def qmm(W: Q1Weight, x: torch.Tensor, workspace: Optional[torch.Tensor] = None,
     """x [..., K] -> y [..., N]; narrow path up to the row threshold, tcgen05 beyond
     and for group sizes 32 and 64 (which needs a workspace; one is allocated
     when none is given)."""
+    _cuda(x, "x", W.words.device)
+    xdt = _x_dtype(x)
     lead = x.shape[:-1]
     x2 = _flat(x, W.K)
     M = x2.shape[0]
-    y = out if out is not None else torch.empty((M, W.N), dtype=x.dtype, device=x.device)
+    y = _out(out, (M, W.N), x.dtype, x.device)
     ws = workspace
     if ws is None and (M > get_qmm_max_rows() or W.K > NARROW_MAX_K or W.group_size != 128):
         ws = qmm_workspace(M, W.N, W.K, x.device)
-    wp, wn = (ws.data_ptr(), ws.numel()) if ws is not None else (None, 0)
-    _check("q1_qmm", lib().q1_qmm(W.cref(), x2.data_ptr(), M, _DT[x.dtype], y.data_ptr(), wp, wn,
+    if ws is not None:
+        _cuda(ws, "workspace", x.device)
+    wp, wn = (ws.data_ptr(), ws.numel() * ws.element_size()) if ws is not None else (None, 0)
+    _check("q1_qmm", lib().q1_qmm(W.cref(), x2.data_ptr(), M, xdt, y.data_ptr(), wp, wn,
                                   _stream()))
     return y.reshape(*lead, W.N)
 
@@ -230,6 +287,9 @@ def get_qmm_max_rows() -> int:
 
 def embed_gather(E: Q1Weight, ids: torch.Tensor, dtype=torch.bfloat16):
     """ids int32 [T] (device) -> (rows [T, K], out-of-range count int32 [1] on device)."""
+    _cuda(ids, "ids", E.words.device)
+    if dtype not in _DT:
+        raise ValueError(f"dtype must be bfloat16, float16 or float32 (got {dtype})")
     ids = ids.to(torch.int32).contiguous()
     T = ids.numel()
     out = torch.empty((T, E.K), dtype=dtype, device=E.words.device)
@@ -240,20 +300,25 @@ def embed_gather(E: Q1Weight, ids: torch.Tensor, dtype=torch.bfloat16):
 
 
 def ffn_workspace(M: int, D: int, F: int, device) -> torch.Tensor:
+    """A byte buffer of the size q1_ffn_fused needs (at least 256 B)."""
     n = lib().q1_ffn_workspace_size(M, D, F)
     return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
 
 
 def ffn_fused(gate: Q1Weight, up: Q1Weight, down: Q1Weight, x: torch.Tensor,
               workspace=None, out=None) -> torch.Tensor:
+    """y = down . (SiLU(gate . x) * (up . x)); x [..., D] -> y [..., D]."""
+    _cuda(x, "x", gate.words.device)
+    xdt = _x_dtype(x)
     lead = x.shape[:-1]
     x2 = _flat(x, gate.K)
     M = x2.shape[0]
-    y = out if out is not None else torch.empty((M, down.N), dtype=x.dtype, device=x.device)
+    y = _out(out, (M, down.N), x.dtype, x.device)
     ws = workspace if workspace is not None else ffn_workspace(M, gate.K, gate.N, x.device)
+    _cuda(ws, "workspace", x.device)
     _check("q1_ffn_fused", lib().q1_ffn_fused(gate.cref(), up.cref(), down.cref(), x2.data_ptr(), M,
-                                              _DT[x.dtype], y.data_ptr(), ws.data_ptr(),
-                                              ws.numel(), _stream()))
+                                              xdt, y.data_ptr(), ws.data_ptr(),
+                                              ws.numel() * ws.element_size(), _stream()))
     return y.reshape(*lead, down.N)
 
 
@@ -261,12 +326,14 @@ def ffn_fused_noalloc(gate: Q1Weight, up: Q1Weight, down: Q1Weight, x: torch.Ten
                       out=None) -> torch.Tensor:
     """q1_ffn_fused with h in the library's fixed device array (no workspace,
     no allocation in the call; `out` may be preallocated too)."""
+    _cuda(x, "x", gate.words.device)
+    xdt = _x_dtype(x)
     lead = x.shape[:-1]
     x2 = _flat(x, gate.K)
     M = x2.shape[0]
-    y = out if out is not None else torch.empty((M, down.N), dtype=x.dtype, device=x.device)
+    y = _out(out, (M, down.N), x.dtype, x.device)
     _check("q1_ffn_fused_noalloc", lib().q1_ffn_fused_noalloc(gate.cref(), up.cref(), down.cref(),
-                                                              x2.data_ptr(), M, _DT[x.dtype],
+                                                              x2.data_ptr(), M, xdt,
                                                               y.data_ptr(), _stream()))
     return y.reshape(*lead, down.N)
 
@@ -282,6 +349,10 @@ def pack_from_dense(dense: torch.Tensor, symmetric: bool, bad: Optional[torch.Te
     tensor.  Returns (Q1Weight, bad), bad a device int32 [1] that counts the
     refused groups (added to `bad` when given).  `out` (a Q1Weight of the same
     shape, with biases unless symmetric) receives the result in place."""
+    _cuda(dense, "dense")
+    ddt = _x_dtype(dense, "dense")
+    if dense.dim() != 2:
+        raise ValueError(f"dense must be 2-D [N, K] (got {tuple(dense.shape)})")
     d = dense.contiguous()
     N, K = int(d.shape[0]), int(d.shape[1])
     dev = d.device
@@ -294,13 +365,18 @@ def pack_from_dense(dense: torch.Tensor, symmetric: bool, bad: Optional[torch.Te
         raise ValueError("pack_from_dense: `out` does not match the dense shape or mode")
     if bad is None:
         bad = torch.zeros((1,), dtype=torch.int32, device=dev)
-    _check("q1_pack_from_dense", lib().q1_pack_from_dense(d.data_ptr(), _DT[d.dtype], N, K, out.words.data_ptr(),
+    elif bad.dtype != torch.int32 or bad.numel() < 1:
+        raise ValueError("bad must be an int32 tensor of at least one element")
+    _cuda(bad, "bad", dev)
+    _cuda(out.words, "out words", dev)
+    _check("q1_pack_from_dense", lib().q1_pack_from_dense(d.data_ptr(), ddt, N, K, out.words.data_ptr(),
                                                           out.scales.data_ptr(), _ptr(out.biases),
                                                           bad.data_ptr(), _stream()))
     return out, bad
 
 
 def decode_chain_workspace(M: int, D: int, F_max: int, device) -> torch.Tensor:
+    """A byte buffer of the size q1_decode_chain needs (at least 256 B)."""
     n = lib().q1_decode_chain_workspace_size(M, D, F_max)
     return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
 
@@ -309,17 +385,26 @@ def decode_chain(layers, x: torch.Tensor, workspace=None, out=None) -> torch.Ten
     """q1_decode_chain: layers is a sequence of (attn, gate, up, down) Q1Weights;
     per layer a = attn . h, then h = down . (SiLU(gate . a) * (up . a))."""
     layers = list(layers)
+    if not layers:
+        raise ValueError("decode_chain needs at least one layer")
+    _cuda(x, "x", layers[0][0].words.device)
+    xdt = _x_dtype(x)
+    for li, lw in enumerate(layers):
+        for W in lw:
+            _cuda(W.words, f"layer {li} weights", x.device)
     lead = x.shape[:-1]
     D = layers[0][0].N
     x2 = _flat(x, D)
     M = x2.shape[0]
     arr = (_CLayer * len(layers))(*[_CLayer(a._c, g._c, u._c, d._c) for (a, g, u, d) in layers])
-    y = out if out is not None else torch.empty((M, D), dtype=x.dtype, device=x.device)
+    y = _out(out, (M, D), x.dtype, x.device)
     if workspace is None:
         workspace = decode_chain_workspace(M, D, max(g.N for (_, g, _, _) in layers), x.device)
-    _check("q1_decode_chain", lib().q1_decode_chain(arr, len(layers), x2.data_ptr(), M, _DT[x.dtype],
+    _cuda(workspace, "workspace", x.device)
+    _check("q1_decode_chain", lib().q1_decode_chain(arr, len(layers), x2.data_ptr(), M, xdt,
                                                     y.data_ptr(), workspace.data_ptr(),
-                                                    workspace.numel(), _stream()))
+                                                    workspace.numel() * workspace.element_size(),
+                                                    _stream()))
     return y.reshape(*lead, D)
 
 
