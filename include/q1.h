@@ -18,7 +18,10 @@
  * Conventions for every call:
  *   - Pointers named d_* or documented as "device" are device pointers
  *     allocated by the caller (the library never allocates or frees device
- *     memory).  Arrays are row-major and contiguous.
+ *     memory).  Arrays are row-major and contiguous.  The library cannot tell
+ *     a host pointer, or an output array shorter than the call writes, from a
+ *     good one: passing either is undefined behaviour (the Python binding
+ *     checks both before it calls in).
  *   - Work is enqueued on `stream` (NULL = the legacy default stream) and the
  *     call returns without waiting, unless stated otherwise.
  *   - Arguments are validated on the host before anything is launched; an
@@ -160,8 +163,8 @@ q1_status q1_pack_from_dense(const void *dense, q1_dtype in_t, int64_t N, int64_
  *   ones rounded once at 2^-11; the activations enter as fp16 rows scaled by
  *   a power of two per row (kept in the workspace), which is exact for every
  *   activation whose scaled value is a normal fp16 number.
- * The narrow kernel covers K <= 40960 (a cluster of at most 8 CTAs, each with
- * 10 warps that own 512 k each): q1_qmv and q1_qmm_narrow return
+ * The narrow kernel covers K <= 40960 (a cluster of at most 8 CTAs, each
+ * holding at most 10 spans of 512 k): q1_qmv and q1_qmm_narrow return
  * Q1_ERR_SHAPE above it, and q1_qmm runs such K on the prefill path for any
  * M (workspace required). */
 q1_status q1_qmv(const q1_weight *W, const void *x, q1_dtype dtype, void *y, q1_stream stream);
