@@ -33,3 +33,24 @@ def test_decode_chain_bytes():
     w = 2 * 12_533_760 + 12_533_760 + 3_686_400
     act = 2 * (5120 + 5120) + 2 * (5120 + 17408) + 2 * (17408 + 5120)
     assert bench.chain_bytes(1) == 64 * (w + act)
+
+
+def test_reference_arm_prints_the_contract_line():
+    # the reference arm times the oracle on the host: one JSON line with the
+    # GPU arm's metric and unit, marked as the reference, warm-up of at least 3
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "0"],
+                         capture_output=True, text=True, cwd=root, check=True, timeout=300).stdout
+    lines = [ln for ln in out.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
+    assert d["steps"] == 1 and d["warmup"] >= 3 and d["n_gpus"] == 1
+    assert d["higher_is_better"] is True and d["config"]["workload"] == bench.WORKLOAD
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
