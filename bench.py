@@ -604,7 +604,7 @@ def reference_arm(args):
     el = time.perf_counter() - t0
     b = (weight_bytes(256, K, False) + K * 2 + 256 * 2) * args.steps
     v = b / el / 1e9
-    cores = os.cpu_count()
+    cores = int(os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1))
     line = {"metric": "Q1 QMV achieved HBM GB/s (% of 8 TB/s) at M=1..8; prefill QMM TFLOP/s",
             "value": round(v, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
@@ -641,6 +641,10 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
+        # numpy is not imported yet: fix the BLAS thread count to the host's
+        # cores, so that the line's `cores` is the count the oracle ran with
+        for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[var] = str(os.cpu_count() or 1)
         reference_arm(args)
     else:
         gpu_arm(args)
