@@ -76,7 +76,8 @@ def chain_bytes(M):
 class ClockSampler:
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+              "utilization.gpu")
 
     def __init__(self, index: int):
         self.index = index
@@ -108,24 +109,34 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
+        """Median SM clock over the samples taken under load (GPU utilization
+        >= 50 %; all samples if none is), the maximum clock, every throttle
+        reason seen active, and both sample counts."""
+        sm, mx, busy, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             p = [c.strip() for c in ln.split(",")]
-            if len(p) < 8:
+            if len(p) < 9:
                 continue
             try:
-                sm.append(float(p[0]))
-                mx.append(float(p[1]))
+                clk, cmax = float(p[0]), float(p[1])
             except ValueError:
                 continue
+            sm.append(clk)
+            mx.append(cmax)
+            try:
+                if float(p[8]) >= 50.0:
+                    busy.append(clk)
+            except ValueError:
+                pass
             for nm, v in zip(names, p[4:8]):
                 if v.lower() == "active":
                     reasons.add(nm)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "samples_under_load": 0}
+        return {"sm_mhz": statistics.median(busy or sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm), "samples_under_load": len(busy),
+                "sample_period_ms": 100}
 
 
 # ---------------------------------------------------------------------------
@@ -154,18 +165,21 @@ def cpu_worker(seconds: float):
 
 
 def cpu_baseline(seconds: float):
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
-               CUDA_VISIBLE_DEVICES="")
+    # the oracle on every host core: its BLAS thread count is fixed to the
+    # core count before numpy loads in the child, and the line reports it
+    cores = os.cpu_count() or 1
+    env = dict(os.environ, OMP_NUM_THREADS=str(cores), OPENBLAS_NUM_THREADS=str(cores),
+               MKL_NUM_THREADS=str(cores), CUDA_VISIBLE_DEVICES="")
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-worker", str(seconds)],
                        capture_output=True, text=True, env=env, timeout=600)
     if r.returncode != 0:
-        return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle",
+        return {"value": None, "unit": "GB/s", "cores": cores, "kind": "oracle",
                 "sample": f"failed: {r.stderr.strip()[-200:]}"}
     d = json.loads(r.stdout.strip().splitlines()[-1])
-    return {"value": d["bytes"] / d["seconds"] / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+    return {"value": d["bytes"] / d["seconds"] / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": (f"oracle QMV M=1 on {d['rows']} rows of a symmetric 17408x5120 gate matrix "
-                       f"(chunks of 256 rows, {d['seconds']:.1f} s, 1 thread); GB/s of the same "
-                       "algorithmic bytes per row as the GPU metric")}
+                       f"(chunks of 256 rows, {d['seconds']:.1f} s, BLAS on {cores} threads); GB/s of "
+                       "the same algorithmic bytes per row as the GPU metric")}
 
 
 # ---------------------------------------------------------------------------

@@ -116,13 +116,28 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
 
 # The library takes raw device pointers and cannot tell a host pointer, a
 # tensor on another GPU or a short output buffer from a good one: the kernels
-# would fault or write past the end.  These checks turn such calls into a
-# ValueError before anything is launched.
-def _cuda(t, name: str, device=None) -> torch.Tensor:
-    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+# would fault or write past the end.  It also launches on the CUDA device that
+# is current for the calling thread, with that device's current stream, so a
+# tensor on any other device would be handed to kernels of the wrong GPU.
+# These checks turn such calls into a ValueError before anything is launched.
+def _is_cuda(t: torch.Tensor) -> bool:
+    return t.is_cuda
+
+
+def _current_device() -> torch.device:
+    return torch.device("cuda", torch.cuda.current_device())
+
+
+def _cuda(t, name: str, device=None, current: bool = True) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor) or not _is_cuda(t):
         raise ValueError(f"{name} must be a CUDA tensor")
     if device is not None and t.device != device:
         raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if current:
+        cur = _current_device()
+        if t.device != cur:
+            raise ValueError(f"{name} is on {t.device} but the current CUDA device is {cur}: the library "
+                             f"launches on the current device (select it with torch.cuda.device)")
     return t
 
 
@@ -154,10 +169,10 @@ class Q1Weight:
 
     def __init__(self, words: torch.Tensor, scales: torch.Tensor,
                  biases: Optional[torch.Tensor], K: int):
-        _cuda(words, "Q1Weight words")
-        _cuda(scales, "Q1Weight scales", words.device)
+        _cuda(words, "Q1Weight words", current=False)
+        _cuda(scales, "Q1Weight scales", words.device, current=False)
         if biases is not None:
-            _cuda(biases, "Q1Weight biases", words.device)
+            _cuda(biases, "Q1Weight biases", words.device, current=False)
         if words.dtype not in (torch.int32, torch.uint32):
             raise ValueError(f"Q1Weight words must be int32 or uint32 (the packed words), got {words.dtype}")
         self.words = words.contiguous()
@@ -219,6 +234,7 @@ def unpack(words: torch.Tensor, K: int) -> torch.Tensor:
 
 
 def dequantize(W: Q1Weight, dtype=torch.bfloat16) -> torch.Tensor:
+    _cuda(W.words, "weight")
     if dtype not in _DT:
         raise ValueError(f"dtype must be bfloat16, float16 or float32 (got {dtype})")
     out = torch.empty((W.N, W.K), dtype=dtype, device=W.words.device)
@@ -299,6 +315,13 @@ def embed_gather(E: Q1Weight, ids: torch.Tensor, dtype=torch.bfloat16):
     return out, bad
 
 
+def _ffn_devices(gate: Q1Weight, up: Q1Weight, down: Q1Weight, x: torch.Tensor):
+    """x and all three matrices on one device, the current one."""
+    _cuda(x, "x", gate.words.device)
+    _cuda(up.words, "up", gate.words.device)
+    _cuda(down.words, "down", gate.words.device)
+
+
 def ffn_workspace(M: int, D: int, F: int, device) -> torch.Tensor:
     """A byte buffer of the size q1_ffn_fused needs (at least 256 B)."""
     n = lib().q1_ffn_workspace_size(M, D, F)
@@ -308,7 +331,7 @@ def ffn_workspace(M: int, D: int, F: int, device) -> torch.Tensor:
 def ffn_fused(gate: Q1Weight, up: Q1Weight, down: Q1Weight, x: torch.Tensor,
               workspace=None, out=None) -> torch.Tensor:
     """y = down . (SiLU(gate . x) * (up . x)); x [..., D] -> y [..., D]."""
-    _cuda(x, "x", gate.words.device)
+    _ffn_devices(gate, up, down, x)
     xdt = _x_dtype(x)
     lead = x.shape[:-1]
     x2 = _flat(x, gate.K)
@@ -326,7 +349,7 @@ def ffn_fused_noalloc(gate: Q1Weight, up: Q1Weight, down: Q1Weight, x: torch.Ten
                       out=None) -> torch.Tensor:
     """q1_ffn_fused with h in the library's fixed device array (no workspace,
     no allocation in the call; `out` may be preallocated too)."""
-    _cuda(x, "x", gate.words.device)
+    _ffn_devices(gate, up, down, x)
     xdt = _x_dtype(x)
     lead = x.shape[:-1]
     x2 = _flat(x, gate.K)
@@ -390,8 +413,8 @@ def decode_chain(layers, x: torch.Tensor, workspace=None, out=None) -> torch.Ten
     _cuda(x, "x", layers[0][0].words.device)
     xdt = _x_dtype(x)
     for li, lw in enumerate(layers):
-        for W in lw:
-            _cuda(W.words, f"layer {li} weights", x.device)
+        for name, W in zip(("attn", "gate", "up", "down"), lw):
+            _cuda(W.words, f"layer {li} {name}", x.device)
     lead = x.shape[:-1]
     D = layers[0][0].N
     x2 = _flat(x, D)
@@ -410,6 +433,7 @@ def decode_chain(layers, x: torch.Tensor, workspace=None, out=None) -> torch.Ten
 
 def check_symmetric(W: Q1Weight) -> torch.Tensor:
     """Device int32 [1]: 1 iff every stored bias is exactly -scale/2."""
+    _cuda(W.words, "weight")
     r = torch.empty((1,), dtype=torch.int32, device=W.words.device)
     _check("q1_check_symmetric", lib().q1_check_symmetric(W.cref(), r.data_ptr(), _stream()))
     return r

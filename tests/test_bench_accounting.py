@@ -54,3 +54,17 @@ def test_reference_arm_prints_the_contract_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_clock_summary_reports_the_median_under_load():
+    # nvidia-smi lines: sm, max sm, power, active mask, four reasons, utilization
+    s = bench.ClockSampler(0)
+    s.lines = ["345, 2070, 150.0, 0x0, Not Active, Not Active, Not Active, Not Active, 0",
+               "2070, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, Not Active, 100",
+               "2055, 2070, 950.0, 0x4, Not Active, Not Active, Not Active, Active, 99",
+               "2040, 2070, 980.0, 0x0, Not Active, Not Active, Not Active, Not Active, 100",
+               "garbage"]
+    d = s.summary()
+    assert d["samples"] == 4 and d["samples_under_load"] == 3
+    assert d["sm_mhz"] == 2055 and d["sm_max_mhz"] == 2070
+    assert d["reasons"] == ["sw_power_cap"]

@@ -93,3 +93,57 @@ def test_activation_dtype_and_shape_rules(no_library, monkeypatch):
         q1.unpack(torch.zeros((4, 3), dtype=torch.int32), 64)
     with pytest.raises(ValueError, match="uint8"):
         q1.pack(torch.zeros((4, 64), dtype=torch.int32))
+
+
+def _pretend_cuda(monkeypatch, current):
+    """Every tensor passes the is-CUDA test and `current` is the thread's CUDA
+    device; tensors keep their real device, so a CPU tensor reads as a tensor
+    on a device other than `current`."""
+    monkeypatch.setattr(q1, "_is_cuda", lambda t: True)
+    monkeypatch.setattr(q1, "_current_device", lambda: current)
+
+
+@pytest.mark.parametrize("call", [
+    lambda W, x: q1.qmv(W, x[0]),
+    lambda W, x: q1.qmm_narrow(W, x),
+    lambda W, x: q1.qmm(W, x),
+    lambda W, x: q1.ffn_fused(W, W, W, x),
+    lambda W, x: q1.ffn_fused_noalloc(W, W, W, x),
+    lambda W, x: q1.decode_chain([(W, W, W, W)], x),
+    lambda W, x: q1.dequantize(W),
+    lambda W, x: q1.check_symmetric(W),
+    lambda W, x: q1.embed_gather(W, torch.zeros((3,), dtype=torch.int32)),
+])
+def test_calls_refuse_tensors_off_the_current_device(no_library, monkeypatch, call):
+    # the library launches on the current device: weights and activations on
+    # another GPU must be refused before anything reaches it
+    _pretend_cuda(monkeypatch, torch.device("cuda", 0))
+    W = _fake_weight()
+    x = torch.zeros((2, W.K), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="current CUDA device"):
+        call(W, x)
+
+
+@pytest.mark.parametrize("which", ["up", "down"])
+@pytest.mark.parametrize("noalloc", [False, True])
+def test_ffn_refuses_a_matrix_on_another_device(no_library, monkeypatch, which, noalloc):
+    _pretend_cuda(monkeypatch, torch.device("cpu"))
+    G, U, D = _fake_weight(), _fake_weight(), _fake_weight()
+    # one matrix on another device (the meta device stands in for another GPU)
+    odd = U if which == "up" else D
+    odd.words = torch.zeros(odd.words.shape, dtype=torch.int32, device="meta")
+    x = torch.zeros((2, G.K), dtype=torch.bfloat16)
+    fn = q1.ffn_fused_noalloc if noalloc else q1.ffn_fused
+    with pytest.raises(ValueError, match=f"{which} is on meta"):
+        fn(G, U, D, x)
+
+
+@pytest.mark.parametrize("which", ["attn", "gate", "up", "down"])
+def test_decode_chain_refuses_a_layer_matrix_on_another_device(no_library, monkeypatch, which):
+    _pretend_cuda(monkeypatch, torch.device("cpu"))
+    layer = {n: _fake_weight() for n in ("attn", "gate", "up", "down")}
+    layer[which].words = torch.zeros(layer[which].words.shape, dtype=torch.int32, device="meta")
+    x = torch.zeros((1, 256), dtype=torch.bfloat16)
+    ok = tuple(_fake_weight() for _ in range(4))
+    with pytest.raises(ValueError, match=f"layer 1 {which} is on meta"):
+        q1.decode_chain([ok, tuple(layer[n] for n in ("attn", "gate", "up", "down"))], x)

@@ -135,3 +135,24 @@ def test_ffn_full_shape(q1, M):
     assert np.linalg.norm(h - ho) / np.linalg.norm(ho) < 5e-3
     check_matmul(y[:, rows], yo, ho, O.dequantize_f32(down.words[rows], down.scales[rows], None, D_FF),
                  f"ffn M={M}")
+
+
+def test_ffn_full_shape_all_affine(q1):
+    # the 27B-class FFN with stored biases on all three matrices, M = 4; the
+    # down product's output includes its own bf16 rounding in the bar
+    # (tests/tolerance.py: outputs dominated by group means times sums of h)
+    M = 4
+    gate = synth.q1_tensor(D_FF, D_MODEL, seed=2011, affine=True)
+    up = synth.q1_tensor(D_FF, D_MODEL, seed=2012, affine=True)
+    down = synth.q1_tensor(D_MODEL, D_FF, seed=2013, affine=True)
+    x = synth.activations(M, D_MODEL, seed=2014)
+    G, U, Dn = (q1.Q1Weight.from_host(w) for w in (gate, up, down))
+    ws = q1.ffn_workspace(M, D_MODEL, D_FF, DEV)
+    y = q1.ffn_fused(G, U, Dn, x.to(DEV), workspace=ws).float().cpu().double().numpy()
+    rows = _rows(D_MODEL, 128, 2015)
+    yo, ho = O.ffn(x, (gate.words, gate.scales, gate.biases, D_MODEL), (up.words, up.scales, up.biases, D_MODEL),
+                   (down.words, down.scales, down.biases, D_FF), rows=rows)
+    h = q1.ffn_h(ws, M, D_FF).float().cpu().double().numpy()
+    assert np.linalg.norm(h - ho) / np.linalg.norm(ho) < 5e-3
+    check_matmul(y[:, rows], yo, ho, O.dequantize_f32(down.words[rows], down.scales[rows], down.biases[rows], D_FF),
+                 "affine ffn full shape", rounded_to="bf16")

@@ -127,8 +127,8 @@ def test_qmv_and_leading_dims(q1):
 @pytest.mark.parametrize("N,K", [(333, 4096), (1000, 5120)])
 @pytest.mark.parametrize("affine", [False, True])
 def test_qmm_narrow_many_spans(q1, N, K, affine):
-    # K with at least 16 spans of two groups: the 2-group-span kernel (up to
-    # 20 warps per CTA, the tile issue inside warp 0), ragged row tiles
+    # K of 8 and 10 spans of 512 k: every consumer warp owns a span and, with
+    # 10 spans, one group of the last two; ragged row tiles
     for M in (1, 3, 8):
         t, x = _case(N, K, M, affine, seed=N + K + 7 * M)
         W = q1.Q1Weight.from_host(t)
@@ -320,6 +320,32 @@ def test_ffn_fused(q1, M, D, F):
     h = q1.ffn_h(ws, M, F).float().cpu().double().numpy()
     assert np.linalg.norm(h - ho) / np.linalg.norm(ho) < 5e-3
     check_matmul(y, yo, ho, O.dequantize_f32(down.words, down.scales, None, F), f"ffn M={M}")
+
+
+_NAME = {torch.bfloat16: "bf16", torch.float16: "f16", torch.float32: "f32"}
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])
+@pytest.mark.parametrize("M", [1, 4, 8])
+def test_ffn_fused_all_affine(q1, M, dtype):
+    # gate, up and down all with stored biases: the down product's output is
+    # dominated by the group means times sums of h, so the bar includes the
+    # output's own rounding (tests/tolerance.py)
+    D, F = 512, 1408
+    gate = synth.q1_tensor(F, D, seed=311, affine=True)
+    up = synth.q1_tensor(F, D, seed=312, affine=True)
+    down = synth.q1_tensor(D, F, seed=313, affine=True)
+    x = _acts(M, D, 314 + M, dtype) if dtype != torch.bfloat16 else synth.activations(M, D, seed=314 + M)
+    G, U, Dn = (q1.Q1Weight.from_host(w) for w in (gate, up, down))
+    ws = q1.ffn_workspace(M, D, F, DEV)
+    y = q1.ffn_fused(G, U, Dn, x.to(DEV), workspace=ws)
+    assert y.dtype == dtype
+    tup = lambda t, K: (t.words, t.scales, t.biases, K)
+    yo, ho = O.ffn(x, tup(gate, D), tup(up, D), tup(down, F))
+    h = q1.ffn_h(ws, M, F).float().cpu().double().numpy()
+    assert np.linalg.norm(h - ho) / np.linalg.norm(ho) < 5e-3
+    check_matmul(y, yo, ho, O.dequantize_f32(down.words, down.scales, down.biases, F),
+                 f"affine ffn M={M} {dtype}", rounded_to=_NAME[dtype])
 
 
 # ------------------------------------------------------------------ bf16 metadata
@@ -562,15 +588,15 @@ def _scaled(t, factor):
     return synth.Q1Tensor(t.words, s, b, t.K)
 
 
-def _chain_host(D, Fs, seed, affine=()):
+def _chain_host(D, Fs, seed, affine=(), factor=7.0):
     layers = []
     for l, F in enumerate(Fs):
         base = seed + 10 * l
         layers.append((
-            _scaled(synth.q1_tensor(D, D, seed=base, affine=("attn", l) in affine), 7.0),
-            _scaled(synth.q1_tensor(F, D, seed=base + 1, affine=("gate", l) in affine), 7.0),
-            _scaled(synth.q1_tensor(F, D, seed=base + 2, affine=("up", l) in affine), 7.0),
-            _scaled(synth.q1_tensor(D, F, seed=base + 3, affine=("down", l) in affine), 7.0)))
+            _scaled(synth.q1_tensor(D, D, seed=base, affine=("attn", l) in affine), factor),
+            _scaled(synth.q1_tensor(F, D, seed=base + 1, affine=("gate", l) in affine), factor),
+            _scaled(synth.q1_tensor(F, D, seed=base + 2, affine=("up", l) in affine), factor),
+            _scaled(synth.q1_tensor(D, F, seed=base + 3, affine=("down", l) in affine), factor)))
     return layers
 
 
@@ -607,6 +633,41 @@ def test_decode_chain_oracle(q1, M):
     _, h_last = O.ffn(a, gate, up, down)
     wd = O.dequantize_f32(down[0], down[1], down[2], down[3])
     check_chain(y, yo.double().numpy(), h_last, wd, stages=3 * len(layers), what=f"chain M={M}")
+
+
+@pytest.mark.parametrize("M", [1, 4])
+def test_decode_chain_affine_layers_stage_by_stage(q1, M):
+    # every matrix of both layers affine.  The chain equals the same calls
+    # made one by one, bit for bit; each of those calls is then held to the
+    # single-product bar against the oracle computed from the GPU's own bf16
+    # input to it (the attention product and the whole FFN block)
+    D, Fs = 256, [512, 384]
+    every = {(n, l) for n in ("attn", "gate", "up", "down") for l in range(len(Fs))}
+    # metadata x2: with stored biases the group means make the activations
+    # grow from layer to layer, and x7 (the symmetric tests' factor) would
+    # overflow bf16 by the second layer
+    host = _chain_host(D, Fs, seed=470, affine=every, factor=2.0)
+    dev = [tuple(q1.Q1Weight.from_host(w) for w in L) for L in host]
+    x = synth.activations(M, D, seed=479)
+    y = q1.decode_chain(dev, x.to(DEV))
+    tup = lambda t: (t.words, t.scales, t.biases, t.K)
+    h = x.to(DEV)
+    for l, ((A, G, U, Dn), (ta, tg, tu, td)) in enumerate(zip(dev, host)):
+        a = q1.qmm_narrow(A, h)
+        h_in = h.cpu()
+        check_matmul(a, O.qmm(h_in, *tup(ta)), h_in, O.dequantize_f32(ta.words, ta.scales, ta.biases, D),
+                     f"chain layer {l} attn M={M}", rounded_to="bf16")
+        ws = q1.ffn_workspace(M, D, Fs[l], DEV)
+        h = q1.ffn_fused(G, U, Dn, a, workspace=ws)
+        a_in = a.cpu()
+        yo, ho = O.ffn(a_in, tup(tg), tup(tu), tup(td))
+        hg = q1.ffn_h(ws, M, Fs[l]).float().cpu().double().numpy()
+        assert np.linalg.norm(hg - ho) / np.linalg.norm(ho) < 5e-3, f"layer {l} h"
+        check_matmul(h, yo, ho, O.dequantize_f32(td.words, td.scales, td.biases, Fs[l]),
+                     f"chain layer {l} ffn M={M}", rounded_to="bf16")
+    torch.cuda.synchronize()
+    assert torch.equal(y, h), "the chain differs from the same calls made one by one"
+    assert float(y.float().abs().max()) > 0
 
 
 def test_decode_chain_rejects_bad_arguments(q1):
@@ -664,6 +725,46 @@ def test_check_symmetric_tail_and_unaligned_metadata(q1):
         Wu = q1.Q1Weight(W.words, sd, bd, K)
         assert Wu.scales.data_ptr() % 16 != 0
         assert int(q1.check_symmetric(Wu).item()) == want
+
+
+def _f16(bits):
+    return np.array([bits], dtype=np.uint16).view(np.float16)[0]
+
+
+@pytest.mark.parametrize("unaligned", [False, True])
+@pytest.mark.parametrize("case", ["pm_zero", "nan_scale", "nan_bias", "tiny_scale", "neg_zero_scale"])
+def test_check_symmetric_edge_cases(q1, case, unaligned):
+    # the cases the oracle's is_symmetric is pinned on, run through the
+    # kernel's 16-byte vector path (aligned metadata, 8 groups per load) and
+    # its element-wise path (metadata 2 bytes past a 16-byte boundary)
+    N, K = 5, 1024  # 8 groups per row
+    t = synth.q1_tensor(N, K, seed=711, affine=False)
+    s = np.maximum(t.scales, np.float16(2.0 ** -13))
+    b = (-(s.astype(np.float32) / 2)).astype(np.float16)
+    r, g = 3, 6
+    if case == "pm_zero":        # scale +0 with bias +0 (derived -0): equal
+        s[r, g], b[r, g] = np.float16(0.0), np.float16(0.0)
+        s[r, g + 1], b[r, g + 1] = np.float16(-0.0), np.float16(-0.0)  # derived +0 vs -0
+    elif case == "neg_zero_scale":  # scale -0, bias -0 stored: derived +0 == -0
+        s[r, g], b[r, g] = np.float16(-0.0), np.float16(-0.0)
+    elif case == "nan_scale":
+        s[r, g] = np.float16(np.nan)
+    elif case == "nan_bias":
+        b[r, g] = np.float16(np.nan)
+    elif case == "tiny_scale":   # -s/2 is not an fp16 value: no stored bias equals it
+        s[r, g] = _f16(0x0001)
+        b[r, g] = (-(s[r, g].astype(np.float32) / 2)).astype(np.float16)
+    want = int(O.is_symmetric(s, b))
+    assert want == (1 if case in ("pm_zero", "neg_zero_scale") else 0)
+    if unaligned:
+        sd = torch.from_numpy(np.concatenate([[np.float16(1)], s.reshape(-1)])).to(DEV)[1:].reshape(N, K // 128)
+        bd = torch.from_numpy(np.concatenate([[np.float16(1)], b.reshape(-1)])).to(DEV)[1:].reshape(N, K // 128)
+        W = q1.Q1Weight(torch.from_numpy(t.words.view("<i4").copy()).to(DEV), sd, bd, K)
+        assert W.scales.data_ptr() % 16 != 0
+    else:
+        W = q1.Q1Weight.from_host(synth.Q1Tensor(t.words, s, b, K))
+        assert W.scales.data_ptr() % 16 == 0 and W.biases.data_ptr() % 16 == 0
+    assert int(q1.check_symmetric(W).item()) == want
 
 
 def test_no_device_errors_after_suite(q1):

@@ -499,3 +499,23 @@ def test_storage_bytes_bias_is_one_sixty_fourth_byte_per_weight():
     # 1.125 bits per weight symmetric, 1.25 affine
     assert sym["total"] * 8 / (17408 * 5120) == pytest.approx(1.125)
     assert st["total"] * 8 / (17408 * 5120) == pytest.approx(1.25)
+
+
+# ---------------------------------------------------------------- tolerance helper
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+def test_half_ulp_covers_one_rounding_and_is_tight(dtype):
+    # the output-rounding term of the matmul bar: rounding any value once to
+    # the dtype moves it by at most half_ulp, and half_ulp is not loose by
+    # more than a factor of two (a value half-way between two neighbours moves
+    # by exactly half an ulp)
+    from tests.tolerance import half_ulp
+    rng = np.random.default_rng(5)
+    top = 14 if dtype == "f16" else 20  # within fp16's range
+    y = rng.standard_normal(20000) * np.exp2(rng.integers(-20, top, 20000))
+    y = np.concatenate([y, [1.0 - 2.0 ** -12, 255.9, -3.0, 1e-6]])
+    r = O.round_to(y, dtype).double().numpy()
+    err = np.abs(r - y.astype(np.float32).astype(np.float64))
+    h = half_ulp(y, dtype)
+    assert np.all(err <= h)
+    one = O.round_to(np.array([1.0]), dtype).double().numpy()
+    assert half_ulp(one, dtype)[0] == {"bf16": 2.0 ** -8, "f16": 2.0 ** -11, "f32": 2.0 ** -24}[dtype]
