@@ -161,6 +161,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t *>(&h);
 }
+// One of the two fp16 or bf16 metadata values packed in `pair` (hi: the upper
+// one) widened to fp32, exactly.  For fp16 this is the FMA pipe's half-to-float
+// conversion reading the chosen half in place (no shift on the integer pipe,
+// which the unpack keeps busy).
+__device__ __forceinline__ float meta_half_f32(uint32_t pair, int hi, bool bf16) {
+  if (bf16) return __uint_as_float(hi ? (pair & 0xFFFF0000u) : (pair << 16));
+  const __half2 h2 = *reinterpret_cast<const __half2 *>(&pair);
+  return hi ? __high2float(h2) : __low2float(h2);
+}
+
 // one output value in the activation dtype (one rounding for 16-bit types)
 __device__ __forceinline__ void store_act(void *out, size_t i, float v, int dt) {
   if (dt == Q1_F32) static_cast<float *>(out)[i] = v;
@@ -578,11 +588,13 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
             xbb = lds16(mb + xm + 24 * MROW);
           }
         }
+        // the words shifted right by 8, as the high half of a multiply by 2^24:
+        // a multiply-add pipe instruction instead of an integer-pipe shift
         uint32_t wa8[NG], wb8[NG];
 #pragma unroll
         for (int u = 0; u < NG; ++u) {
-          wa8[u] = wa[u] >> 8;
-          wb8[u] = wb[u] >> 8;
+          wa8[u] = __umulhi(wa[u], 0x01000000u);
+          wb8[u] = __umulhi(wb[u], 0x01000000u);
         }
         // independent chains (one per group), interleaved step by step
         float d[NG][4];
@@ -602,10 +614,8 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
         const bool mbf = VAR >= 1 && ((a.meta_bf16 >> ((NMAT == 2 && ((rb + lt) & 1)) ? 1 : 0)) & 1) != 0;
 #pragma unroll
         for (int u = 0; u < NG; ++u) {
-          const uint32_t hs_a = u < kQuad ? (u < 2 ? sa.x : sa.y) >> (16 * (u & 1)) : xsa;
-          const uint32_t hs_b = u < kQuad ? (u < 2 ? sb.x : sb.y) >> (16 * (u & 1)) : xsb;
-          const float s_a = meta_f32(hs_a, mbf);
-          const float s_b = meta_f32(hs_b, mbf);
+          const float s_a = u < kQuad ? meta_half_f32(u < 2 ? sa.x : sa.y, u & 1, mbf) : meta_half_f32(xsa, 0, mbf);
+          const float s_b = u < kQuad ? meta_half_f32(u < 2 ? sb.x : sb.y, u & 1, mbf) : meta_half_f32(xsb, 0, mbf);
           if (u == 0) {
             acc[0] = s_a * d[u][0]; acc[1] = s_a * d[u][1]; acc[2] = s_b * d[u][2]; acc[3] = s_b * d[u][3];
           } else {
@@ -615,8 +625,8 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
           if (AFFINE) {
             float b_a, b_b;
             if (has_b) {
-              b_a = meta_f32(u < kQuad ? (u < 2 ? ba.x : ba.y) >> (16 * (u & 1)) : xba, mbf);
-              b_b = meta_f32(u < kQuad ? (u < 2 ? bb.x : bb.y) >> (16 * (u & 1)) : xbb, mbf);
+              b_a = u < kQuad ? meta_half_f32(u < 2 ? ba.x : ba.y, u & 1, mbf) : meta_half_f32(xba, 0, mbf);
+              b_b = u < kQuad ? meta_half_f32(u < 2 ? bb.x : bb.y, u & 1, mbf) : meta_half_f32(xbb, 0, mbf);
             } else {  // matrix without stored biases: symmetric
               b_a = __fmul_rn(-0.5f, s_a);
               b_b = __fmul_rn(-0.5f, s_b);
@@ -652,11 +662,13 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
     consumer_sync(nthreads);
 
     // ---- combine the spans' partials of each output, in span order
+    // the token index runs fastest: consecutive threads read consecutive
+    // words of a partial row (no bank conflicts at M = 8)
     const int npairs = trc / NMAT;
     if (KS == 1) {
       const int cnt = npairs * 16 * M;
       for (int i = tid; i < cnt; i += nthreads) {
-        const int r = i & 15, lp = (i >> 4) % npairs, m = (i >> 4) / npairs;
+        const int m = i % M, r = (i / M) & 15, lp = (i / M) >> 4;
         const int lt = lp * NMAT;
         const int64_t n = (int64_t)((rb + lt) / NMAT) * 16 + r;
         // unrolled to the most K-warps a CTA holds, so that the loads need
@@ -695,7 +707,7 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
       const int lo = min(npairs, rank * per), hi = min(npairs, lo + per);
       const int cnt2 = (hi - lo) * 16 * M;
       for (int i = tid; i < cnt2; i += nthreads) {
-        const int r = i & 15, lp = lo + (i >> 4) % (hi - lo), m = (i >> 4) / (hi - lo);
+        const int m = i % M, r = (i / M) & 15, lp = lo + ((i / M) >> 4);
         const int lt = lp * NMAT;
         const int64_t n = (int64_t)((rb + lt) / NMAT) * 16 + r;
         // every rank's value is requested before the first one is added: the
