@@ -82,7 +82,7 @@ const char *q1_status_string(q1_status s) {
     case Q1_ERR_SHAPE: return "invalid shape (need N>=1, K>=128, K%128==0, M in range)";
     case Q1_ERR_ALIGN: return "pointer misaligned (packed words, x, y, out: 16 bytes)";
     case Q1_ERR_DTYPE: return "unsupported dtype for this call";
-    case Q1_ERR_GROUP: return "group_size must be 32, 64 or 128 (128 for the narrow-only calls)";
+    case Q1_ERR_GROUP: return "group_size must be 32, 64 or 128 (gate and up of one FFN: the same)";
     case Q1_ERR_WORKSPACE: return "workspace missing, too small or not 256-byte aligned";
     case Q1_ERR_CUDA: return "CUDA runtime error";
     case Q1_ERR_TIMEOUT: return "a bounded device-side wait ran out";
@@ -126,7 +126,6 @@ q1_status q1_dequantize(const q1_weight *W, q1_dtype out_t, void *out, q1_stream
 q1_status q1_qmv(const q1_weight *W, const void *x, q1_dtype dtype, void *y, q1_stream stream) {
   q1_status s = matmul_common(W, x, 1, dtype, y);
   if (s != Q1_OK) return s;
-  if (W->group_size != 128) return Q1_ERR_GROUP;
   if (W->K > q1::kNarrowMaxK) return Q1_ERR_SHAPE;
   return cuda_status(q1::launch_narrow(q1::view(W), x, 1, y, (cudaStream_t)stream, true, dtype, dtype));
 }
@@ -135,7 +134,6 @@ q1_status q1_qmm_narrow(const q1_weight *W, const void *x, int64_t M, q1_dtype d
                         q1_stream stream) {
   q1_status s = matmul_common(W, x, M, dtype, y);
   if (s != Q1_OK) return s;
-  if (W->group_size != 128) return Q1_ERR_GROUP;
   if (M > q1::kNarrowMaxM || W->K > q1::kNarrowMaxK) return Q1_ERR_SHAPE;
   return cuda_status(q1::launch_narrow(q1::view(W), x, M, y, (cudaStream_t)stream, true, dtype, dtype));
 }
@@ -150,7 +148,7 @@ q1_status q1_qmm(const q1_weight *W, const void *x, int64_t M, q1_dtype dtype, v
                  void *workspace, size_t workspace_bytes, q1_stream stream) {
   q1_status s = matmul_common(W, x, M, dtype, y);
   if (s != Q1_OK) return s;
-  if (M <= g_max_rows.load() && W->K <= q1::kNarrowMaxK && W->group_size == 128)
+  if (M <= g_max_rows.load() && W->K <= q1::kNarrowMaxK)
     return cuda_status(q1::launch_narrow(q1::view(W), x, M, y, (cudaStream_t)stream, true, dtype, dtype));
   s = check_ws(workspace, workspace_bytes, q1::wide_workspace_bytes(M, W->K));
   if (s != Q1_OK) return s;
@@ -186,7 +184,8 @@ q1_status q1_ffn_fused(const q1_weight *gate, const q1_weight *up, const q1_weig
   if ((s = check_weight(gate)) != Q1_OK || (s = check_weight(up)) != Q1_OK ||
       (s = check_weight(down)) != Q1_OK)
     return s;
-  if (gate->group_size != 128 || up->group_size != 128 || down->group_size != 128) return Q1_ERR_GROUP;
+  // gate and up run in one launch with one group size; down may differ
+  if (gate->group_size != up->group_size) return Q1_ERR_GROUP;
   if (!x || !y) return Q1_ERR_NULL;
   if (dtype != Q1_BF16 && dtype != Q1_F16 && dtype != Q1_F32) return Q1_ERR_DTYPE;
   if (M < 1 || M > q1::kNarrowMaxM) return Q1_ERR_SHAPE;
@@ -228,9 +227,7 @@ q1_status q1_decode_chain(const q1_decode_layer *layers, int32_t n_layers, const
     if ((s = check_weight(&L.attn)) != Q1_OK || (s = check_weight(&L.gate)) != Q1_OK ||
         (s = check_weight(&L.up)) != Q1_OK || (s = check_weight(&L.down)) != Q1_OK)
       return s;
-    if (L.attn.group_size != 128 || L.gate.group_size != 128 || L.up.group_size != 128 ||
-        L.down.group_size != 128)
-      return Q1_ERR_GROUP;
+    if (L.gate.group_size != L.up.group_size) return Q1_ERR_GROUP;
     const int64_t F = L.gate.N;
     if (L.attn.N != D || L.attn.K != D || L.gate.K != D || L.up.K != D || L.up.N != F ||
         L.down.K != F || L.down.N != D)

@@ -161,6 +161,27 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t *>(&h);
 }
+// Two weights (bits q and q+16 of `src`) -> bf16x2 with base 1.0, the mask in
+// a register (the small-group mapping's masks depend on the lane).
+__device__ __forceinline__ uint32_t selr(uint32_t src, uint32_t mask, uint32_t base) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xE2;" : "=r"(r) : "r"(src), "r"(mask), "r"(base));
+  return r;
+}
+// activations i, i+1 of x (dtype xdt) as bf16x2, rounded once for fp16/fp32
+__device__ __forceinline__ uint32_t x_pair(const void *x, int xdt, size_t i) {
+  if (xdt == Q1_F32) {
+    const float2 v = __ldg(reinterpret_cast<const float2 *>(static_cast<const float *>(x) + i));
+    return pack_bf16x2(v.x, v.y);
+  }
+  const uint32_t v = __ldg(reinterpret_cast<const unsigned int *>(static_cast<const uint16_t *>(x) + i));
+  if (xdt == Q1_F16) {
+    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&v));
+    return pack_bf16x2(f.x, f.y);
+  }
+  return v;
+}
+
 // One of the two fp16 or bf16 metadata values packed in `pair` (hi: the upper
 // one) widened to fp32, exactly.  For fp16 this is the FMA pipe's half-to-float
 // conversion reading the chosen half in place (no shift on the integer pipe,
@@ -189,6 +210,11 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
 __device__ __forceinline__ uint32_t lds16(uint32_t addr) {
   unsigned short v;
   asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ float4 lds128f(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
   return v;
 }
 __device__ __forceinline__ uint2 lds64(uint32_t addr) {
@@ -238,24 +264,32 @@ struct Geo {
 };
 
 // metadata row of a slot: the groups of spans (q_lo & ~1) .. q_lo + qm, in
-// whole boxes of 8 groups
-__host__ __device__ inline int meta_groups(int qm) { return (4 * (qm + 1) + 7) / 8 * 8; }
+// whole boxes of 8 groups; gps = groups per span of 512 k (4 for groups of
+// 128 weights, 8 for 64, 16 for 32)
+__host__ __device__ inline int meta_groups(int qm, int gps = 4) { return (gps * (qm + 1) + 7) / 8 * 8; }
+
+// Warps that hold 5 groups of 128 k, the most any warp holds (kwarps).
+constexpr int kMaxUnits = 5;
 
 struct SmemLayout {
-  int ring, meta, bars, part, red, total;
+  int ring, meta, bars, part, red, seeds, total;
   int slot_words, slot_meta;  // bytes per ring slot
 };
 
-__host__ __device__ inline SmemLayout smem_layout(const Geo &g, bool affine) {
+// gw: words of 32 weights per metadata group (4, 2 or 1).  Groups of 64 or 32
+// weights keep their accumulator seeds in shared memory: per consumer warp,
+// unit of 128 k and group, a float4 for each of the quad's four lanes.
+__host__ __device__ inline SmemLayout smem_layout(const Geo &g, bool affine, int gw = 4) {
   SmemLayout L;
   L.slot_words = g.qm * kTileBytes;
-  L.slot_meta = align_up(16 * meta_groups(g.qm) * 2 * (affine ? 2 : 1), 128);
+  L.slot_meta = align_up(16 * meta_groups(g.qm, 16 / gw) * 2 * (affine ? 2 : 1), 128);
   int off = 0;
   L.ring = off; off += g.ring * L.slot_words;
   L.meta = off; off += g.ring * L.slot_meta;
   L.bars = off; off += align_up(2 * g.ring * 8, 128);
   L.part = off; off += g.tr * kwarps(g.qm) * 16 * (g.mst < 2 ? 2 : g.mst) * 4;
   L.red = off; off += g.ks > 1 ? g.tr * 16 * (g.mst < 2 ? 2 : g.mst) * 4 : 0;
+  L.seeds = off; off += gw < 4 ? kwarps(g.qm) * g.R * kMaxUnits * (4 / gw) * 64 : 0;
   L.total = off + 1024;  // slack for aligning the dynamic shared memory base
   return L;
 }
@@ -314,24 +348,36 @@ __device__ __forceinline__ void consumer_sync(int nthreads) {
 // the producer's lanes load them (zero past K) and store them before their
 // arrivals.  Either way a slot's metadata is [16 rows][meta_groups] fp16
 // starting at group 4 (q_lo & ~1).
-template <int NMAT, bool AFFINE, bool FASTMETA, int VAR>
+// GW: words of 32 weights per metadata group, 4 (groups of 128), 2 (64) or 1
+// (32).  With 4 every m16n8k16 step of a lane pairs word t of its group with
+// the other lanes' words, so one step spans a whole group.  With 2 or 1 a step
+// must stay within one group: the quad's four lanes then take different bit
+// pairs of one word (lane t the pairs 2t and 2t + 1 of each half), which
+// closes a chain of MMAs on every group; the group's accumulator seeds (C_g
+// or E_g, and Sx_g) go to a shared-memory table, since a warp holds up to 20
+// groups.
+template <int NMAT, bool AFFINE, bool FASTMETA, int VAR, int GW>
 __global__ void __launch_bounds__(kMaxThreads, 1)
 narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
+  static_assert(GW == 4 || GW == 2 || GW == 1, "words per metadata group");
+  constexpr int GPS = 16 / GW;  // metadata groups per span of 512 k
+  constexpr int GPU = 4 / GW;   // metadata groups per unit of 128 k
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // TMA with the 64-byte swizzle wants 512-byte aligned boxes: align the base
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   cg::cluster_group cluster = cg::this_cluster();
 
-  const int M = a.M, K = a.K, G = K / 128;
+  const int M = a.M, K = a.K, G = K / 128;  // G: units of 128 k
+  const int GM = K / (32 * GW);               // metadata groups per row
   const int64_t N = a.N;
   const Geo geo = a.geo;
   const int KS = geo.ks, RING = geo.ring, QM = geo.qm, R = geo.R, TR = geo.tr;
   const int MST = geo.mst < 2 ? 2 : geo.mst;  // tokens stored per partial row (a lane stores a pair)
-  const SmemLayout L = smem_layout(geo, AFFINE);
+  const SmemLayout L = smem_layout(geo, AFFINE, GW);
   const int NWM = kwarps(QM);               // K-warps of the widest slice
   const int NC = NWM * R;                   // consumer warps
-  const int MROW = meta_groups(QM) * 2;     // bytes per metadata row
+  const int MROW = meta_groups(QM, GPS) * 2;  // bytes per metadata row
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, t = lane & 3;
@@ -399,23 +445,26 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
           for (int qs = 0; qs < QS; ++qs) tma_2d(wdst + qs * kTileBytes, wm, (q_lo + qs) * 16, rt * 16, fb);
         }
         if (FASTMETA) {
-          tma_2d(mdst, mat ? &maps.s[1] : &maps.s[0], q_base * kQuad, rt * 16, fb);
-          if (has_b) tma_2d(mdst + 16 * MROW, mat ? &maps.b[1] : &maps.b[0], q_base * kQuad, rt * 16, fb);
+          tma_2d(mdst, mat ? &maps.s[1] : &maps.s[0], q_base * GPS, rt * 16, fb);
+          if (has_b) tma_2d(mdst + 16 * MROW, mat ? &maps.b[1] : &maps.b[0], q_base * GPS, rt * 16, fb);
         }
       }
       if (!FASTMETA) {
         const uint16_t *sp = mat ? a.s[1] : a.s[0];
         const uint16_t *bp = mat ? a.b[1] : a.b[0];
-        for (int e = lane; e < 16 * QS * (has_b ? 2 : 1); e += 32) {
-          const int r = e & 15, qs = (e >> 4) % QS, isb = (e >> 4) / QS;
+        // runs of 4 metadata values: (row, span, run) per lane, GPS / 4 runs per span
+        constexpr int RUNS = GPS / 4;
+        for (int e = lane; e < 16 * QS * RUNS * (has_b ? 2 : 1); e += 32) {
+          const int r = e & 15, c = (e >> 4) % RUNS, qs = (e >> 4) / RUNS % QS, isb = (e >> 4) / RUNS / QS;
           const int64_t row = (int64_t)rt * 16 + r;
           const int s = q_lo + qs;
-          const uint16_t *src = (isb ? bp : sp) + row * G + s * kQuad;
-          uint32_t h[kQuad];
+          const int g0 = s * GPS + 4 * c;
+          const uint16_t *src = (isb ? bp : sp) + row * GM + g0;
+          uint32_t h[4];
 #pragma unroll
-          for (int u = 0; u < kQuad; ++u) h[u] = (row < N && s * kQuad + u < G) ? (uint32_t)__ldg(src + u) : 0u;
+          for (int u = 0; u < 4; ++u) h[u] = (row < N && g0 + u < GM) ? (uint32_t)__ldg(src + u) : 0u;
           asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(mdst + isb * 16 * MROW + r * MROW +
-                                                              (s - q_base) * 8),
+                                                              ((s - q_base) * GPS + 4 * c) * 2),
                        "r"(h[0] | (h[1] << 16)), "r"(h[2] | (h[3] << 16))
                        : "memory");
         }
@@ -469,7 +518,56 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
   uint32_t bfr[NG][16];
   float seed[NG][4];
   float sx[NG][2];
-  if (active) {
+  // the small-group mapping's lane constants: bit pairs q0 = 2t, q1 = 2t + 1
+  // of each half of a word, their masks, 1/d, and the C/E chains' a and d/2
+  const uint32_t m0 = 0x00010001u << (2 * t), m1 = 0x00010001u << (2 * t + 1);
+  const uint32_t seeds_s = smem_u32(smem + L.seeds) + (uint32_t)(warp * kMaxUnits * GPU * 64 + 16 * t);
+  if (active && GW < 4) {
+    const uint32_t id0 = inv_d_bits(2 * t), id1 = inv_d_bits(2 * t + 1);
+    // word w, half j of unit u: lanes take k = 8j + 2t (+1) and k + 16 (+1)
+    uint32_t xl[NG][8], xh[NG][8];
+#pragma unroll
+    for (int u = 0; u < NG; ++u) {
+      const int g = u < kQuad ? span * kQuad + u : xspan * kQuad + xu;
+      const bool ok = gid < M && g < G;
+#pragma unroll
+      for (int wj = 0; wj < 8; ++wj) {
+        const size_t k = (size_t)gid * K + (size_t)g * 128 + 32 * (wj >> 1) + 8 * (wj & 1) + 2 * t;
+        xl[u][wj] = ok ? x_pair(a.x, xdt, k) : 0u;
+        xh[u][wj] = ok ? x_pair(a.x, xdt, k + 16) : 0u;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < NG; ++u)
+#pragma unroll
+      for (int wj = 0; wj < 8; ++wj) {
+        bfr[u][2 * wj] = bmul2(prmt(xl[u][wj], xh[u][wj], 0x5410u), id0);
+        bfr[u][2 * wj + 1] = bmul2(prmt(xl[u][wj], xh[u][wj], 0x7632u), id1);
+      }
+    // per group: rows 0..7 give C_g = sum a_q x', rows 8..15 Sx_g / 2
+    const uint32_t ac0 = a_bits(2 * t), hc0 = halfd_bits(2 * t), ac1 = a_bits(2 * t + 1), hc1 = halfd_bits(2 * t + 1);
+#pragma unroll
+    for (int gi = 0; gi < GPU; ++gi) {
+      float d[NG][4];
+#pragma unroll
+      for (int u = 0; u < NG; ++u) d[u][0] = d[u][1] = d[u][2] = d[u][3] = 0.f;
+#pragma unroll
+      for (int wj = 2 * GW * gi; wj < 2 * GW * (gi + 1); ++wj)
+#pragma unroll
+        for (int u = 0; u < NG; ++u) mma_acc(d[u], ac0, hc0, ac1, hc1, bfr[u][2 * wj], bfr[u][2 * wj + 1]);
+      if (gid == 0) {
+#pragma unroll
+        for (int u = 0; u < NG; ++u) {
+          const float e0 = AFFINE ? d[u][0] : d[u][0] + d[u][2], e1 = AFFINE ? d[u][1] : d[u][1] + d[u][3];
+          asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(seeds_s + (uint32_t)((u * GPU + gi) * 64)),
+                       "f"(-e0), "f"(-e1), "f"(2.f * d[u][2]), "f"(2.f * d[u][3])
+                       : "memory");
+        }
+      }
+    }
+    __syncwarp();
+  }
+  if (active && GW == 4) {
     uint32_t xv[NG][16];
 #pragma unroll
     for (int u = 0; u < NG; ++u) {
@@ -542,7 +640,7 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
   // gid and gid + 8 share it: ((r >> 1) & 3) is the same for both)
   const int swz = (gid >> 1) & 3;
   const uint32_t wlane = ring_s + qi * kTileBytes + gid * 64 + 4 * t;
-  const uint32_t mlane = meta_s + gid * MROW + (span - q_base) * 8;
+  const uint32_t mlane = meta_s + gid * MROW + (GW == 4 ? (span - q_base) * 8 : 0);
   // the extra group's words and metadata, relative to those of the span
   const uint32_t xw = (uint32_t)((xspan - span) * kTileBytes + ((xu ^ swz) << 4));
   const uint32_t xm = (uint32_t)((xspan - span) * 8 + 2 * xu);
@@ -565,6 +663,70 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
         // a wait that ran out has set the device error word; the results of
         // this call are then undefined, but the CTA still reaches its barriers
         mbar_wait(fb, ph);
+        float acc[4];
+        const bool mbf_t = VAR >= 1 && ((a.meta_bf16 >> ((NMAT == 2 && ((rb + lt) & 1)) ? 1 : 0)) & 1) != 0;
+        const bool has_b_t = AFFINE && ((NMAT == 2 && ((rb + lt) & 1)) ? a.b[1] : a.b[0]) != nullptr;
+        if constexpr (GW < 4) {
+          // the lane's row base (all four words of a unit) and metadata row
+          const uint32_t tq = tb - 4 * t;
+#pragma unroll
+          for (int gi = 0; gi < GPU; ++gi) {
+            float4 sd[NG];
+#pragma unroll
+            for (int u = 0; u < NG; ++u) sd[u] = lds128f(seeds_s + (uint32_t)((u * GPU + gi) * 64));
+            float d[NG][4];
+#pragma unroll
+            for (int w = GW * gi; w < GW * (gi + 1); ++w) {
+              uint32_t wa[NG], wb[NG];
+#pragma unroll
+              for (int u = 0; u < NG; ++u) {
+                const uint32_t o = (u < kQuad ? (uint32_t)((u ^ swz) << 4) : xw) + 4 * w;
+                wa[u] = lds32(tq + o);
+                wb[u] = lds32(tq + o + 8 * 64);
+              }
+#pragma unroll
+              for (int j = 0; j < 2; ++j) {
+#pragma unroll
+                for (int u = 0; u < NG; ++u) {
+                  const uint32_t ra = j ? __umulhi(wa[u], 0x01000000u) : wa[u];
+                  const uint32_t rb2 = j ? __umulhi(wb[u], 0x01000000u) : wb[u];
+                  const uint32_t A0 = selr(ra, m0, kbase), A1 = selr(rb2, m0, kbase);
+                  const uint32_t A2 = selr(ra, m1, kbase), A3 = selr(rb2, m1, kbase);
+                  if (w == GW * gi && j == 0) {
+                    const float c[4] = {sd[u].x, sd[u].y, sd[u].x, sd[u].y};
+                    mma_from(d[u], A0, A1, A2, A3, bfr[u][4 * w + 2 * j], bfr[u][4 * w + 2 * j + 1], c);
+                  } else {
+                    mma_acc(d[u], A0, A1, A2, A3, bfr[u][4 * w + 2 * j], bfr[u][4 * w + 2 * j + 1]);
+                  }
+                }
+              }
+            }
+            // the group's epilogue in every unit
+#pragma unroll
+            for (int u = 0; u < NG; ++u) {
+              const int mi = (u < kQuad ? (span - q_base) * GPS + u * GPU : (xspan - q_base) * GPS + xu * GPU) + gi;
+              const float s_a = meta_f32(lds16(mb + 2 * mi), mbf_t), s_b = meta_f32(lds16(mb + 8 * MROW + 2 * mi), mbf_t);
+              if (gi == 0 && u == 0) {
+                acc[0] = s_a * d[u][0]; acc[1] = s_a * d[u][1]; acc[2] = s_b * d[u][2]; acc[3] = s_b * d[u][3];
+              } else {
+                acc[0] = fmaf(s_a, d[u][0], acc[0]); acc[1] = fmaf(s_a, d[u][1], acc[1]);
+                acc[2] = fmaf(s_b, d[u][2], acc[2]); acc[3] = fmaf(s_b, d[u][3], acc[3]);
+              }
+              if (AFFINE) {
+                float b_a, b_b;
+                if (has_b_t) {
+                  b_a = meta_f32(lds16(mb + 16 * MROW + 2 * mi), mbf_t);
+                  b_b = meta_f32(lds16(mb + 24 * MROW + 2 * mi), mbf_t);
+                } else {
+                  b_a = __fmul_rn(-0.5f, s_a);
+                  b_b = __fmul_rn(-0.5f, s_b);
+                }
+                acc[0] = fmaf(b_a, sd[u].z, acc[0]); acc[1] = fmaf(b_a, sd[u].w, acc[1]);
+                acc[2] = fmaf(b_b, sd[u].z, acc[2]); acc[3] = fmaf(b_b, sd[u].w, acc[3]);
+              }
+            }
+          }
+        } else {
         uint32_t wa[NG], wb[NG];
 #pragma unroll
         for (int u = 0; u < NG; ++u) {
@@ -610,8 +772,7 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
               bfr[u][2 * (JJ)], bfr[u][2 * (JJ) + 1]);
         Q1_MMA(1) Q1_MMA(2) Q1_MMA(3) Q1_MMA(4) Q1_MMA(5) Q1_MMA(6) Q1_MMA(7)
 #undef Q1_MMA
-        float acc[4];
-        const bool mbf = VAR >= 1 && ((a.meta_bf16 >> ((NMAT == 2 && ((rb + lt) & 1)) ? 1 : 0)) & 1) != 0;
+        const bool mbf = mbf_t;
 #pragma unroll
         for (int u = 0; u < NG; ++u) {
           const float s_a = u < kQuad ? meta_half_f32(u < 2 ? sa.x : sa.y, u & 1, mbf) : meta_half_f32(xsa, 0, mbf);
@@ -634,6 +795,7 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
             acc[0] = fmaf(b_a, sx[u][0], acc[0]); acc[1] = fmaf(b_a, sx[u][1], acc[1]);
             acc[2] = fmaf(b_b, sx[u][0], acc[2]); acc[3] = fmaf(b_b, sx[u][1], acc[3]);
           }
+        }
         }
         // every lane's values are consumed: release the slot to the producer
         __syncwarp();
@@ -752,7 +914,7 @@ int sm_count_cached() {
   return n;
 }
 
-template <int NMAT, bool AFFINE, bool FASTMETA, int VAR>
+template <int NMAT, bool AFFINE, bool FASTMETA, int VAR, int GW>
 int max_clusters(int ks) {
   static std::atomic<int> cache[kMaxDevices][9];
   const int dev = current_device();
@@ -770,7 +932,7 @@ int max_clusters(int ks) {
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, narrow_kernel<NMAT, AFFINE, FASTMETA, VAR>, &cfg) != cudaSuccess || n < 1) {
+  if (cudaOccupancyMaxActiveClusters(&n, narrow_kernel<NMAT, AFFINE, FASTMETA, VAR, GW>, &cfg) != cudaSuccess || n < 1) {
     cudaGetLastError();
     n = sm_count_cached() / ks;
   }
@@ -846,7 +1008,7 @@ bool make_meta_map(CUtensorMap *map, const uint16_t *m, int64_t N, int64_t G, in
 // balanced) or the producer's per-slot cost if that is larger, about 0.7
 // tile per warp for the activation fragments, the cluster exchange, and the
 // extra rounds when the partial sums do not fit at once.
-template <int NMAT, bool AFFINE, bool FASTMETA, int VAR>
+template <int NMAT, bool AFFINE, bool FASTMETA, int VAR, int GW>
 bool choose_geo(int64_t N, int K, int M, Geo *out) {
   const int G = K / 128;
   const int QK = (G + kQuad - 1) / kQuad;
@@ -858,7 +1020,7 @@ bool choose_geo(int64_t N, int K, int M, Geo *out) {
     const int qm = (QK + ks - 1) / ks;
     if (qm > kMaxSpans) continue;
     const int nw = kwarps(qm);
-    int nclus = max_clusters<NMAT, AFFINE, FASTMETA, VAR>(ks);
+    int nclus = max_clusters<NMAT, AFFINE, FASTMETA, VAR, GW>(ks);
     if (nclus > NT) nclus = NT;
     const int tv = ((NT + nclus - 1) / nclus) * NMAT;  // virtual row tiles of the widest range
     int R = kMaxWarps / nw;
@@ -871,7 +1033,7 @@ bool choose_geo(int64_t N, int K, int M, Geo *out) {
     // that the activation loads wait in.  At least R + 1 slots, so that every
     // consumer warp can have its next tile loading.
     Geo g{ks, nclus, qm, R, tv, 2, mst};
-    const SmemLayout L0 = smem_layout(g, AFFINE);
+    const SmemLayout L0 = smem_layout(g, AFFINE, GW);
     const int slot = L0.slot_words + L0.slot_meta;
     int ring = (kRingBytes + slot - 1) / slot;
     if (ring > 8) ring = 8;
@@ -880,7 +1042,7 @@ bool choose_geo(int64_t N, int K, int M, Geo *out) {
     if (ring < 2) ring = 2;
     g.ring = ring;
     // shrink the round, then the ring, until shared memory fits
-    while (smem_layout(g, AFFINE).total > kSmemMax) {
+    while (smem_layout(g, AFFINE, GW).total > kSmemMax) {
       if (g.tr > 16 * NMAT) {
         g.tr = (g.tr / 2 / NMAT) * NMAT;
       } else if (g.ring > 3 && g.ring > R + 1) {
@@ -894,7 +1056,7 @@ bool choose_geo(int64_t N, int K, int M, Geo *out) {
         break;
       }
     }
-    if (smem_layout(g, AFFINE).total > kSmemMax) continue;
+    if (smem_layout(g, AFFINE, GW).total > kSmemMax) continue;
     // the producer refills a slot only after its tile is read: with R warps
     // per span, a ring shorter than R + 1 could starve a warp
     if (g.ring < (R + 1 < tv ? R + 1 : tv)) continue;
@@ -923,9 +1085,9 @@ bool choose_geo(int64_t N, int K, int M, Geo *out) {
   return best >= 0;
 }
 
-template <int NMAT, bool AFFINE, bool FASTMETA, int VAR>
+template <int NMAT, bool AFFINE, bool FASTMETA, int VAR, int GW>
 cudaError_t launch_impl(NarrowArgs args, const uint32_t *w0, const uint32_t *w1, cudaStream_t st, bool pdl) {
-  auto kern = narrow_kernel<NMAT, AFFINE, FASTMETA, VAR>;
+  auto kern = narrow_kernel<NMAT, AFFINE, FASTMETA, VAR, GW>;
   static std::atomic<uint64_t> attr_set{0};
   const int dev = current_device();
   if (not_done(attr_set, dev)) {
@@ -934,10 +1096,10 @@ cudaError_t launch_impl(NarrowArgs args, const uint32_t *w0, const uint32_t *w1,
     mark_done(attr_set, dev);
   }
   Geo g;
-  if (!choose_geo<NMAT, AFFINE, FASTMETA, VAR>(args.N, args.K, args.M, &g)) return cudaErrorInvalidConfiguration;
+  if (!choose_geo<NMAT, AFFINE, FASTMETA, VAR, GW>(args.N, args.K, args.M, &g)) return cudaErrorInvalidConfiguration;
   args.geo = g;
   {
-    const SmemLayout L0 = smem_layout(g, AFFINE);
+    const SmemLayout L0 = smem_layout(g, AFFINE, GW);
     args.slot_words = L0.slot_words;
     args.slot_meta = L0.slot_meta;
     args.part_tile = kwarps(g.qm) * 16 * (g.mst < 2 ? 2 : g.mst) * 4;
@@ -952,14 +1114,15 @@ cudaError_t launch_impl(NarrowArgs args, const uint32_t *w0, const uint32_t *w1,
     for (int v = 0; v < 2 && args.w3; ++v)
       if (g.qm - v >= 1 && !make_word_map3(&maps.w3[m][v], m ? w1 : w0, args.N, args.K, g.qm - v)) args.w3 = 0;
   if (FASTMETA) {
-    const int64_t G = args.K / 128;
+    const int64_t G = args.K / (32 * GW);
+    const int box = meta_groups(g.qm, 16 / GW);
     for (int i = 0; i < 2; ++i) {
-      if (!make_meta_map(&maps.s[i], args.s[i], args.N, G, meta_groups(g.qm))) return cudaErrorInvalidValue;
-      if (args.b[i] && !make_meta_map(&maps.b[i], args.b[i], args.N, G, meta_groups(g.qm)))
+      if (!make_meta_map(&maps.s[i], args.s[i], args.N, G, box)) return cudaErrorInvalidValue;
+      if (args.b[i] && !make_meta_map(&maps.b[i], args.b[i], args.N, G, box))
         return cudaErrorInvalidValue;
     }
   }
-  const SmemLayout L = smem_layout(g, AFFINE);
+  const SmemLayout L = smem_layout(g, AFFINE, GW);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(g.nclus * g.ks), 1, 1);
   cfg.blockDim = dim3((unsigned)((kwarps(g.qm) * g.R + 1) * 32), 1, 1);
@@ -977,16 +1140,26 @@ cudaError_t launch_impl(NarrowArgs args, const uint32_t *w0, const uint32_t *w1,
   return cudaLaunchKernelEx(&cfg, kern, maps, args);
 }
 
-template <int NMAT, bool AFFINE, int VAR>
+template <int NMAT, bool AFFINE, int VAR, int GW = 4>
 cudaError_t launch_meta(NarrowArgs args, const uint32_t *w0, const uint32_t *w1, cudaStream_t st, bool pdl) {
-  // metadata by TMA needs 16-byte rows (G % 8 == 0) and 16-byte aligned arrays
-  bool fast = (args.K / 128) % 8 == 0;
+  // metadata by TMA needs 16-byte rows (groups per row % 8 == 0) and 16-byte
+  // aligned arrays
+  bool fast = (args.K / (32 * GW)) % 8 == 0;
   for (int i = 0; i < 2; ++i) {
     fast = fast && (reinterpret_cast<uintptr_t>(args.s[i]) & 15) == 0;
     fast = fast && (reinterpret_cast<uintptr_t>(args.b[i]) & 15) == 0;
   }
-  if (fast) return launch_impl<NMAT, AFFINE, true, VAR>(args, w0, w1, st, pdl);
-  return launch_impl<NMAT, AFFINE, false, VAR>(args, w0, w1, st, pdl);
+  if (fast) return launch_impl<NMAT, AFFINE, true, VAR, GW>(args, w0, w1, st, pdl);
+  return launch_impl<NMAT, AFFINE, false, VAR, GW>(args, w0, w1, st, pdl);
+}
+
+// Groups of 64 or 32 weights: one instance per group size, every type read
+// at run time (VAR 2).
+template <int NMAT, bool AFFINE>
+cudaError_t launch_small(NarrowArgs args, const uint32_t *w0, const uint32_t *w1, int gshift, cudaStream_t st,
+                         bool pdl) {
+  if (gshift == 1) return launch_meta<NMAT, AFFINE, 2, 2>(args, w0, w1, st, pdl);
+  return launch_meta<NMAT, AFFINE, 2, 1>(args, w0, w1, st, pdl);
 }
 
 NarrowArgs make_args(const void *x, int64_t M, int64_t N, int64_t K, void *out, q1_dtype xdt, q1_dtype ydt) {
@@ -1009,6 +1182,9 @@ cudaError_t launch_narrow(const WeightView &W, const void *x, int64_t M, void *y
   a.s[0] = a.s[1] = W.s;
   a.b[0] = a.b[1] = W.b;
   a.meta_bf16 = W.mbf16 ? 3 : 0;
+  if (W.gshift < 2)
+    return W.b ? launch_small<1, true>(a, W.w, W.w, W.gshift, st, pdl)
+               : launch_small<1, false>(a, W.w, W.w, W.gshift, st, pdl);
   if (xdt != Q1_BF16 || ydt != Q1_BF16)
     return W.b ? launch_meta<1, true, 2>(a, W.w, W.w, st, pdl) : launch_meta<1, false, 2>(a, W.w, W.w, st, pdl);
   if (W.mbf16)
@@ -1025,7 +1201,11 @@ cudaError_t launch_narrow_gate_up(const WeightView &G, const WeightView &U, cons
   a.b[1] = U.b;
   a.meta_bf16 = (G.mbf16 ? 1 : 0) | (U.mbf16 ? 2 : 0);
   // With mixed metadata the affine variant runs for both matrices; it derives
-  // -scale/2 for the one whose biases pointer is null.
+  // -scale/2 for the one whose biases pointer is null.  Gate and up share one
+  // group size (the API checks it).
+  if (G.gshift < 2)
+    return (G.b || U.b) ? launch_small<2, true>(a, G.w, U.w, G.gshift, st, pdl)
+                        : launch_small<2, false>(a, G.w, U.w, G.gshift, st, pdl);
   if (xdt != Q1_BF16) {
     if (G.b || U.b) return launch_meta<2, true, 2>(a, G.w, U.w, st, pdl);
     return launch_meta<2, false, 2>(a, G.w, U.w, st, pdl);

@@ -273,9 +273,8 @@ def qmm_narrow(W: Q1Weight, x: torch.Tensor, out=None) -> torch.Tensor:
 
 def qmm(W: Q1Weight, x: torch.Tensor, workspace: Optional[torch.Tensor] = None,
         out=None) -> torch.Tensor:
-    """x [..., K] -> y [..., N]; narrow path up to the row threshold, tcgen05 beyond
-    and for group sizes 32 and 64 (which needs a workspace; one is allocated
-    when none is given)."""
+    """x [..., K] -> y [..., N]; narrow path up to the row threshold, tcgen05
+    beyond (which needs a workspace; one is allocated when none is given)."""
     _cuda(x, "x", W.words.device)
     xdt = _x_dtype(x)
     lead = x.shape[:-1]
@@ -283,7 +282,7 @@ def qmm(W: Q1Weight, x: torch.Tensor, workspace: Optional[torch.Tensor] = None,
     M = x2.shape[0]
     y = _out(out, (M, W.N), x.dtype, x.device)
     ws = workspace
-    if ws is None and (M > get_qmm_max_rows() or W.K > NARROW_MAX_K or W.group_size != 128):
+    if ws is None and (M > get_qmm_max_rows() or W.K > NARROW_MAX_K):
         ws = qmm_workspace(M, W.N, W.K, x.device)
     if ws is not None:
         _cuda(ws, "workspace", x.device)

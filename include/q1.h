@@ -90,11 +90,11 @@ typedef enum { Q1_META_F16 = 0, Q1_META_BF16 = 1 } q1_meta_dtype;
  *   group_size: 128 (every checkpoint on the pages), or 32 or 64 (MLX's affine
  *   format allows them; "1-bit affine weight support", rMLX issue #207, lists
  *   "group_size=32 occupancy" among mlx#3161's edge cases).  scales/biases are
- *   then [N][K/group_size].  Every call takes 128; q1_dequantize,
- *   q1_embed_gather, q1_check_symmetric and q1_qmm also take 32 and 64 (q1_qmm
- *   runs them on its prefill path for every M, so it needs its workspace);
- *   the narrow-only calls (q1_qmv, q1_qmm_narrow, q1_ffn_fused*,
- *   q1_decode_chain) return Q1_ERR_GROUP for them.
+ *   then [N][K/group_size].  Every call takes all three; the gate and up
+ *   matrices of one FFN (q1_ffn_fused*, q1_decode_chain) must share a group
+ *   size (else Q1_ERR_GROUP).  The narrow products (M <= 8) close their MMA
+ *   chains on every group: 128 is their fast path, 64 and 32 cost more
+ *   instructions per weight (each step then covers one 32-weight word).
  *   meta_dtype: Q1_META_F16 (0, so a zero-initialised field means fp16) or
  *   Q1_META_BF16; anything else returns Q1_ERR_DTYPE.
  * The prefill path (q1_qmm above the narrow threshold) builds fp16 weight

@@ -156,3 +156,16 @@ def test_ffn_full_shape_all_affine(q1):
     assert np.linalg.norm(h - ho) / np.linalg.norm(ho) < 5e-3
     check_matmul(y[:, rows], yo, ho, O.dequantize_f32(down.words[rows], down.scales[rows], down.biases[rows], D_FF),
                  "affine ffn full shape", rounded_to="bf16")
+
+
+@pytest.mark.parametrize("group", [32, 64])
+@pytest.mark.parametrize("M", [1, 8])
+@pytest.mark.parametrize("N,K,affine", [(D_FF, D_MODEL, False), (D_MODEL, D_FF, True)])
+def test_small_group_narrow_full_shapes(q1, group, M, N, K, affine):
+    # the 27B-class shapes with metadata per 32 or 64 weights, on the narrow
+    # kernel (the K-split down shape included)
+    t = synth.q1_tensor(N, K, seed=1021 + group + affine, affine=affine, group=group)
+    x = synth.activations(M, K, seed=1022 + M)
+    W = q1.Q1Weight.from_host(t)
+    y = q1.qmm_narrow(W, x.to(DEV)).float().cpu().double().numpy()
+    _check_rows(y, t, x, _rows(N, 96, group + M), f"group {group} narrow M={M} {N}x{K}")

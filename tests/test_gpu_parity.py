@@ -515,16 +515,90 @@ def test_small_groups(q1, group, affine):
     want, _ = O.embed_gather(ids, t.words, t.scales, t.biases, K, "bf16")
     assert int(bad.item()) == 0 and torch.equal(out.cpu().view(torch.int16), want.view(torch.int16))
     wd = O.dequantize_f32(t.words, t.scales, t.biases, K)
-    for M in (1, 8, 200):  # every M runs on the prefill path
+    for M in (1, 8, 200):  # narrow (the per-word mapping) and prefill
         x = synth.activations(M, K, seed=673 + M)
         y = q1.qmm(W, x.to(DEV))
         check_matmul(y, O.qmm(x, t.words, t.scales, t.biases, K), x, wd, f"group {group} M={M}")
-    # the narrow-only calls refuse these group sizes
-    x1 = torch.zeros((K,), dtype=torch.bfloat16, device=DEV)
-    y1 = torch.empty((N,), dtype=torch.bfloat16, device=DEV)
-    st = torch.cuda.current_stream().cuda_stream
-    assert q1.lib().q1_qmv(W.cref(), x1.data_ptr(), 0, y1.data_ptr(), st) == 5
-    assert q1.lib().q1_qmm_narrow(W.cref(), x1.data_ptr(), 1, 0, y1.data_ptr(), st) == 5
+
+
+@pytest.mark.parametrize("group", [32, 64])
+@pytest.mark.parametrize("affine", [False, True])
+@pytest.mark.parametrize("N,K", [(1024, 1024), (333, 640), (130, 5120), (48, 17408 // 4)])
+def test_small_groups_narrow(q1, group, affine, N, K):
+    # the narrow kernel's groups-of-32/64 path at every window size 1..8:
+    # ragged row tiles, K of 5 to 34 spans (extra groups past the K-warps),
+    # metadata rows whose group count is not a multiple of 8 (K = 640 at
+    # group 64: 10 groups, loaded by the producer's lanes instead of TMA)
+    t = synth.q1_tensor(N, K, seed=681 + group + affine + N, affine=affine, group=group)
+    W = q1.Q1Weight.from_host(t)
+    wd = O.dequantize_f32(t.words, t.scales, t.biases, K)
+    for M in (1, 2, 3, 5, 8):
+        x = synth.activations(M, K, seed=682 + M)
+        y = q1.qmm_narrow(W, x.to(DEV))
+        check_matmul(y, O.qmm(x, t.words, t.scales, t.biases, K), x, wd, f"group {group} narrow N={N} K={K} M={M}")
+    y1 = q1.qmv(W, x[0].to(DEV))
+    check_matmul(y1[None], O.qmm(x[:1], t.words, t.scales, t.biases, K), x[:1], wd, f"group {group} qmv")
+
+
+@pytest.mark.parametrize("group", [32, 64])
+def test_small_groups_fp16_fp32_and_bf16_metadata(q1, group):
+    N, K = 600, 1280
+    t = synth.q1_tensor(N, K, seed=691 + group, affine=True, group=group)
+    W = q1.Q1Weight.from_host(t)
+    wd = O.dequantize_f32(t.words, t.scales, t.biases, K)
+    for dtype in (torch.float16, torch.float32):
+        x = _acts(4, K, 692, dtype)
+        y = q1.qmm_narrow(W, x.to(DEV))
+        assert y.dtype == dtype
+        # affine weights: the oracle takes the bf16 operands the kernel multiplies
+        xb = x.to(torch.bfloat16)
+        check_matmul(y, O.qmm(xb, t.words, t.scales, t.biases, K), xb, wd, f"group {group} {dtype}",
+                     rounded_to=_NAME[dtype])
+    w, s, b = _bf16_meta(t)
+    Wb = q1_weight_from(w, s, b, K)
+    x = synth.activations(3, K, seed=693)
+    y = q1.qmm_narrow(Wb, x.to(DEV))
+    check_matmul(y, O.qmm(x, w, s, b, K), x, O.dequantize_f32(w, s, b, K), f"group {group} bf16 metadata")
+
+
+def test_small_groups_ffn_and_chain(q1):
+    # gate/up with groups of 64, down with groups of 32; and a two-layer chain
+    # mixing the three group sizes
+    M, D, F = 4, 512, 1408
+    gate = synth.q1_tensor(F, D, seed=701, affine=False, group=64)
+    up = synth.q1_tensor(F, D, seed=702, affine=True, group=64)
+    down = synth.q1_tensor(D, F, seed=703, affine=False, group=32)
+    x = synth.activations(M, D, seed=704)
+    G, U, Dn = (q1.Q1Weight.from_host(w) for w in (gate, up, down))
+    ws = q1.ffn_workspace(M, D, F, DEV)
+    y = q1.ffn_fused(G, U, Dn, x.to(DEV), workspace=ws)
+    yo, ho = O.ffn(x, (gate.words, gate.scales, None, D), (up.words, up.scales, up.biases, D),
+                   (down.words, down.scales, None, F))
+    h = q1.ffn_h(ws, M, F).float().cpu().double().numpy()
+    assert np.linalg.norm(h - ho) / np.linalg.norm(ho) < 5e-3
+    check_matmul(y, yo, ho, O.dequantize_f32(down.words, down.scales, None, F), "ffn groups 64/32")
+    # gate and up with different group sizes are refused
+    U32 = q1.Q1Weight.from_host(synth.q1_tensor(F, D, seed=705, affine=False, group=32))
+    with pytest.raises(q1.Q1Error) as e:
+        q1.ffn_fused(G, U32, Dn, x.to(DEV))
+    assert e.value.status == 5
+    # chain: layer 0 with groups of 32 (attn) and 64 (gate/up), layer 1 of 128
+    D2, F2 = 256, 512
+    layers = []
+    for l, (ga, gg, gd) in enumerate(((32, 64, 32), (128, 128, 64))):
+        base = 710 + 10 * l
+        layers.append((_scaled(synth.q1_tensor(D2, D2, seed=base, affine=False, group=ga), 7.0),
+                       _scaled(synth.q1_tensor(F2, D2, seed=base + 1, affine=False, group=gg), 7.0),
+                       _scaled(synth.q1_tensor(F2, D2, seed=base + 2, affine=False, group=gg), 7.0),
+                       _scaled(synth.q1_tensor(D2, F2, seed=base + 3, affine=False, group=gd), 7.0)))
+    dev = [tuple(q1.Q1Weight.from_host(w) for w in L) for L in layers]
+    xc = synth.activations(2, D2, seed=729).to(DEV)
+    yc = q1.decode_chain(dev, xc)
+    hc = xc
+    for A, Gg, Uu, Dd in dev:
+        hc = q1.ffn_fused(Gg, Uu, Dd, q1.qmm_narrow(A, hc))
+    torch.cuda.synchronize()
+    assert torch.equal(yc, hc)
 
 
 def test_small_groups_check_symmetric(q1):
