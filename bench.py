@@ -348,6 +348,78 @@ def time_prefill(q1, synth, torch, device, M, shape, affine, reps=20):
     return 2.0 * M * N * K / t / 1e12, 2.0 * M * N * K / t_unfused / 1e12
 
 
+def weight_bytes_g(N, K, affine, group):
+    """Algorithmic bytes of one packed matrix with metadata per `group` weights."""
+    G = K // group
+    return N * K // 8 + N * G * 2 * (2 if affine else 1)
+
+
+def narrow_sweep(q1, synth, torch, device, stream):
+    """GB/s of single launches (graph of launches over 12 distinct matrices,
+    150-210 MB, more than the L2) on the two 27B-class FFN shapes: M = 1..9
+    (M = 9 crosses to the prefill path at the default threshold), symmetric
+    and affine; and M = 1 with metadata per 64 and per 32 weights."""
+    out = {}
+    nl = 12
+    for name, N, K in (SHAPES[0], SHAPES[2]):
+        for affine in (False, True):
+            Ws = [q1.Q1Weight(synth.device_weight_words(N, K, 300 + i, device),
+                              synth.device_scales(N, K, 320 + i, device),
+                              synth.device_biases(N, K, 340 + i, device) if affine else None, K)
+                  for i in range(nl)]
+            ws = q1.qmm_workspace(9, N, K, device)
+            for M in range(1, 10):
+                x = torch.randn((M, K), device=device).to(torch.bfloat16)
+                y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+                t = graph_time(torch, [lambda W=W: q1.qmm(W, x, workspace=ws, out=y) for W in Ws], stream, per=24)
+                b = weight_bytes(N, K, affine) + M * K * 2 + M * N * 2
+                out[f"qmm_{name}_{'affine' if affine else 'sym'}_M{M}_GBps"] = round(b / t / 1e9, 1)
+            del Ws
+            torch.cuda.empty_cache()
+    name, N, K = SHAPES[0]
+    for group in (64, 32):
+        Ws = []
+        for i in range(nl):
+            g = torch.Generator(device=device)
+            g.manual_seed(360 + i)
+            sc = (torch.randn((N, K // group), generator=g, device=device).abs() * 0.02 + 1e-4).to(torch.float16)
+            Ws.append(q1.Q1Weight(synth.device_weight_words(N, K, 350 + i, device), sc, None, K))
+        x = torch.randn((K,), device=device).to(torch.bfloat16)
+        y = torch.empty((N,), dtype=torch.bfloat16, device=device)
+        t = graph_time(torch, [lambda W=W: q1.qmv(W, x, out=y) for W in Ws], stream, per=24)
+        out[f"qmv_{name}_group{group}_M1_GBps"] = round((weight_bytes_g(N, K, False, group) + K * 2 + N * 2) / t / 1e9, 1)
+        del Ws
+        torch.cuda.empty_cache()
+    return out
+
+
+def ffn_bytes(M, affine=False):
+    """Algorithmic bytes of one fused FFN call: the three matrices once, x in,
+    the bf16 intermediate h written and read, y out."""
+    w = 2 * weight_bytes(D_FF, D_MODEL, affine) + weight_bytes(D_MODEL, D_FF, affine)
+    return w + M * D_MODEL * 2 + 2 * M * D_FF * 2 + M * D_MODEL * 2
+
+
+def ffn_sweep(q1, synth, torch, device, stream):
+    """GB/s of q1_ffn_fused at M = 1, 4, 8 over 6 distinct FFN blocks (226 MB)."""
+    out = {}
+    blocks = []
+    for i in range(6):
+        mk = lambda N, K, sd: q1.Q1Weight(synth.device_weight_words(N, K, sd, device),
+                                          synth.device_scales(N, K, sd + 1, device), None, K)
+        blocks.append((mk(D_FF, D_MODEL, 400 + 10 * i), mk(D_FF, D_MODEL, 402 + 10 * i), mk(D_MODEL, D_FF, 404 + 10 * i)))
+    for M in (1, 4, 8):
+        x = torch.randn((M, D_MODEL), device=device).to(torch.bfloat16)
+        y = torch.empty((M, D_MODEL), dtype=torch.bfloat16, device=device)
+        ws = q1.ffn_workspace(M, D_MODEL, D_FF, device)
+        t = graph_time(torch, [lambda B=B: q1.ffn_fused(*B, x, workspace=ws, out=y) for B in blocks], stream, per=12)
+        out[f"ffn_fused_M{M}_GBps"] = round(ffn_bytes(M) / t / 1e9, 1)
+        out[f"ffn_fused_M{M}_us"] = round(t * 1e6, 2)
+    del blocks
+    torch.cuda.empty_cache()
+    return out
+
+
 def profile_case(args):
     """A few launches of one kernel on one shape, for ncu (small device footprint)."""
     import torch
@@ -523,13 +595,19 @@ def gpu_arm(args):
         torch.cuda.empty_cache()
         sub.update(elementwise_and_head(q1, synth, torch, device, stream))
         torch.cuda.empty_cache()
-        # prefill on the tensor cores
-        for M in (128, 2048):
+        # narrow M = 1..9 (and the crossover), group sizes 64/32, standalone FFN
+        sub.update(narrow_sweep(q1, synth, torch, device, stream))
+        sub.update(ffn_sweep(q1, synth, torch, device, stream))
+        # prefill on the tensor cores, symmetric and affine, against the
+        # unfused dequantize + cuBLAS comparator
+        for M in (128, 512, 2048):
             for shp in (SHAPES[0], SHAPES[2]):
-                tf, tf_unf = time_prefill(q1, synth, torch, device, M, shp, affine=False)
-                sub[f"prefill_M{M}_{shp[0]}_TFLOPs"] = round(tf, 1)
-                sub[f"prefill_M{M}_{shp[0]}_unfused_TFLOPs"] = round(tf_unf, 1)
-                torch.cuda.empty_cache()
+                for affine in (False, True):
+                    tf, tf_unf = time_prefill(q1, synth, torch, device, M, shp, affine=affine)
+                    tag = f"prefill_M{M}_{shp[0]}" + ("_affine" if affine else "")
+                    sub[f"{tag}_TFLOPs"] = round(tf, 1)
+                    sub[f"{tag}_unfused_TFLOPs"] = round(tf_unf, 1)
+                    torch.cuda.empty_cache()
     assert q1.device_errors() == 0, "device-side wait ran out"
 
     if rank != 0:

@@ -68,3 +68,14 @@ def test_clock_summary_reports_the_median_under_load():
     assert d["samples"] == 4 and d["samples_under_load"] == 3
     assert d["sm_mhz"] == 2055 and d["sm_max_mhz"] == 2070
     assert d["reasons"] == ["sw_power_cap"]
+
+
+def test_ffn_and_small_group_bytes():
+    # FFN: gate and up 17408 x 5120 and down 5120 x 17408 once (12,533,760 B
+    # each, symmetric), x and y [M, 5120] bf16, h [M, 17408] bf16 written and read
+    for M in (1, 4, 8):
+        assert bench.ffn_bytes(M) == 3 * 12_533_760 + M * 5120 * 2 * 2 + 2 * M * 17408 * 2
+    # metadata per 64 / 32 weights: 80 / 160 fp16 scales per 5120-weight row
+    assert bench.weight_bytes_g(17408, 5120, False, 64) == 11_141_120 + 17408 * 80 * 2
+    assert bench.weight_bytes_g(17408, 5120, False, 32) == 11_141_120 + 17408 * 160 * 2
+    assert bench.weight_bytes_g(17408, 5120, True, 128) == bench.weight_bytes(17408, 5120, True)
