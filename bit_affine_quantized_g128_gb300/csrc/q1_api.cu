@@ -93,6 +93,7 @@ const char *q1_status_string(q1_status s) {
 
 void q1_set_qmm_max_rows(int rows) { g_max_rows.store(rows < 0 ? 0 : (rows > 8 ? 8 : rows)); }
 int q1_get_qmm_max_rows(void) { return g_max_rows.load(); }
+void q1_set_prefill_plan(int token_tile, int split) { q1::set_pair_plan(token_tile, split); }
 
 q1_status q1_pack(const uint8_t *bits, int64_t N, int64_t K, uint32_t *w, q1_stream stream) {
   q1_status s = check_device();

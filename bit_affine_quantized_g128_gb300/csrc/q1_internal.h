@@ -87,6 +87,8 @@ size_t wide_workspace_bytes(int64_t M, int64_t K);
 // x [M][K] and y [M][N] in dt (bf16, fp16 or fp32)
 cudaError_t launch_wide(const WeightView &W, const void *x, int64_t M, void *y, void *ws,
                         cudaStream_t st, q1_dtype dt = Q1_BF16);
+// fixed prefill tiling (token_tile, split), or the automatic choice when invalid
+void set_pair_plan(int token_tile, int split);
 
 // ---- device error words (each translation unit with bounded waits owns one)
 unsigned int read_and_clear_wide_errors(cudaStream_t st, cudaError_t *err);

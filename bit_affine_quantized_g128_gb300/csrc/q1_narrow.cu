@@ -520,7 +520,7 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
   float sx[NG][2];
   // the small-group mapping's lane constants: bit pairs q0 = 2t, q1 = 2t + 1
   // of each half of a word, their masks, 1/d, and the C/E chains' a and d/2
-  const uint32_t m0 = 0x00010001u << (2 * t), m1 = 0x00010001u << (2 * t + 1);
+  [[maybe_unused]] const uint32_t m0 = 0x00010001u << (2 * t), m1 = 0x00010001u << (2 * t + 1);
   const uint32_t seeds_s = smem_u32(smem + L.seeds) + (uint32_t)(warp * kMaxUnits * GPU * 64 + 16 * t);
   if (active && GW < 4) {
     const uint32_t id0 = inv_d_bits(2 * t), id1 = inv_d_bits(2 * t + 1);
@@ -643,7 +643,7 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
   const uint32_t mlane = meta_s + gid * MROW + (GW == 4 ? (span - q_base) * 8 : 0);
   // the extra group's words and metadata, relative to those of the span
   const uint32_t xw = (uint32_t)((xspan - span) * kTileBytes + ((xu ^ swz) << 4));
-  const uint32_t xm = (uint32_t)((xspan - span) * 8 + 2 * xu);
+  [[maybe_unused]] const uint32_t xm = (uint32_t)((xspan - span) * 8 + 2 * xu);
 
   // this lane's partial sums (rows gid, gid + 8 of K-warp qi; tokens 2t, 2t+1)
   const uint32_t plane = smem_u32(part) + (uint32_t)(((qi * 16 + gid) * MST + 2 * t) * 4);
@@ -665,7 +665,7 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
         mbar_wait(fb, ph);
         float acc[4];
         const bool mbf_t = VAR >= 1 && ((a.meta_bf16 >> ((NMAT == 2 && ((rb + lt) & 1)) ? 1 : 0)) & 1) != 0;
-        const bool has_b_t = AFFINE && ((NMAT == 2 && ((rb + lt) & 1)) ? a.b[1] : a.b[0]) != nullptr;
+        [[maybe_unused]] const bool has_b_t = AFFINE && ((NMAT == 2 && ((rb + lt) & 1)) ? a.b[1] : a.b[0]) != nullptr;
         if constexpr (GW < 4) {
           // the lane's row base (all four words of a unit) and metadata row
           const uint32_t tq = tb - 4 * t;

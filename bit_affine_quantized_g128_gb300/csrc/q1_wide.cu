@@ -5,41 +5,29 @@
 // "Limitations / non-goals", runs forwards wider than the narrow threshold by
 // dequantizing the whole matrix to the input dtype and calling a dense matmul,
 // which is what set its peak memory ("Measured impact": peak about 6.65 GB
-// from dense prefill temporaries).  Here the dequantization happens per tile
-// in shared memory, feeding the MMA directly: no dense weight temporary.
+// from dense prefill temporaries).  Here the dequantization happens per stage
+// straight into tensor memory, feeding the MMA: no dense weight temporary.
 //
 // Operand precision.  Rounding the dequantized weights to bf16 (a half-ulp of
 // 2^-8, the same for every weight of a symmetric group) moves a few outputs in
-// 10^5 past the per-element error bar the method is held to, so the tiles are
-// fp16 instead: symmetric weights +-s/2 are exact in fp16 and affine values
-// s+b are rounded once at 2^-11.  The activations go to fp16 through a
+// 10^5 past the per-element error bar the method is held to, so the operands
+// are fp16 instead: symmetric weights +-s/2 are exact in fp16 and affine
+// values s+b are rounded once at 2^-11.  The activations go to fp16 through a
 // per-row power-of-two scale 2^e_m chosen so that the row maximum lands in
 // [2^14, 2^15) (exact for every normal fp16 result, no overflow); the
 // epilogue multiplies by 2^-e_m.  A small prep kernel writes the scaled fp16
 // rows and the scales into the caller's workspace.
 //
-// One CTA computes MT x 128 tokens x 256 rows (MT = 2 when that needs fewer
-// CTA-times than MT = 1, see launch_wide):
-// every dequantized weight tile feeds MT MMAs, one per 128-token tile, into
-// MT 256-column TMEM accumulators.  About 192 KB of shared memory keeps the
-// CTA alone on its SM, so its TMEM allocation (256 or 512 columns) cannot
-// contend:
-//   warp 0        TMA producer: x tiles [MT x 128 tokens x 64 k] fp16, 128B swizzle
-//   warp 1        TMEM allocator and the single MMA-issuing thread
-//                 (tcgen05.mma.cta_group::1.kind::f16, M=128 N=256 K=16)
-//   warps 2..17   dequantizers: two threads per weight row read the packed
-//                 words of one group (uint4) and the group's scale/bias; each
-//                 writes 32 fp16 (one word) per k-step into the 128B-swizzled
-//                 K-major layout the MMA reads; then the epilogue:
-//                 TMEM -> registers -> scale -> bf16 -> global.
-// Stages: 4 (MT = 1) or 3 (MT = 2) x (x tiles + 32 KB weight tile), mbarrier
-// hand-offs.
-// When the tiles are too few to fill the SMs (small M, or the 5120-row down
-// projection), a cluster of up to 8 CTAs splits K for each tile and sums the
-// partial tiles through distributed shared memory (see SPLIT below).
-// Every wait is bounded (globaltimer); one that runs out sets a device error
-// word and a CTA-wide abort flag so that the other roles stop waiting too.
-#include <cooperative_groups.h>
+// The matmul runs on CTA pairs (tcgen05.mma.cta_group::2): the pair computes
+// 256 weight rows x NT tokens, the dequantized weights are the MMA's A
+// operand in tensor memory (M = 256, 128 rows per CTA) and the activations
+// the B operand in shared memory (N = NT, NT/2 tokens per CTA), K = 16 per
+// instruction.  Weights written to tensor memory by tcgen05.st never touch
+// shared memory, and each CTA holds only its half of the token tile, so
+// shared memory carries about 64 B/clk at full MMA rate.  (With the weights
+// as the shared-memory operand instead, every MMA re-read the weight tile
+// from shared memory and the dequantizers' stores drained slowly behind those
+// reads: the k-steps ran at about half the MMA rate.)
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -53,34 +41,8 @@ __device__ unsigned int g_wide_err = 0;
 
 namespace {
 
-constexpr int BM = 128;  // tokens per MMA tile (TMEM lanes)
-constexpr int BN = 256;  // weight rows per tile (MMA N)
-constexpr int BK = 64;   // k per stage (one 128-byte swizzle atom of fp16)
-// MT token tiles of BM per CTA share every dequantized weight tile (MT = 2
-// halves the dequantization per MMA); the stages then shrink from 4 to 3
-template <int MT> constexpr int kStages = MT == 1 ? 4 : 3;
-constexpr int kThreadsWide = 576;  // 18 warps
-constexpr int kDeqWarp0 = 2;
-constexpr int kDeqThreads = 512;   // two threads per weight row: one word each per k-step
-constexpr uint32_t A_TILE = BM * BK * 2;   // 16 KB per token tile
-constexpr uint32_t B_BYTES = BN * BK * 2;  // 32 KB
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s: every barrier wait is bounded
 
-constexpr int kMaxStages = 4;
-// split-K partial tile in the (then idle) stage memory: 128 rows x 256 fp32,
-// rows padded by 16 bytes so that a warp's row-wise stores spread over the banks
-constexpr int kPartStride = BN + 4;
-struct __align__(8) WideShared {
-  uint64_t full_a[kMaxStages];
-  uint64_t full_b[kMaxStages];
-  uint64_t empty[kMaxStages];
-  uint64_t accum_full;
-  uint32_t tmem_base;
-  volatile int abort_flag;
-};
-
-template <int MT>
-constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + kStages<MT> * (MT * A_TILE + B_BYTES) + sizeof(WideShared);
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -105,25 +67,6 @@ __device__ __forceinline__ bool mbar_try(uint32_t addr, uint32_t parity) {
       : "r"(addr), "r"(parity)
       : "memory");
   return ok != 0;
-}
-
-// Bounded wait on the phase with the given parity.  Returns false when the
-// wait ran out or another role of this CTA already aborted.
-__device__ __noinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, WideShared *sh) {
-  const uint32_t addr = smem_u32(bar);
-  if (mbar_try(addr, parity)) return true;
-  const unsigned long long t0 = globaltimer();
-  for (uint32_t i = 0;; ++i) {
-    if (mbar_try(addr, parity)) return true;
-    if ((i & 15u) == 15u) {
-      if (sh->abort_flag) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
-        sh->abort_flag = 1;
-        atomicOr(&g_wide_err, 1u);
-        return false;
-      }
-    }
-  }
 }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t *b) {
@@ -156,33 +99,14 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor, kind::f16: fp32 accumulator (bits 4..5 = 1), fp16 A
-// and B (format 0 at bits 7..9 and 10..12), both K-major, N >> 3 at bits
-// 17..22, M >> 4 at bits 24..28.
-constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
-
-__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
-      : "memory");
-}
-
-__device__ __forceinline__ void umma_commit(uint64_t *bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   smem_u32(bar))
-               : "memory");
-}
-
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
   return d;
 }
 
-// 32 weights of one word -> 16 bf16x2 in k order: out[j] = (k = 2j, 2j+1).
+// 32 weights of one word -> 16 pairs of 16-bit values in k order: out[j] =
+// (k = 2j, 2j+1), each lo (bit 0) or hi (bit 1) of the group.
 // A prmt with the sign-replicate selector turns bit 7 of a source byte into a
 // 0x00/0xFF byte, so two shifted copies of the word give 16-bit masks for two
 // adjacent weights at once; one LOP3 then selects hi (bit 1) or lo (bit 0).
@@ -220,343 +144,6 @@ __device__ __forceinline__ void store4(void *y, size_t i, const float (&f)[4], i
     *reinterpret_cast<float4 *>(static_cast<float *>(y) + i) = make_float4(f[0], f[1], f[2], f[3]);
   } else {
     *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(y) + i) = make_uint2(pack2(f[0], f[1], dt), pack2(f[2], f[3], dt));
-  }
-}
-// eight values, y + i aligned to 16 bytes
-__device__ __forceinline__ void store8(void *y, size_t i, const float (&f)[8], int dt) {
-  if (dt == Q1_F32) {
-    float4 *d = reinterpret_cast<float4 *>(static_cast<float *>(y) + i);
-    d[0] = make_float4(f[0], f[1], f[2], f[3]);
-    d[1] = make_float4(f[4], f[5], f[6], f[7]);
-  } else {
-    *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(y) + i) =
-        make_uint4(pack2(f[0], f[1], dt), pack2(f[2], f[3], dt), pack2(f[4], f[5], dt), pack2(f[6], f[7], dt));
-  }
-}
-
-// One thread's share of a 128-k unit: its row's four words, and the metadata
-// of the two words it expands (k-steps 0 and 1); the same group for both
-// unless the group size is 32 or 64.
-struct GroupData {
-  uint4 w;
-  uint16_t s[2], b[2];
-};
-
-// SPLIT: a thread-block cluster of `ksplit` CTAs shares one output tile, each
-// taking a contiguous range of the 128-k groups; the fp32 partial tiles are
-// summed through distributed shared memory in rank order (deterministic, no
-// workspace).  Only with MT = 1.
-template <int MT, bool SPLIT, bool G128>
-__global__ void __launch_bounds__(kThreadsWide, 1)
-wide_kernel(const __grid_constant__ CUtensorMap tmap_x, const uint32_t *__restrict__ W,
-            const uint16_t *__restrict__ S, const uint16_t *__restrict__ Bv, int M, int N, int K,
-            const float *__restrict__ inv_scale, void *__restrict__ y, int ksplit, int mbf16, int ydt,
-            int gshift) {
-  static_assert(!SPLIT || MT == 1, "split-K keeps one token tile per CTA");
-  extern __shared__ unsigned char smem_raw[];
-  unsigned char *base = reinterpret_cast<unsigned char *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  constexpr int STAGES = kStages<MT>;
-  constexpr uint32_t A_BYTES = MT * A_TILE;        // the stage's x tiles (MT x 128 tokens)
-  constexpr uint32_t kTmemCols = 256 * MT;         // one 256-column accumulator per token tile
-  unsigned char *sa = base;                        // STAGES x A_BYTES
-  unsigned char *sb = base + STAGES * A_BYTES;     // STAGES x B_BYTES
-  WideShared *sh = reinterpret_cast<WideShared *>(sb + STAGES * B_BYTES);
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int rank = SPLIT ? (int)(blockIdx.x % (unsigned)ksplit) : 0;
-  const int n0 = (SPLIT ? (int)(blockIdx.x / (unsigned)ksplit) : (int)blockIdx.x) * BN;
-  const int m0 = blockIdx.y * (BM * MT);
-  // this CTA's groups [g_lo, g_hi) and k-steps (two per group)
-  const int GK = K / 128;
-  const int g_lo = SPLIT ? (int)(((int64_t)GK * rank) / ksplit) : 0;
-  const int g_hi = SPLIT ? (int)(((int64_t)GK * (rank + 1)) / ksplit) : GK;
-  const int KS0 = 2 * g_lo, KSTEPS = 2 * (g_hi - g_lo);
-
-  if (tid == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&sh->full_a[s], 1);
-      mbar_init(&sh->full_b[s], kDeqThreads / 32);
-      mbar_init(&sh->empty[s], 1);
-    }
-    mbar_init(&sh->accum_full, 1);
-    sh->abort_flag = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_x) : "memory");
-  }
-  if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(&sh->tmem_base)),
-                 "r"(kTmemCols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-  __syncthreads();
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-  const uint32_t tmem_d = sh->tmem_base;
-
-  if (warp == 0) {
-    // ---------------- TMA producer (x tiles)
-    if (lane == 0) {
-      // the fp16 rows come from the prep kernel that precedes this one
-      asm volatile("griddepcontrol.wait;" ::: "memory");
-      for (int ks = 0; ks < KSTEPS; ++ks) {
-        const int s = ks % STAGES;
-        const uint32_t ph = (uint32_t)(ks / STAGES) & 1u;
-        if (!mbar_wait(&sh->empty[s], ph ^ 1u, sh)) break;
-        mbar_arrive_expect_tx(&sh->full_a[s], A_BYTES);
-        tma_load_2d(sa + s * A_BYTES, &tmap_x, &sh->full_a[s], (KS0 + ks) * BK, m0);
-      }
-    }
-  } else if (warp == 1) {
-    // ---------------- MMA issuer
-    if (lane == 0) {
-      bool ok = true;
-      for (int ks = 0; ks < KSTEPS && ok; ++ks) {
-        const int s = ks % STAGES;
-        const uint32_t ph = (uint32_t)(ks / STAGES) & 1u;
-        ok = mbar_wait(&sh->full_a[s], ph, sh) && mbar_wait(&sh->full_b[s], ph, sh);
-        if (!ok) break;
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint32_t a_addr = smem_u32(sa + s * A_BYTES), b_addr = smem_u32(sb + s * B_BYTES);
-#pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-#pragma unroll
-          for (int mt = 0; mt < MT; ++mt)
-            umma_bf16(tmem_d + 256u * mt, sw128_desc(a_addr + mt * A_TILE + kk * 32), sw128_desc(b_addr + kk * 32),
-                      (ks > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(&sh->empty[s]);
-      }
-      umma_commit(&sh->accum_full);  // arrives once every issued MMA has completed
-    }
-  } else {
-    // ---------------- dequantizers: threads 2r and 2r+1 own weight row n0 + r;
-    //                  thread 2r+wh expands word wh of each 64-k stage
-    const int d = (tid - kDeqWarp0 * 32) >> 1, wh = tid & 1;
-    const int n = n0 + d;
-    const bool ok_row = n < N;
-    const int wpr = K / 32, G = wpr >> gshift;  // G: metadata groups per row
-    const uint4 *wrow = reinterpret_cast<const uint4 *>(W + (size_t)(ok_row ? n : 0) * wpr);
-    const uint16_t *srow = S + (size_t)(ok_row ? n : 0) * G;
-    const uint16_t *brow = Bv ? Bv + (size_t)(ok_row ? n : 0) * G : nullptr;
-    auto load = [&](int g, GroupData &gd) {  // g: 128-k unit
-      if (g < g_hi && ok_row) {
-        gd.w = __ldg(wrow + g);
-        if constexpr (G128) {  // one group per 128-k unit
-          gd.s[0] = gd.s[1] = srow[g];
-          gd.b[0] = gd.b[1] = brow ? brow[g] : (uint16_t)0;
-        } else {
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int mi = (4 * g + 2 * h + wh) >> gshift;  // group of word 2h + wh
-            gd.s[h] = srow[mi];
-            gd.b[h] = brow ? brow[mi] : (uint16_t)0;
-          }
-        }
-      } else {
-        gd.w = make_uint4(0, 0, 0, 0);
-        gd.s[0] = gd.s[1] = gd.b[0] = gd.b[1] = 0;
-      }
-    };
-    bool alive = true;
-    // fp16x2 patterns of the two dequantized values (q = 0, q = 1) of a group
-    auto pair_of = [&](uint16_t s16, uint16_t b16, uint32_t &lo2, uint32_t &hi2) {
-      const float sc = meta_f32(s16, mbf16 != 0);
-      const float bi = brow ? meta_f32(b16, mbf16 != 0) : __fmul_rn(-0.5f, sc);
-      const uint32_t lo16 = __half_as_ushort(__float2half_rn(bi));
-      const uint32_t hi16 = __half_as_ushort(__float2half_rn(__fadd_rn(sc, bi)));
-      lo2 = lo16 | (lo16 << 16);
-      hi2 = hi16 | (hi16 << 16);
-    };
-    auto process = [&](int g, const GroupData &gd) {
-      uint32_t lo2v[2], hi2v[2];
-      pair_of(gd.s[0], gd.b[0], lo2v[0], hi2v[0]);
-      if constexpr (G128) {
-        lo2v[1] = lo2v[0];
-        hi2v[1] = hi2v[0];
-      } else {
-        pair_of(gd.s[1], gd.b[1], lo2v[1], hi2v[1]);
-      }
-      if constexpr (MT == 2) {
-        // the group's two k-steps, one stage at a time: each stage is handed to
-        // the MMA as soon as it is written, so that the dequantizers can run up
-        // to STAGES stages ahead
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int ks = 2 * (g - g_lo) + h;  // this CTA's k-step
-          const int st = ks % STAGES;
-          const uint32_t ph = (uint32_t)(ks / STAGES) & 1u;
-          // one lane waits, the warp follows its verdict (keeps the warp converged)
-          int okw = 0;
-          if (lane == 0) okw = alive && mbar_wait(&sh->empty[st], ph ^ 1u, sh);
-          okw = __shfl_sync(0xffffffffu, okw, 0);
-          if (!okw) {
-            alive = false;
-            return;
-          }
-          unsigned char *rowp = sb + st * B_BYTES + d * 128;
-          const uint32_t word = h == 0 ? (wh == 0 ? gd.w.x : gd.w.y) : (wh == 0 ? gd.w.z : gd.w.w);
-          uint32_t out[16];
-          expand_word(word, lo2v[h], hi2v[h], out);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int c = wh * 4 + q;  // 16-byte chunk: k = 8c .. 8c+7 of this stage
-            *reinterpret_cast<uint4 *>(rowp + ((c ^ (d & 7)) << 4)) =
-                make_uint4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
-          }
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sh->full_b[st]);
-        }
-      } else {
-        // four stages: wait for both of the group's stages, write both, then
-        // one proxy fence and the two arrivals (halves the hand-offs; with four
-        // stages the dequantizers still run a stage ahead)
-        const int ks0 = 2 * (g - g_lo);  // this CTA's k-step
-        const int s0 = ks0 % STAGES, s1 = (ks0 + 1) % STAGES;
-        const uint32_t ph0 = (uint32_t)(ks0 / STAGES) & 1u, ph1 = (uint32_t)((ks0 + 1) / STAGES) & 1u;
-        // one lane waits, the warp follows its verdict (keeps the warp converged)
-        int okw = 0;
-        if (lane == 0)
-          okw = alive && mbar_wait(&sh->empty[s0], ph0 ^ 1u, sh) && mbar_wait(&sh->empty[s1], ph1 ^ 1u, sh);
-        okw = __shfl_sync(0xffffffffu, okw, 0);
-        if (!okw) {
-          alive = false;
-          return;
-        }
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          unsigned char *rowp = sb + (h == 0 ? s0 : s1) * B_BYTES + d * 128;
-          const uint32_t word = h == 0 ? (wh == 0 ? gd.w.x : gd.w.y) : (wh == 0 ? gd.w.z : gd.w.w);
-          uint32_t out[16];
-          expand_word(word, lo2v[h], hi2v[h], out);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int c = wh * 4 + q;  // 16-byte chunk: k = 8c .. 8c+7 of this stage
-            *reinterpret_cast<uint4 *>(rowp + ((c ^ (d & 7)) << 4)) =
-                make_uint4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
-          }
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&sh->full_b[s0]);
-          mbar_arrive(&sh->full_b[s1]);
-        }
-      }
-    };
-    GroupData r0, r1, r2;
-    load(g_lo, r0);
-    load(g_lo + 1, r1);
-    for (int g = g_lo; g < g_hi && alive; g += 3) {
-      load(g + 2, r2);
-      process(g, r0);
-      if (g + 1 >= g_hi || !alive) break;
-      load(g + 3, r0);
-      process(g + 1, r1);
-      if (g + 2 >= g_hi || !alive) break;
-      load(g + 4, r1);
-      process(g + 2, r2);
-    }
-
-    // ---------------- epilogue: warp w reads TMEM lanes 32*(w%4).., columns half (w-2)/4
-    int acc_ok = 0;
-    if (lane == 0) acc_ok = mbar_wait(&sh->accum_full, 0u, sh) && !sh->abort_flag;
-    acc_ok = __shfl_sync(0xffffffffu, acc_ok, 0);
-    if (acc_ok) {
-      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      asm volatile("griddepcontrol.wait;" ::: "memory");  // inv_scale comes from the prep kernel
-      const int quarter = warp & 3, part = (warp - kDeqWarp0) >> 2;  // 4 column quarters
-#pragma unroll 1
-      for (int mc = 0; mc < 2 * MT; ++mc) {
-        const int mt = mc >> 1, cc = mc & 1;
-        const int m = m0 + BM * mt + 32 * quarter + lane;
-        const float rs = m < M ? inv_scale[m] : 0.f;
-        const int col = part * 64 + cc * 32;
-        uint32_t v[32];
-        const uint32_t taddr = tmem_d + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(256 * mt + col);
-        asm volatile(
-            "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-            "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-            "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-            : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-              "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
-              "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]),
-              "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
-              "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
-              "=r"(v[31])
-            : "r"(taddr)
-            : "memory");
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        if (SPLIT) {
-          // this rank's partial sums stay in shared memory for the cluster reduction
-          float *prow = reinterpret_cast<float *>(sa) + (size_t)(32 * quarter + lane) * kPartStride + col;
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            *reinterpret_cast<float4 *>(prow + 4 * q) =
-                make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                            __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
-        } else if (m < M) {
-          const int n = n0 + col;
-          const size_t i0 = (size_t)m * N + n;
-          // 16-byte stores need 16-byte aligned rows: N % 8 == 0 (16-bit
-          // outputs) or N % 4 == 0 (fp32)
-          if (n + 32 <= N && (N & (ydt == Q1_F32 ? 3 : 7)) == 0) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              float f[8];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(v[8 * q + e]) * rs;
-              store8(y, i0 + 8 * q, f, ydt);
-            }
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (n + e < N) store1(y, i0 + e, __uint_as_float(v[e]) * rs, ydt);
-          }
-        }
-      }
-    }
-  }
-
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-  __syncthreads();
-  if (SPLIT) {
-    // rank r finishes rows [128 r / S, 128 (r+1) / S) of the tile: the sum of
-    // the ranks' partial tiles in rank order, scaled back and rounded once
-    cooperative_groups::cluster_group cluster = cooperative_groups::this_cluster();
-    cluster.sync();
-    asm volatile("griddepcontrol.wait;" ::: "memory");  // inv_scale comes from the prep kernel
-    const int r_lo = (BM * rank) / ksplit, r_hi = (BM * (rank + 1)) / ksplit;
-    const int nvec = (r_hi - r_lo) * (BN / 4);
-    for (int i = tid; i < nvec; i += kThreadsWide) {
-      const int r = r_lo + i / (BN / 4), c4 = i % (BN / 4);
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int q = 0; q < ksplit; ++q) {
-        const float *pq = cluster.map_shared_rank(reinterpret_cast<float *>(sa), q);
-        const float4 v = *reinterpret_cast<const float4 *>(pq + (size_t)r * kPartStride + 4 * c4);
-        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-      }
-      const int m = m0 + r, n = n0 + 4 * c4;
-      if (m < M && n < N) {
-        const float rs = inv_scale[m];
-        const size_t i0 = (size_t)m * N + n;
-        const float a4[4] = {acc.x * rs, acc.y * rs, acc.z * rs, acc.w * rs};
-        if (n + 4 <= N && (N & 3) == 0) {
-          store4(y, i0, a4, ydt);
-        } else {
-          for (int e = 0; e < 4 && n + e < N; ++e) store1(y, i0 + e, a4[e], ydt);
-        }
-      }
-    }
-    cluster.sync();  // no rank leaves while another still reads its partial tile
-  }
-  if (warp == 1) {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_d), "r"(kTmemCols)
-                 : "memory");
   }
 }
 
@@ -646,85 +233,735 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
-template <int MT, bool SPLIT, bool G128>
-cudaError_t launch_wide_mma_g(const WeightView &W, const __half *x16, int64_t M, const float *inv_scale, void *y,
-                            int ksplit, cudaStream_t st, q1_dtype dt) {
+// ======================================================================
+// Pair kernel.  Per CTA (576 threads), CTA h of the pair owning weight rows
+// n0 + 128h .. n0 + 128h + 127 of the tile:
+//   warp 0        TMA producer: this CTA's NT/2 tokens x 128 k of fp16 x per
+//                 stage (two 128B-swizzled boxes of 64 k), up to 8 stages ahead
+//   warp 1        TMEM allocation for the pair (512 columns: the fp32
+//                 accumulator in columns [0, 256), four 64-column weight
+//                 stages in [256, 512)); in the even CTA one thread issues the
+//                 pair's MMAs and commits them to both CTAs' barriers
+//   warps 2..9    dequantizers, two sets of four taking alternate stages:
+//                 thread = weight row, four words (128 k) -> 64 fp16 pairs ->
+//                 tcgen05.st; then, once this CTA's x stage has landed, one
+//                 arrival per warp on the even CTA's stage barrier
+//   warps 10..17  epilogue: tcgen05.ld -> x 2^-e_m per token -> output dtype
+//                 -> a staged tile and one TMA store per tile (16-bit outputs)
+//                 or direct stores (a warp's store covers 32 consecutive rows)
+// Tiles (256 weight rows x NT tokens) are taken persistently by the pairs;
+// the accumulator is released to the next tile as soon as it has been read.
+// With SPLIT, a cluster of S pairs shares one tile, pair p taking the p-th of
+// S contiguous k ranges, and the fp32 partial tiles are summed through
+// distributed shared memory in pair order (deterministic).
+constexpr int kPairThreads = 576;
+constexpr int kPairAStages = 4;              // 128-k weight stages in TMEM (64 columns each)
+constexpr int kPairXMax = 8;                 // at most 8 x stages of 128 k in shared memory
+constexpr uint32_t kPairDeqWarp0 = 2, kPairEpiWarp0 = 10;
+constexpr uint32_t kPairACol = 256;          // first TMEM column of the weight stages
+// Dynamic shared memory, in this order (every part 1024-byte aligned):
+//   the barriers (one 1024-byte header),
+//   the x ring: xstages x (NT/2 tokens x 128 k fp16), as many stages as fit;
+//     after the k loop of a split-K tile it holds the fp32 partial tile,
+//     token-major [NT][128] (a warp's accesses cover 32 consecutive weight rows)
+//   the 16-bit output tile [NT][128] of this CTA's rows, staged for one TMA store.
+constexpr size_t kPairSmemMax = 232448;      // the per-block opt-in limit
+constexpr size_t kPairHeader = 1024;
+
+struct __align__(8) PairShared {
+  uint64_t full_x[kPairXMax];     // this CTA's x stage landed (TMA bytes)
+  uint64_t empty_x[kPairXMax];    // the pair's MMAs reading the x stage completed (commit, both CTAs)
+  uint64_t full[kPairAStages];    // even CTA: both CTAs' weights + x of the step ready (8 warps)
+  uint64_t empty[kPairAStages];   // the pair's MMAs reading the weight stage completed (commit, both CTAs)
+  uint64_t accum_full;            // the tile's MMAs completed (commit, both CTAs)
+  uint64_t accum_empty;           // even CTA: both CTAs' epilogues loaded the accumulator (16 warps)
+  uint64_t drain;                 // final commit before the allocation is released
+  uint64_t stg_ready;             // the epilogue warps' rows of the output tile are staged (8 warps)
+  uint64_t stg_free;              // the previous tile's TMA store has read the staging buffer
+  uint32_t tmem_base;
+  volatile int abort_flag;
+};
+static_assert(sizeof(PairShared) <= kPairHeader, "barrier header");
+// x stages that fit beside the staging tile for a token tile of NT (at least 4:
+// the split-K partial tile, NT x 128 fp32, lives in the ring)
+__host__ __device__ constexpr int pair_xstages(int NT) {
+  return (int)((kPairSmemMax - 1024 - kPairHeader - (size_t)NT * 256) / ((size_t)NT * 128)) < kPairXMax
+             ? (int)((kPairSmemMax - 1024 - kPairHeader - (size_t)NT * 256) / ((size_t)NT * 128))
+             : kPairXMax;
+}
+__host__ __device__ constexpr size_t pair_smem_bytes(int NT) {
+  return 1024 + kPairHeader + (size_t)pair_xstages(NT) * NT * 128 + (size_t)NT * 256;
+}
+static_assert(pair_xstages(256) >= 4 && pair_smem_bytes(256) <= kPairSmemMax, "pair kernel shared memory");
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// the same shared-memory offset in CTA `rank` of this cluster
+__device__ __forceinline__ uint32_t mapa_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// Arrive on a barrier of another CTA of the cluster (default semantics:
+// release at CTA scope).  What the arrival publishes is complete before it:
+// tensor-memory stores are waited for (tcgen05.wait::st) and fenced, and x
+// stages were observed complete on their own barrier.  A cluster-scope
+// release measured about 1000 clocks more per arrival, on the critical path.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Bounded wait, slow path: polls the phase with the given parity until it has
+// completed, the limit runs out, or any CTA has recorded an error (the pair's
+// roles depend on each other's progress).  `sleep` spaces the polls of long
+// waits (the epilogue's) so that they take few issue slots from the
+// dequantizers.
+__device__ __noinline__ bool pair_wait_slow(uint32_t addr, uint32_t parity, PairShared *sh, int sleep) {
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t i = 0;; ++i) {
+    if (sleep) __nanosleep(sleep);
+    if (mbar_try(addr, parity)) return true;
+    if ((i & 15u) == 15u) {
+      if (sh->abort_flag || *(volatile unsigned int *)&g_wide_err) {
+        sh->abort_flag = 1;
+        return false;
+      }
+      if (globaltimer() - t0 > kWaitLimitNs) {
+        sh->abort_flag = 1;
+        atomicOr(&g_wide_err, 1u);
+        return false;
+      }
+    }
+  }
+}
+// one thread: an inline test first, the polling loop only when the phase is open
+__device__ __forceinline__ bool pair_wait(uint64_t *bar, uint32_t parity, PairShared *sh, int sleep) {
+  const uint32_t addr = smem_u32(bar);
+  return mbar_try(addr, parity) || pair_wait_slow(addr, parity, sh, sleep);
+}
+// a whole warp: every lane tests once (no divergence when the phase has
+// completed); otherwise lane 0 polls and the warp takes its verdict
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, PairShared *sh, int sleep) {
+  const uint32_t addr = smem_u32(bar);
+  if (__all_sync(0xffffffffu, mbar_try(addr, parity))) return true;
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = pair_wait_slow(addr, parity, sh, sleep);
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+__device__ __forceinline__ void umma_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// arrives on the barrier at this offset in both CTAs of the pair once every
+// MMA issued so far by this thread has completed
+__device__ __forceinline__ void umma_commit_pair(uint64_t *bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(mask)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
+      "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
+      "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
+        "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]),
+        "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]),
+        "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// 2-D tiled store from shared memory (bulk-group completion)
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(map),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// fp16x2 patterns of a group's two dequantized values (q = 0, q = 1): the
+// fp32 metadata result rounded once to fp16
+__device__ __forceinline__ void deq_pair(uint32_t s16, uint32_t b16, bool affine, bool mbf16, uint32_t &lo2,
+                                         uint32_t &hi2) {
+  const float sc = meta_f32(s16, mbf16);
+  const float bi = affine ? meta_f32(b16, mbf16) : __fmul_rn(-0.5f, sc);
+  const uint32_t lo16 = __half_as_ushort(__float2half_rn(bi));
+  const uint32_t hi16 = __half_as_ushort(__float2half_rn(__fadd_rn(sc, bi)));
+  lo2 = lo16 | (lo16 << 16);
+  hi2 = hi16 | (hi16 << 16);
+}
+
+// One 128-k stage of one weight row: four words and their metadata.
+struct PairStage {
+  uint4 w;
+  uint32_t s[4], b[4];
+};
+
+template <bool SPLIT, bool G128>
+__global__ void __launch_bounds__(kPairThreads, 1)
+pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_y,
+            const uint32_t *__restrict__ W, const uint16_t *__restrict__ S, const uint16_t *__restrict__ Bv,
+            int M, int N, int K, const float *__restrict__ inv_scale, void *__restrict__ y, int NT, int ksplit,
+            int mbf16, int ydt, int gshift, int ystage) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char *base = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  PairShared *sh = reinterpret_cast<PairShared *>(base);
+  unsigned char *ring = base + kPairHeader;
+  const int xstages = pair_xstages(NT);
+  const uint32_t XS = (uint32_t)NT * 128u;         // bytes of one x stage (NT/2 tokens x 256 B)
+  uint16_t *stg = reinterpret_cast<uint16_t *>(ring + (size_t)xstages * XS);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t crank = cluster_rank();
+  const int h = (int)(crank & 1u);                 // half of the pair: weight rows 128h ..
+  const uint32_t lead = crank & ~1u;               // the pair's even CTA
+  const uint16_t pair_mask = (uint16_t)(3u << lead);
+  const int XH = NT >> 1;                          // tokens whose x this CTA holds
+  const int KS = K / 128;                          // 128-k stages of a whole row
+  const int mtiles = (M + NT - 1) / NT, ntiles = (N + 255) / 256;
+  // this pair's tiles and k range
+  int t_first, t_step, ks_lo, ks_hi;
+  if (SPLIT) {
+    const int pr = (int)(crank >> 1);              // pair within the cluster
+    t_first = (int)(blockIdx.x / (unsigned)(2 * ksplit));
+    t_step = 1 << 30;                              // one tile per cluster
+    ks_lo = (int)(((int64_t)KS * pr) / ksplit);
+    ks_hi = (int)(((int64_t)KS * (pr + 1)) / ksplit);
+  } else {
+    t_first = (int)(blockIdx.x >> 1);
+    t_step = (int)(gridDim.x >> 1);
+    ks_lo = 0;
+    ks_hi = KS;
+  }
+  const int T = mtiles * ntiles;
+  const int nks = ks_hi - ks_lo;
+
+  if (tid == 0) {
+    for (int s = 0; s < xstages; ++s) {
+      mbar_init(&sh->full_x[s], 1);
+      mbar_init(&sh->empty_x[s], 1);
+    }
+    for (int s = 0; s < kPairAStages; ++s) {
+      mbar_init(&sh->full[s], 8);
+      mbar_init(&sh->empty[s], 1);
+    }
+    mbar_init(&sh->accum_full, 1);
+    mbar_init(&sh->accum_empty, 16);
+    mbar_init(&sh->drain, 1);
+    mbar_init(&sh->stg_ready, 8);
+    mbar_init(&sh->stg_free, 1);
+    sh->abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_x) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&sh->tmem_base)),
+                 "r"(512)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  cluster_sync_all();  // barriers initialised and TMEM allocated in every CTA of the cluster
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = sh->tmem_base;
+  const uint32_t full_lead0 = mapa_rank(smem_u32(&sh->full[0]), lead);
+  const uint32_t accum_empty_lead = mapa_rank(smem_u32(&sh->accum_empty), lead);
+
+  if (warp == 0) {
+    // ---------------- TMA producer: this CTA's token half, two 64-k boxes per stage
+    if (lane == 0) {
+      asm volatile("griddepcontrol.wait;" ::: "memory");  // x16 comes from the prep kernel
+      uint32_t s = 0, ph = 0;
+      bool ok = true;
+      for (int t = t_first; t < T && ok; t += t_step) {
+        const int m0 = (t % mtiles) * NT;
+        for (int ks = ks_lo; ks < ks_hi; ++ks) {
+          if (!(ok = pair_wait(&sh->empty_x[s], ph ^ 1u, sh, 0))) break;
+          unsigned char *dst = ring + s * XS;
+          mbar_arrive_expect_tx(&sh->full_x[s], XS);
+          tma_load_2d(dst, &tmap_x, &sh->full_x[s], ks * 128, m0 + h * XH);
+          tma_load_2d(dst + XS / 2, &tmap_x, &sh->full_x[s], ks * 128 + 64, m0 + h * XH);
+          if (++s == (uint32_t)xstages) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (even CTA)
+    if (h == 0 && lane == 0) {
+      const uint32_t idesc = (1u << 4) | ((uint32_t)(NT >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+      uint32_t it = 0, tl = 0, sx = 0;
+      bool ok = true;
+      for (int t = t_first; t < T && ok; t += t_step, ++tl) {
+        if (tl > 0 && !(ok = pair_wait(&sh->accum_empty, (tl - 1) & 1u, sh, 0))) break;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        for (int ks = 0; ks < nks; ++ks, ++it) {
+          const uint32_t s = it % kPairAStages, ph = (it / kPairAStages) & 1u;
+          if (!(ok = pair_wait(&sh->full[s], ph, sh, 0))) break;
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          const uint32_t xs = smem_u32(ring + sx * XS);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma_pair(tmem, tmem + kPairACol + 64u * s + 8u * kk,
+                      sw128_desc(xs + (kk >> 2) * (XS / 2) + (kk & 3) * 32), idesc, (ks > 0 || kk > 0) ? 1u : 0u);
+          umma_commit_pair(&sh->empty[s], pair_mask);
+          umma_commit_pair(&sh->empty_x[sx], pair_mask);
+          if (++sx == (uint32_t)xstages) sx = 0;
+        }
+        if (ok) umma_commit_pair(&sh->accum_full, pair_mask);
+      }
+      umma_commit_pair(&sh->drain, pair_mask);  // every MMA issued, complete
+    }
+    // both CTAs see the pair's last commit arrive before the allocation is released
+    if (lane == 0) pair_wait(&sh->drain, 0, sh, 0);
+  } else if (warp < (int)kPairEpiWarp0) {
+    // ---------------- dequantizers: set ds takes this CTA's stages it = ds (mod 2)
+    const int ds = (warp - (int)kPairDeqWarp0) >> 2, q = warp & 3;
+    const int r = 32 * q + lane;                   // TMEM lane = weight row of this CTA
+    const int wpr = K / 32, G = wpr >> gshift;     // words and metadata groups per row
+    const bool affine = Bv != nullptr, mb = mbf16 != 0;
+    const uint32_t a_lane = tmem + ((uint32_t)(32 * q) << 16) + kPairACol;
+    const int my_tiles = t_first < T ? (T - 1 - t_first) / t_step + 1 : 0;
+    const uint32_t total = (uint32_t)nks * (uint32_t)my_tiles;
+    // A cursor over this set's stages: tile iteration ti, k-step ks and this
+    // thread's weight row n (-1 past the last tile).  It moves two stages at a
+    // time; only a move to the next tile costs a division.
+    struct Cursor {
+      int ti, ks, n;
+    };
+    auto set_row = [&](Cursor &c) {
+      c.n = c.ti < my_tiles ? ((t_first + c.ti * t_step) / mtiles) * 256 + 128 * h + r : -1;
+    };
+    auto step2 = [&](Cursor &c) {
+      c.ks += 2;
+      if (c.ks >= ks_hi) {
+        while (c.ks >= ks_hi) {
+          c.ks -= nks;
+          ++c.ti;
+        }
+        set_row(c);
+      }
+    };
+    auto load = [&](const Cursor &c, PairStage &p) {
+      if (c.n >= 0 && c.n < N) {
+        const int n = c.n, ks = c.ks;
+        p.w = __ldg(reinterpret_cast<const uint4 *>(W + (size_t)n * wpr) + ks);
+        const uint16_t *srow = S + (size_t)n * G;
+        const uint16_t *brow = affine ? Bv + (size_t)n * G : nullptr;
+        if (G128) {
+          p.s[0] = srow[ks];
+          p.b[0] = affine ? brow[ks] : 0u;
+        } else {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int g = (4 * ks + u) >> gshift;
+            p.s[u] = srow[g];
+            p.b[u] = affine ? brow[g] : 0u;
+          }
+        }
+      } else {
+        p.w = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) p.s[u] = p.b[u] = 0u;
+      }
+    };
+    // this set's stages j, j + 2, j + 4: the loads run two of its stages ahead
+    PairStage cur, nx1, nx2;
+    uint32_t j = (uint32_t)ds;
+    uint32_t xj = (uint32_t)ds, xph = 0;           // x stage of step j and its phase (xstages >= 4)
+    Cursor pf{0, ks_lo, 0};
+    set_row(pf);
+    // stage ds may already lie in the second tile when a tile has one k-step
+    pf.ks += ds;
+    while (pf.ks >= ks_hi) {
+      pf.ks -= nks;
+      ++pf.ti;
+    }
+    set_row(pf);
+    if (j < total) load(pf, cur);
+    step2(pf);
+    if (j + 2 < total) load(pf, nx1);
+    step2(pf);
+    for (; j < total; j += 2) {
+      const uint32_t s = j % kPairAStages, ph = (j / kPairAStages) & 1u;
+      if (!warp_wait(&sh->empty[s], ph ^ 1u, sh, 0)) break;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");  // the MMAs that read the slot are done
+      const uint32_t words[4] = {cur.w.x, cur.w.y, cur.w.z, cur.w.w};
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t v[32];
+#pragma unroll
+        for (int u2 = 0; u2 < 2; ++u2) {
+          const int u = 2 * half + u2;
+          uint32_t lo2, hi2;
+          deq_pair(G128 ? cur.s[0] : cur.s[u], G128 ? cur.b[0] : cur.b[u], affine, mb, lo2, hi2);
+          uint32_t out[16];
+          expand_word(words[u], lo2, hi2, out);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[16 * u2 + e] = out[e];
+        }
+        tmem_st32(a_lane + 64u * s + 32u * half, v);
+      }
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      // this CTA's x half of the step must have landed before the pair's MMA may run
+      if (!warp_wait(&sh->full_x[xj], xph, sh, 0)) break;
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      __syncwarp();
+      // the even CTA's own warps signal at CTA scope; the odd CTA's at cluster
+      // scope.  No load is in flight here: a cluster-scope release would wait
+      // for it.
+      if (lane == 0) {
+        if (h == 0) mbar_arrive(&sh->full[s]);
+        else mbar_arrive_remote(full_lead0 + 8u * s);
+      }
+      if (j + 4 < total) load(pf, nx2);
+      step2(pf);
+      cur = nx1;
+      nx1 = nx2;
+      xj += 2;
+      if (xj >= (uint32_t)xstages) {
+        xj -= (uint32_t)xstages;
+        xph ^= 1u;
+      }
+    }
+  } else {
+    // ---------------- epilogue: warp (q, eh) reads TMEM lanes 32q.., token columns [128 eh, 128 eh + 128)
+    const int q = warp & 3, eh = (warp - (int)kPairEpiWarp0) >> 2;
+    const int r = 32 * q + lane;
+    const uint32_t d_lane = tmem + ((uint32_t)(32 * q) << 16);
+    uint32_t tl = 0;
+    bool deps = false;
+    for (int t = t_first; t < T; t += t_step, ++tl) {
+      if (!warp_wait(&sh->accum_full, tl & 1u, sh, 64)) break;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      if (!deps) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");  // inv_scale comes from the prep kernel
+        deps = true;
+      }
+      const int m0 = (t % mtiles) * NT;
+      const int n = (t / mtiles) * 256 + 128 * h + r;
+      const int c_lo = 128 * eh, c_hi = min(NT, 128 * eh + 128);
+      if (!SPLIT && ystage) {
+        // 16-bit outputs through the staging tile: the accumulator is released
+        // as soon as it is read, and one TMA store writes the CTA's 128 rows x
+        // NT tokens (clipping rows and tokens beyond N and M)
+        if (tl > 0 && !warp_wait(&sh->stg_free, (tl - 1) & 1u, sh, 0)) break;
+#pragma unroll 1
+        for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
+          const int m_l = m0 + c0 + (lane & 15);
+          const float rs_l = m_l < M ? inv_scale[m_l] : 0.f;
+          uint32_t v[16];
+          tmem_ld16(d_lane + (uint32_t)c0, v);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float f = __uint_as_float(v[e]) * __shfl_sync(0xffffffffu, rs_l, e);
+            const uint16_t o = ydt == Q1_F16 ? __half_as_ushort(__float2half_rn(f))
+                                             : __bfloat16_as_ushort(__float2bfloat16_rn(f));
+            if (c0 + e < c_hi) stg[(c0 + e) * 128 + r] = o;
+          }
+        }
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          if (h == 0) mbar_arrive(&sh->accum_empty);
+          else mbar_arrive_remote(accum_empty_lead);
+          mbar_arrive(&sh->stg_ready);
+        }
+        if (warp == (int)kPairEpiWarp0) {
+          int okw = 1;
+          if (lane == 0) {
+            okw = pair_wait(&sh->stg_ready, tl & 1u, sh, 0);
+            if (okw) {
+              tma_store_2d(&tmap_y, stg, (t / mtiles) * 256 + 128 * h, m0);
+              asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+              asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+              mbar_arrive(&sh->stg_free);
+            }
+          }
+          if (!__shfl_sync(0xffffffffu, okw, 0)) break;
+        }
+        continue;
+      }
+      for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(d_lane + (uint32_t)c0, v);
+        if (!SPLIT && c0 + 32 >= c_hi) {
+          // the accumulator's last columns of this warp are in registers
+          asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) {
+            if (h == 0) mbar_arrive(&sh->accum_empty);
+            else mbar_arrive_remote(accum_empty_lead);
+          }
+        }
+        if (SPLIT) {
+          // partial tile, token-major: column c of this rank's rows
+          float *part = reinterpret_cast<float *>(ring);
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (c0 + e < NT) part[(size_t)(c0 + e) * 128 + r] = __uint_as_float(v[e]);
+        } else {
+          const int m_l = m0 + c0 + lane;
+          const float rs_l = m_l < M ? inv_scale[m_l] : 0.f;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float rs = __shfl_sync(0xffffffffu, rs_l, e);
+            const int m = m0 + c0 + e;
+            if (c0 + e < c_hi && m < M && n < N) store1(y, (size_t)m * N + n, __uint_as_float(v[e]) * rs, ydt);
+          }
+        }
+      }
+      if (!SPLIT && c_lo >= c_hi) {  // no columns for this warp: release at once
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          if (h == 0) mbar_arrive(&sh->accum_empty);
+          else mbar_arrive_remote(accum_empty_lead);
+        }
+      }
+    }
+    // the staged tiles' stores complete before the CTA leaves
+    if (warp == (int)kPairEpiWarp0 && lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  }
+
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncwarp();
+  if (SPLIT) {
+    // the pairs' partial tiles are complete in every CTA of the cluster
+    cluster_sync_all();
+    if (!sh->abort_flag) {
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      const int t = t_first;
+      const int m0 = (t % mtiles) * NT, nb = (t / mtiles) * 256 + 128 * h;
+      const int pr = (int)(crank >> 1);
+      // pair pr finishes token columns [NT pr / S, NT (pr + 1) / S) of its half;
+      // a thread sums four consecutive weight rows over the S partials in pair order
+      const int c_lo = (NT * pr) / ksplit, c_hi = (NT * (pr + 1)) / ksplit;
+      const int items = (c_hi - c_lo) * 32;
+      for (int i = tid; i < items; i += kPairThreads) {
+        const int c = c_lo + (i >> 5), r4 = (i & 31) * 4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int p2 = 0; p2 < ksplit; ++p2) {
+          const uint32_t src = mapa_rank(smem_u32(ring), (uint32_t)(2 * p2 + h)) + (uint32_t)((c * 128 + r4) * 4);
+          float4 v;
+          asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
+                       : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                       : "r"(src)
+                       : "memory");
+          acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+        const int m = m0 + c, n = nb + r4;
+        if (m < M && n < N) {
+          const float rs = inv_scale[m];
+          const float a4[4] = {acc.x * rs, acc.y * rs, acc.z * rs, acc.w * rs};
+          const size_t i0 = (size_t)m * N + n;
+          if (n + 4 <= N && (N & 3) == 0) {
+            store4(y, i0, a4, ydt);
+          } else {
+            for (int e = 0; e < 4 && n + e < N; ++e) store1(y, i0 + e, a4[e], ydt);
+          }
+        }
+      }
+    }
+  }
+  cluster_sync_all();  // no CTA releases TMEM or leaves while its pair or cluster still uses it
+  if (warp == 1) {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512) : "memory");
+  }
+}
+
+// Active clusters of 2 * ksplit pair-kernel CTAs (one CTA per SM).
+int pair_clusters(int ksplit) {
+  static std::atomic<int> cache[kMaxDevices][5];
+  if (ksplit < 1 || ksplit > 4) return 0;
+  const int dev = current_device();
+  if (dev < kMaxDevices && cache[dev][ksplit].load(std::memory_order_relaxed) > 0)
+    return cache[dev][ksplit].load(std::memory_order_relaxed);
+  cudaFuncSetAttribute(pair_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPairSmemMax);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2 * ksplit * 16), 1, 1);
+  cfg.blockDim = dim3(kPairThreads, 1, 1);
+  cfg.dynamicSmemBytes = pair_smem_bytes(256);
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = (unsigned)(2 * ksplit);
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, pair_kernel<true, true>, &cfg) != cudaSuccess || n < 1) {
+    cudaGetLastError();
+    n = 0;
+  }
+  if (dev < kMaxDevices && n > 0) cache[dev][ksplit].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+template <bool SPLIT, bool G128>
+cudaError_t launch_pair_g(const WeightView &W, const __half *x16, int64_t M, const float *inv_scale, void *y, int NT,
+                          int ksplit, unsigned grid, cudaStream_t st, q1_dtype dt) {
   auto encode = get_encode();
   if (!encode) return cudaErrorNotSupported;
   CUtensorMap map;
   cuuint64_t gdim[2] = {(cuuint64_t)W.K, (cuuint64_t)M};
   cuuint64_t gstride[1] = {(cuuint64_t)W.K * 2};
-  cuuint32_t box[2] = {BK, (cuuint32_t)(BM * MT)};
+  cuuint32_t box[2] = {64, (cuuint32_t)(NT / 2)};
   cuuint32_t estride[2] = {1, 1};
   CUresult r = encode(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half *>(x16), gdim, gstride, box,
                       estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  // 16-bit outputs with 16-byte rows go out through the staging tile and one
+  // TMA store per tile (box: 128 weight rows x NT tokens)
+  const int ystage = !SPLIT && dt != Q1_F32 && W.N % 8 == 0 && (reinterpret_cast<uintptr_t>(y) & 15) == 0;
+  CUtensorMap ymap = map;
+  if (ystage) {
+    cuuint64_t ydim[2] = {(cuuint64_t)W.N, (cuuint64_t)M};
+    cuuint64_t ystr[1] = {(cuuint64_t)W.N * 2};
+    cuuint32_t ybox[2] = {128, (cuuint32_t)NT};
+    r = encode(&ymap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, y, ydim, ystr, ybox, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
   static std::atomic<uint64_t> attr{0};
   const int dev = current_device();
   if (not_done(attr, dev)) {
-    cudaError_t e = cudaFuncSetAttribute(wide_kernel<MT, SPLIT, G128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes<MT>);
+    cudaError_t e = cudaFuncSetAttribute(pair_kernel<SPLIT, G128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kPairSmemMax);
     if (e != cudaSuccess) return e;
     mark_done(attr, dev);
   }
-  const unsigned ntn = (unsigned)((W.N + BN - 1) / BN);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(ntn * (unsigned)(SPLIT ? ksplit : 1), (unsigned)((M + BM * MT - 1) / (BM * MT)), 1);
-  cfg.blockDim = dim3(kThreadsWide, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes<MT>;
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kPairThreads, 1, 1);
+  cfg.dynamicSmemBytes = pair_smem_bytes(NT);
   cfg.stream = st;
   cudaLaunchAttribute attrs[2];
   attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attrs[0].val.programmaticStreamSerializationAllowed = 1;
   attrs[1].id = cudaLaunchAttributeClusterDimension;
-  attrs[1].val.clusterDim.x = (unsigned)(SPLIT ? ksplit : 1);
+  attrs[1].val.clusterDim.x = (unsigned)(SPLIT ? 2 * ksplit : 2);
   attrs[1].val.clusterDim.y = 1;
   attrs[1].val.clusterDim.z = 1;
   cfg.attrs = attrs;
-  cfg.numAttrs = SPLIT ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, wide_kernel<MT, SPLIT, G128>, map, W.w, W.s, W.b, (int)M, (int)W.N, (int)W.K,
-                            inv_scale, y, SPLIT ? ksplit : 1, W.mbf16 ? 1 : 0, (int)dt, W.gshift);
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, pair_kernel<SPLIT, G128>, map, ymap, W.w, W.s, W.b, (int)M, (int)W.N, (int)W.K,
+                            inv_scale, y, NT, ksplit, W.mbf16 ? 1 : 0, (int)dt, W.gshift, ystage);
 }
 
-// 128-groups (one scale per 128-k unit) compile to their own kernel: the
-// per-word metadata of 32- and 64-groups costs the dequantizers ~5 %.
-template <int MT, bool SPLIT>
-cudaError_t launch_wide_mma(const WeightView &W, const __half *x16, int64_t M, const float *inv_scale, void *y,
-                            int ksplit, cudaStream_t st, q1_dtype dt) {
-  if (W.gshift == 2) return launch_wide_mma_g<MT, SPLIT, true>(W, x16, M, inv_scale, y, ksplit, st, dt);
-  return launch_wide_mma_g<MT, SPLIT, false>(W, x16, M, inv_scale, y, ksplit, st, dt);
-}
+// Token-tile width NT (a multiple of 16, at most 256) and split factor S
+// (1 to 4 pairs per tile) from a cost model in SM clocks: a 128-k step
+// takes 8 pair MMAs of NT/2 clocks each, or the dequantizers' floor, and
+// the tiles run in rounds over the resident pairs (or clusters of S pairs),
+// each tile adding its epilogue and, with S > 1, the partial-tile reduction.
+struct PairPlan {
+  int NT, S;
+  unsigned grid;
+};
+std::atomic<int> g_plan_nt{0}, g_plan_s{0};
 
-// Clusters of `ks` split-K CTAs that can be resident at once (one per SM).
-int wide_split_clusters(int ks) {
-  static std::atomic<int> cache[kMaxDevices][9];
-  if (ks < 2 || ks > 8) return 0;
-  const int dev = current_device();
-  if (dev < kMaxDevices && cache[dev][ks].load(std::memory_order_relaxed) > 0)
-    return cache[dev][ks].load(std::memory_order_relaxed);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(ks * 32), 1, 1);
-  cfg.blockDim = dim3(kThreadsWide, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes<1>;
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeClusterDimension;
-  attr.val.clusterDim.x = (unsigned)ks;
-  attr.val.clusterDim.y = 1;
-  attr.val.clusterDim.z = 1;
-  cfg.attrs = &attr;
-  cfg.numAttrs = 1;
-  cudaFuncSetAttribute(wide_kernel<1, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes<1>);
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, wide_kernel<1, true, true>, &cfg) != cudaSuccess || n < 1) {
-    cudaGetLastError();
-    n = 0;
+PairPlan plan_pair(int64_t M, int64_t N, int64_t K) {
+  {
+    const int NT = g_plan_nt.load(std::memory_order_relaxed), S = g_plan_s.load(std::memory_order_relaxed);
+    if (NT > 0 && (S == 1 || K / 128 >= 2 * S)) {
+      const int clusters = pair_clusters(S);
+      if (clusters > 0) {
+        const int64_t T = ((N + 255) / 256) * ((M + NT - 1) / NT);
+        return PairPlan{NT, S, S > 1 ? (unsigned)(T * 2 * S) : (unsigned)(2 * (T < clusters ? T : clusters))};
+      }
+    }
   }
-  if (dev < kMaxDevices && n > 0) cache[dev][ks].store(n, std::memory_order_relaxed);
-  return n;
+  constexpr double kDeqFloor = 560.0;   // clocks per 128-k step
+  constexpr double kEpilogue = 1500.0;  // clocks per tile
+  constexpr double kReduce = 2500.0;    // clocks per split tile
+  const int64_t KS = K / 128, ntn = (N + 255) / 256;
+  PairPlan best{256, 1, 0};
+  double best_cost = 1e300;
+  for (int S = 1; S <= 4; ++S) {
+    if (S > 1 && KS < 2 * S) continue;
+    const int clusters = pair_clusters(S);
+    if (clusters < 1) continue;
+    for (int NT = 256; NT >= 16; NT -= 16) {
+      const int64_t T = ntn * ((M + NT - 1) / NT);
+      const int64_t rounds = (T + clusters - 1) / clusters;
+      const double step = 4.0 * NT > kDeqFloor ? 4.0 * NT : kDeqFloor;
+      const double cost = (double)rounds * ((double)((KS + S - 1) / S) * step + kEpilogue + (S > 1 ? kReduce : 0.0));
+      if (cost < best_cost * 0.999) {
+        best_cost = cost;
+        best.NT = NT;
+        best.S = S;
+        best.grid = S > 1 ? (unsigned)(T * 2 * S) : (unsigned)(2 * (T < clusters ? T : clusters));
+      }
+    }
+  }
+  return best;
+}
+
+cudaError_t launch_pair(const WeightView &W, const __half *x16, int64_t M, const float *inv_scale, void *y,
+                        cudaStream_t st, q1_dtype dt) {
+  const PairPlan p = plan_pair(M, W.N, W.K);
+  if (p.grid == 0) return cudaErrorInvalidConfiguration;
+  const bool g128 = W.gshift == 2;
+  if (p.S > 1) {
+    return g128 ? launch_pair_g<true, true>(W, x16, M, inv_scale, y, p.NT, p.S, p.grid, st, dt)
+                : launch_pair_g<true, false>(W, x16, M, inv_scale, y, p.NT, p.S, p.grid, st, dt);
+  }
+  return g128 ? launch_pair_g<false, true>(W, x16, M, inv_scale, y, p.NT, 1, p.grid, st, dt)
+              : launch_pair_g<false, false>(W, x16, M, inv_scale, y, p.NT, 1, p.grid, st, dt);
 }
 
 }  // namespace
+
+void set_pair_plan(int token_tile, int split) {
+  const bool ok = token_tile >= 16 && token_tile <= 256 && token_tile % 16 == 0 && split >= 1 && split <= 4;
+  g_plan_s.store(ok ? split : 0, std::memory_order_relaxed);
+  g_plan_nt.store(ok ? token_tile : 0, std::memory_order_relaxed);
+}
 
 size_t wide_workspace_bytes(int64_t M, int64_t K) {
   const size_t x16 = ((size_t)(M * K * 2) + 255) / 256 * 256;
@@ -747,45 +984,9 @@ cudaError_t launch_wide(const WeightView &W, const void *x, int64_t M, void *y, 
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  // 2. the tcgen05 kernel, launched as a programmatic dependent of the prep:
-  //    barrier set-up, TMEM allocation and the first weight tiles overlap it.
-  //    Two token tiles per CTA when that takes fewer CTA-times: one CTA runs
-  //    per SM, a CTA with two tiles takes ~1.5x the time of one with a single
-  //    tile (measured), and the waves are whole.
-  int sms = 0, dev = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (sms <= 0) sms = 1;
-  const int64_t ntiles = (W.N + BN - 1) / BN;
-  const int64_t tiles1 = ntiles * ((M + BM - 1) / BM);
-  // Cost in CTA-times of a single-tile CTA over all of K: whole waves of
-  // resident CTAs (one per SM) x the time of one CTA.  A CTA with two token
-  // tiles takes ~1.5x (measured); a split-K CTA 1/S of it plus its share of
-  // the cluster reduction.
-  double best = (double)((tiles1 + sms - 1) / sms);
-  int mode = 1, best_split = 1;
-  if (M > BM) {
-    const int64_t tiles2 = ntiles * ((M + 2 * BM - 1) / (2 * BM));
-    const double c2 = 1.5 * (double)((tiles2 + sms - 1) / sms);
-    if (c2 < best) {
-      best = c2;
-      mode = 2;
-    }
-  }
-  const int GK = (int)(W.K / 128);
-  for (int ks = 2; ks <= 8 && ks <= GK / 2; ++ks) {
-    const int active = wide_split_clusters(ks);
-    if (active < 1) continue;
-    const double c = (double)((tiles1 + active - 1) / active) * (1.0 / ks + 0.05);
-    if (c < 0.9 * best) {
-      best = c;
-      mode = 3;
-      best_split = ks;
-    }
-  }
-  if (mode == 2) return launch_wide_mma<2, false>(W, x16, M, inv_scale, y, 1, st, dt);
-  if (mode == 3) return launch_wide_mma<1, true>(W, x16, M, inv_scale, y, best_split, st, dt);
-  return launch_wide_mma<1, false>(W, x16, M, inv_scale, y, 1, st, dt);
+  // 2. the pair kernel, launched as a programmatic dependent of the prep:
+  //    barrier set-up, TMEM allocation and the first weight stages overlap it
+  return launch_pair(W, x16, M, inv_scale, y, st, dt);
 }
 
 unsigned int read_and_clear_wide_errors(cudaStream_t st, cudaError_t *err) {

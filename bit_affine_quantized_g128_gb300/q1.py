@@ -22,7 +22,7 @@ _DT = {torch.bfloat16: Q1_BF16, torch.float16: Q1_F16, torch.float32: Q1_F32}
 # every symbol include/q1.h declares
 EXPORTED = [
     "q1_pack", "q1_unpack", "q1_dequantize", "q1_qmv", "q1_qmm_workspace_size",
-    "q1_qmm_narrow", "q1_qmm", "q1_set_qmm_max_rows", "q1_get_qmm_max_rows",
+    "q1_qmm_narrow", "q1_qmm", "q1_set_qmm_max_rows", "q1_get_qmm_max_rows", "q1_set_prefill_plan",
     "q1_embed_gather", "q1_ffn_workspace_size", "q1_ffn_fused", "q1_check_symmetric",
     "q1_device_errors", "q1_status_string", "q1_ffn_fused_noalloc",
     "q1_decode_chain_workspace_size", "q1_decode_chain", "q1_pack_from_dense",
@@ -78,6 +78,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "q1_qmm": ([W, P, I64, I32, P, P, SZ, P], I32),
         "q1_set_qmm_max_rows": ([ctypes.c_int], None),
         "q1_get_qmm_max_rows": ([], ctypes.c_int),
+        "q1_set_prefill_plan": ([ctypes.c_int, ctypes.c_int], None),
         "q1_embed_gather": ([W, P, I64, I32, P, P, P], I32),
         "q1_ffn_workspace_size": ([I64, I64, I64], SZ),
         "q1_ffn_fused": ([W, W, W, P, I64, I32, P, P, SZ, P], I32),
@@ -294,6 +295,12 @@ def qmm(W: Q1Weight, x: torch.Tensor, workspace: Optional[torch.Tensor] = None,
 
 def set_qmm_max_rows(rows: int):
     lib().q1_set_qmm_max_rows(int(rows))
+
+
+def set_prefill_plan(token_tile: int = 0, split: int = 0):
+    """Fixed prefill tiling (token_tile tokens x 256 weight rows per tile,
+    split CTA pairs per tile); (0, 0) restores the automatic choice."""
+    lib().q1_set_prefill_plan(int(token_tile), int(split))
 
 
 def get_qmm_max_rows() -> int:

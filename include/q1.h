@@ -157,12 +157,13 @@ q1_status q1_pack_from_dense(const void *dense, q1_dtype in_t, int64_t N, int64_
  *   matrix multiplies of up to 8 flattened rows).  Leading dimensions are
  *   flattened by the caller: x [B][T][K] is passed as M = B*T.
  * q1_qmm: any M >= 1.  M <= q1_get_qmm_max_rows() runs the narrow path;
- *   wider M runs the prefill path, which dequantizes weight tiles in shared
- *   memory and multiplies them on the tcgen05 tensor cores (no dense weight
- *   temporary).  Its tiles are fp16: symmetric weights are exact and affine
- *   ones rounded once at 2^-11; the activations enter as fp16 rows scaled by
- *   a power of two per row (kept in the workspace), which is exact for every
- *   activation whose scaled value is a normal fp16 number.
+ *   wider M runs the prefill path, which dequantizes weight stages straight
+ *   into tensor memory and multiplies them on the tcgen05 tensor cores of CTA
+ *   pairs (no dense weight temporary).  Its operands are fp16: symmetric
+ *   weights are exact and affine ones rounded once at 2^-11; the activations
+ *   enter as fp16 rows scaled by a power of two per row (kept in the
+ *   workspace), which is exact for every activation whose scaled value is a
+ *   normal fp16 number.
  * The narrow kernel covers K <= 40960 (a cluster of at most 8 CTAs, each
  * holding at most 10 spans of 512 k): q1_qmv and q1_qmm_narrow return
  * Q1_ERR_SHAPE above it, and q1_qmm runs such K on the prefill path for any
@@ -181,6 +182,16 @@ q1_status q1_qmm(const q1_weight *W, const void *x, int64_t M, q1_dtype dtype, v
  * Q1_QMM_MAX_ROWS, if set, gives the initial value when the library loads. */
 void q1_set_qmm_max_rows(int rows);
 int q1_get_qmm_max_rows(void);
+/* Tiling of the prefill path (no counterpart on the pages; a tuning and test
+ * control).  By default (0, 0) each call picks it from the shape: tiles of
+ * 256 weight rows x token_tile tokens, token_tile a multiple of 16 in
+ * [16, 256], each shared by `split` CTA pairs (1..4) that take contiguous k
+ * ranges and sum their partial tiles in a fixed order.  A pair set here is
+ * used by every later prefill call (with split > 1, by those whose K holds at
+ * least 2 * split groups of 128; others fall back to the automatic choice);
+ * values outside those ranges restore the automatic choice.  Results are the same for every tiling up to the fp32
+ * summation order. */
+void q1_set_prefill_plan(int token_tile, int split);
 
 /* ---- embedding gather (higgs PR #212, "What": Q1 embeddings) --------------
  * out[t][:] = dequant(E row ids[t]) in out_t, bit-exact like q1_dequantize.

@@ -247,6 +247,55 @@ def test_wide_large_and_tiny_activations(q1):
                  O.dequantize_f32(t.words, t.scales, None, K), "wide scaled rows")
 
 
+@pytest.fixture
+def prefill_plan(q1):
+    yield q1.set_prefill_plan
+    q1.set_prefill_plan(0, 0)
+
+
+# every token-tile width class and split factor of the pair kernel, forced:
+# persistent tiles (split 1) with the staged TMA-store epilogue (N % 8 == 0)
+# and the direct one (N % 8 != 0, fp32 outputs), and split-K clusters of 2..4
+# pairs summing partial tiles through distributed shared memory
+@pytest.mark.parametrize("affine", [False, True])
+@pytest.mark.parametrize("NT,S", [(16, 1), (48, 1), (128, 1), (208, 1), (256, 1), (128, 2), (64, 3), (256, 4)])
+def test_prefill_forced_plans(q1, prefill_plan, NT, S, affine):
+    M, N, K = 300, 768, 2048
+    t, x = _case(N, K, M, affine, seed=NT + 7 * S + affine)
+    W = q1.Q1Weight.from_host(t)
+    prefill_plan(NT, S)
+    y = q1.qmm(W, x.to(DEV))
+    check_matmul(y, O.qmm(x, t.words, t.scales, t.biases, K), x,
+                 O.dequantize_f32(t.words, t.scales, t.biases, K), f"prefill plan NT={NT} S={S}")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("NT,S", [(208, 1), (96, 2)])
+def test_prefill_forced_plans_ragged(q1, prefill_plan, dtype, NT, S):
+    M, N, K = 250, 600, 1280
+    t = synth.q1_tensor(N, K, seed=801 + NT, affine=True)
+    x = _acts(M, K, 802 + S, dtype)
+    W = q1.Q1Weight.from_host(t)
+    prefill_plan(NT, S)
+    y = q1.qmm(W, x.to(DEV))
+    assert y.dtype == dtype
+    check_matmul(y, O.qmm(x, t.words, t.scales, t.biases, K), x,
+                 O.dequantize_f32(t.words, t.scales, t.biases, K), f"prefill ragged NT={NT} S={S} {dtype}")
+
+
+@pytest.mark.parametrize("group", [32, 64])
+@pytest.mark.parametrize("NT,S", [(144, 1), (80, 3)])
+def test_prefill_forced_plans_small_groups(q1, prefill_plan, group, NT, S):
+    M, N, K = 200, 512, 1536
+    t = synth.q1_tensor(N, K, seed=811 + group, affine=True, group=group)
+    x = synth.activations(M, K, seed=812)
+    W = q1.Q1Weight.from_host(t)
+    prefill_plan(NT, S)
+    y = q1.qmm(W, x.to(DEV))
+    check_matmul(y, O.qmm(x, t.words, t.scales, t.biases, K), x,
+                 O.dequantize_f32(t.words, t.scales, t.biases, K), f"prefill g{group} NT={NT} S={S}")
+
+
 def test_wide_workspace_required(q1):
     t, x = _case(256, 1024, 64, False, seed=1)
     W = q1.Q1Weight.from_host(t)
