@@ -255,10 +255,15 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 // S contiguous k ranges, and the fp32 partial tiles are summed through
 // distributed shared memory in pair order (deterministic).
 constexpr int kPairThreads = 576;
-constexpr int kPairAStages = 4;              // 128-k weight stages in TMEM (64 columns each)
+// TMEM (512 columns): the fp32 accumulator of a tile takes NT columns, a
+// 128-k weight stage 64.  Token tiles up to 160 get two accumulators
+// ([0, NT) and [160, 160 + NT)) and three weight stages in [320, 512): the
+// epilogue of one tile then runs under the next tile's MMAs.  Wider tiles get
+// one accumulator in [0, 256) and four weight stages in [256, 512).
+constexpr int kPairAStages = 4;              // at most 4 weight stages
+constexpr int kPairDbufMaxNT = 160;          // widest token tile with two accumulators
 constexpr int kPairXMax = 8;                 // at most 8 x stages of 128 k in shared memory
 constexpr uint32_t kPairDeqWarp0 = 2, kPairEpiWarp0 = 10;
-constexpr uint32_t kPairACol = 256;          // first TMEM column of the weight stages
 // Dynamic shared memory, in this order (every part 1024-byte aligned):
 //   the barriers (one 1024-byte header),
 //   the x ring: xstages x (NT/2 tokens x 128 k fp16), as many stages as fit;
@@ -273,8 +278,8 @@ struct __align__(8) PairShared {
   uint64_t empty_x[kPairXMax];    // the pair's MMAs reading the x stage completed (commit, both CTAs)
   uint64_t full[kPairAStages];    // even CTA: both CTAs' weights + x of the step ready (8 warps)
   uint64_t empty[kPairAStages];   // the pair's MMAs reading the weight stage completed (commit, both CTAs)
-  uint64_t accum_full;            // the tile's MMAs completed (commit, both CTAs)
-  uint64_t accum_empty;           // even CTA: both CTAs' epilogues loaded the accumulator (16 warps)
+  uint64_t accum_full[2];         // the tile's MMAs completed (commit, both CTAs), per accumulator
+  uint64_t accum_empty[2];        // even CTA: both CTAs' epilogues loaded the accumulator (16 warps)
   uint64_t drain;                 // final commit before the allocation is released
   uint64_t stg_ready;             // the epilogue warps' rows of the output tile are staged (8 warps)
   uint64_t stg_free;              // the previous tile's TMA store has read the staging buffer
@@ -406,17 +411,6 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void 
                : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
-      : "r"(taddr)
-      : "memory");
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
 // fp16x2 patterns of a group's two dequantized values (q = 0, q = 1): the
 // fp32 metadata result rounded once to fp16
 __device__ __forceinline__ void deq_pair(uint32_t s16, uint32_t b16, bool affine, bool mbf16, uint32_t &lo2,
@@ -484,8 +478,10 @@ pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
       mbar_init(&sh->full[s], 8);
       mbar_init(&sh->empty[s], 1);
     }
-    mbar_init(&sh->accum_full, 1);
-    mbar_init(&sh->accum_empty, 16);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sh->accum_full[b], 1);
+      mbar_init(&sh->accum_empty[b], 16);
+    }
     mbar_init(&sh->drain, 1);
     mbar_init(&sh->stg_ready, 8);
     mbar_init(&sh->stg_free, 1);
@@ -505,7 +501,10 @@ pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = sh->tmem_base;
   const uint32_t full_lead0 = mapa_rank(smem_u32(&sh->full[0]), lead);
-  const uint32_t accum_empty_lead = mapa_rank(smem_u32(&sh->accum_empty), lead);
+  const uint32_t accum_empty_lead0 = mapa_rank(smem_u32(&sh->accum_empty[0]), lead);
+  // accumulators and weight stages in TMEM (see kPairDbufMaxNT)
+  const bool dbuf = !SPLIT && NT <= kPairDbufMaxNT;
+  const uint32_t SA = dbuf ? 3u : 4u, a_col0 = 512u - 64u * SA, nbuf = dbuf ? 2u : 1u;
 
   if (warp == 0) {
     // ---------------- TMA producer: this CTA's token half, two 64-k boxes per stage
@@ -532,25 +531,30 @@ pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
     // ---------------- MMA issuer (even CTA)
     if (h == 0 && lane == 0) {
       const uint32_t idesc = (1u << 4) | ((uint32_t)(NT >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
-      uint32_t it = 0, tl = 0, sx = 0;
+      uint32_t s = 0, ph = 0, tl = 0, sx = 0;
       bool ok = true;
       for (int t = t_first; t < T && ok; t += t_step, ++tl) {
-        if (tl > 0 && !(ok = pair_wait(&sh->accum_empty, (tl - 1) & 1u, sh, 0))) break;
+        // accumulator b of this tile, used for the u-th time
+        const uint32_t b = tl % nbuf, u = tl / nbuf, d_tmem = tmem + 160u * b;
+        if (u > 0 && !(ok = pair_wait(&sh->accum_empty[b], (u - 1) & 1u, sh, 0))) break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        for (int ks = 0; ks < nks; ++ks, ++it) {
-          const uint32_t s = it % kPairAStages, ph = (it / kPairAStages) & 1u;
+        for (int ks = 0; ks < nks; ++ks) {
           if (!(ok = pair_wait(&sh->full[s], ph, sh, 0))) break;
           asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
           const uint32_t xs = smem_u32(ring + sx * XS);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            umma_pair(tmem, tmem + kPairACol + 64u * s + 8u * kk,
+            umma_pair(d_tmem, tmem + a_col0 + 64u * s + 8u * kk,
                       sw128_desc(xs + (kk >> 2) * (XS / 2) + (kk & 3) * 32), idesc, (ks > 0 || kk > 0) ? 1u : 0u);
           umma_commit_pair(&sh->empty[s], pair_mask);
           umma_commit_pair(&sh->empty_x[sx], pair_mask);
           if (++sx == (uint32_t)xstages) sx = 0;
+          if (++s == SA) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
-        if (ok) umma_commit_pair(&sh->accum_full, pair_mask);
+        if (ok) umma_commit_pair(&sh->accum_full[b], pair_mask);
       }
       umma_commit_pair(&sh->drain, pair_mask);  // every MMA issued, complete
     }
@@ -562,7 +566,7 @@ pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
     const int r = 32 * q + lane;                   // TMEM lane = weight row of this CTA
     const int wpr = K / 32, G = wpr >> gshift;     // words and metadata groups per row
     const bool affine = Bv != nullptr, mb = mbf16 != 0;
-    const uint32_t a_lane = tmem + ((uint32_t)(32 * q) << 16) + kPairACol;
+    const uint32_t a_lane = tmem + ((uint32_t)(32 * q) << 16) + a_col0;
     const int my_tiles = t_first < T ? (T - 1 - t_first) / t_step + 1 : 0;
     const uint32_t total = (uint32_t)nks * (uint32_t)my_tiles;
     // A cursor over this set's stages: tile iteration ti, k-step ks and this
@@ -611,6 +615,7 @@ pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
     PairStage cur, nx1, nx2;
     uint32_t j = (uint32_t)ds;
     uint32_t xj = (uint32_t)ds, xph = 0;           // x stage of step j and its phase (xstages >= 4)
+    uint32_t s = (uint32_t)ds, ph = 0;             // weight stage of step j and its phase (SA >= 3)
     Cursor pf{0, ks_lo, 0};
     set_row(pf);
     // stage ds may already lie in the second tile when a tile has one k-step
@@ -625,7 +630,6 @@ pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
     if (j + 2 < total) load(pf, nx1);
     step2(pf);
     for (; j < total; j += 2) {
-      const uint32_t s = j % kPairAStages, ph = (j / kPairAStages) & 1u;
       if (!warp_wait(&sh->empty[s], ph ^ 1u, sh, 0)) break;
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");  // the MMAs that read the slot are done
       const uint32_t words[4] = {cur.w.x, cur.w.y, cur.w.z, cur.w.w};
@@ -665,16 +669,23 @@ pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         xj -= (uint32_t)xstages;
         xph ^= 1u;
       }
+      s += 2;
+      if (s >= SA) {
+        s -= SA;
+        ph ^= 1u;
+      }
     }
   } else {
-    // ---------------- epilogue: warp (q, eh) reads TMEM lanes 32q.., token columns [128 eh, 128 eh + 128)
+    // ---------------- epilogue: warp (q, eh) reads TMEM lanes 32q.. and half eh of the token columns
     const int q = warp & 3, eh = (warp - (int)kPairEpiWarp0) >> 2;
     const int r = 32 * q + lane;
-    const uint32_t d_lane = tmem + ((uint32_t)(32 * q) << 16);
     uint32_t tl = 0;
     bool deps = false;
     for (int t = t_first; t < T; t += t_step, ++tl) {
-      if (!warp_wait(&sh->accum_full, tl & 1u, sh, 64)) break;
+      const uint32_t b = tl % nbuf, u = tl / nbuf;
+      const uint32_t d_lane = tmem + ((uint32_t)(32 * q) << 16) + 160u * b;
+      const uint32_t accum_empty_lead = accum_empty_lead0 + 8u * b;
+      if (!warp_wait(&sh->accum_full[b], u & 1u, sh, 64)) break;
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       if (!deps) {
         asm volatile("griddepcontrol.wait;" ::: "memory");  // inv_scale comes from the prep kernel
@@ -682,20 +693,22 @@ pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
       }
       const int m0 = (t % mtiles) * NT;
       const int n = (t / mtiles) * 256 + 128 * h + r;
-      const int c_lo = 128 * eh, c_hi = min(NT, 128 * eh + 128);
+      // the two warps of a lane quarter take halves of the NT columns (multiples of 16)
+      const int chalf = ((NT >> 1) + 15) & ~15;
+      const int c_lo = eh * chalf, c_hi = min(NT, c_lo + chalf);
       if (!SPLIT && ystage) {
         // 16-bit outputs through the staging tile: the accumulator is released
         // as soon as it is read, and one TMA store writes the CTA's 128 rows x
         // NT tokens (clipping rows and tokens beyond N and M)
         if (tl > 0 && !warp_wait(&sh->stg_free, (tl - 1) & 1u, sh, 0)) break;
 #pragma unroll 1
-        for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
-          const int m_l = m0 + c0 + (lane & 15);
+        for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
+          const int m_l = m0 + c0 + lane;
           const float rs_l = m_l < M ? inv_scale[m_l] : 0.f;
-          uint32_t v[16];
-          tmem_ld16(d_lane + (uint32_t)c0, v);
+          uint32_t v[32];
+          tmem_ld32(d_lane + (uint32_t)c0, v);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
+          for (int e = 0; e < 32; ++e) {
             const float f = __uint_as_float(v[e]) * __shfl_sync(0xffffffffu, rs_l, e);
             const uint16_t o = ydt == Q1_F16 ? __half_as_ushort(__float2half_rn(f))
                                              : __bfloat16_as_ushort(__float2bfloat16_rn(f));
@@ -706,7 +719,7 @@ pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) {
-          if (h == 0) mbar_arrive(&sh->accum_empty);
+          if (h == 0) mbar_arrive(&sh->accum_empty[b]);
           else mbar_arrive_remote(accum_empty_lead);
           mbar_arrive(&sh->stg_ready);
         }
@@ -733,7 +746,7 @@ pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
           asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
           __syncwarp();
           if (lane == 0) {
-            if (h == 0) mbar_arrive(&sh->accum_empty);
+            if (h == 0) mbar_arrive(&sh->accum_empty[b]);
             else mbar_arrive_remote(accum_empty_lead);
           }
         }
@@ -758,7 +771,7 @@ pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
         __syncwarp();
         if (lane == 0) {
-          if (h == 0) mbar_arrive(&sh->accum_empty);
+          if (h == 0) mbar_arrive(&sh->accum_empty[b]);
           else mbar_arrive_remote(accum_empty_lead);
         }
       }
@@ -895,10 +908,13 @@ cudaError_t launch_pair_g(const WeightView &W, const __half *x16, int64_t M, con
 }
 
 // Token-tile width NT (a multiple of 16, at most 256) and split factor S
-// (1 to 4 pairs per tile) from a cost model in SM clocks: a 128-k step
-// takes 8 pair MMAs of NT/2 clocks each, or the dequantizers' floor, and
-// the tiles run in rounds over the resident pairs (or clusters of S pairs),
-// each tile adding its epilogue and, with S > 1, the partial-tile reduction.
+// (1 to 4 pairs per tile) from a cost model in SM clocks, fitted to forced
+// plans on GB300: a 128-k step of a pair takes about 1024 clocks for any NT up
+// to 256 (8 MMAs of K = 16; narrower N does not shorten them, so wide tiles
+// are cheaper per token), the tiles run in rounds over the resident pairs (or
+// clusters of S pairs), consecutive single-accumulator tiles are separated
+// by the epilogue stall (~24 NT) and a split tile adds its partial-tile
+// reduction (~48 NT).  Ties go to the narrowest tile.
 struct PairPlan {
   int NT, S;
   unsigned grid;
@@ -916,9 +932,9 @@ PairPlan plan_pair(int64_t M, int64_t N, int64_t K) {
       }
     }
   }
-  constexpr double kDeqFloor = 560.0;   // clocks per 128-k step
-  constexpr double kEpilogue = 1500.0;  // clocks per tile
-  constexpr double kReduce = 2500.0;    // clocks per split tile
+  constexpr double kStep = 1024.0;      // clocks per 128-k step of a pair
+  constexpr double kEpilogue = 24.0;    // x NT clocks per single-accumulator tile
+  constexpr double kReduce = 48.0;      // x NT clocks per split tile
   const int64_t KS = K / 128, ntn = (N + 255) / 256;
   PairPlan best{256, 1, 0};
   double best_cost = 1e300;
@@ -926,11 +942,12 @@ PairPlan plan_pair(int64_t M, int64_t N, int64_t K) {
     if (S > 1 && KS < 2 * S) continue;
     const int clusters = pair_clusters(S);
     if (clusters < 1) continue;
-    for (int NT = 256; NT >= 16; NT -= 16) {
+    for (int NT = 16; NT <= 256; NT += 16) {
       const int64_t T = ntn * ((M + NT - 1) / NT);
       const int64_t rounds = (T + clusters - 1) / clusters;
-      const double step = 4.0 * NT > kDeqFloor ? 4.0 * NT : kDeqFloor;
-      const double cost = (double)rounds * ((double)((KS + S - 1) / S) * step + kEpilogue + (S > 1 ? kReduce : 0.0));
+      const bool dbuf = S == 1 && NT <= kPairDbufMaxNT;
+      const double cost = (double)rounds * ((double)((KS + S - 1) / S) * kStep + (S > 1 ? kReduce * NT : 0.0)) +
+                          (dbuf ? 0.0 : (double)(rounds - 1) * kEpilogue * NT);
       if (cost < best_cost * 0.999) {
         best_cost = cost;
         best.NT = NT;
