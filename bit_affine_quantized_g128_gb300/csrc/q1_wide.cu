@@ -177,18 +177,31 @@ __device__ __forceinline__ void load8(const void *__restrict__ row, int i, float
 // e_m = 14 - floor(log2(max_k |x[m][k]|)) so that the row maximum lands in
 // [2^14, 2^15).  Multiplying by a power of two is exact; the fp16 rounding is
 // exact for every bf16 or fp16 activation whose scaled value is a normal fp16
-// number, and rounds fp32 activations once (2^-11).  One warp per row.
+// number, and rounds fp32 activations once (2^-11).  One block of 256 threads
+// per row: the maximum pass keeps four independent loads in flight per
+// thread, and the conversion pass reads the row again (mostly from L2).
+constexpr int kPrepThreads = 256;
 template <int XDT>
-__global__ void __launch_bounds__(256) x_to_f16_kernel(const void *__restrict__ x, int M,
-                                                       int K, __half *__restrict__ x16,
-                                                       float *__restrict__ inv_scale) {
+__global__ void __launch_bounds__(kPrepThreads) x_to_f16_kernel(const void *__restrict__ x, int K,
+                                                                __half *__restrict__ x16,
+                                                                float *__restrict__ inv_scale) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-  if (warp >= M) return;
-  const void *row = static_cast<const char *>(x) + (size_t)warp * K * (XDT == Q1_F32 ? 4 : 2);
+  __shared__ float wmax[kPrepThreads / 32];
+  const int m = blockIdx.x, tid = threadIdx.x;
+  const void *row = static_cast<const char *>(x) + (size_t)m * K * (XDT == Q1_F32 ? 4 : 2);
   const int n8 = K / 8;  // chunks of 8 activations
   float mx = 0.f;
-  for (int i = lane; i < n8; i += 32) {
+  int i = tid;
+  for (; i + 3 * kPrepThreads < n8; i += 4 * kPrepThreads) {
+    float f[4][8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) load8<XDT>(row, i + u * kPrepThreads, f[u]);
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) mx = fmaxf(mx, fabsf(f[u][j]));
+  }
+  for (; i < n8; i += kPrepThreads) {
     float f[8];
     load8<XDT>(row, i, f);
 #pragma unroll
@@ -196,6 +209,11 @@ __global__ void __launch_bounds__(256) x_to_f16_kernel(const void *__restrict__ 
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if ((tid & 31) == 0) wmax[tid >> 5] = mx;
+  __syncthreads();
+  mx = wmax[0];
+#pragma unroll
+  for (int w = 1; w < kPrepThreads / 32; ++w) mx = fmaxf(mx, wmax[w]);
   int e = 0;
   if (mx > 0.f && mx <= 3.0e38f) {
     const int E = (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127;  // floor(log2) for normal mx
@@ -205,19 +223,20 @@ __global__ void __launch_bounds__(256) x_to_f16_kernel(const void *__restrict__ 
   }
   const float sc = __uint_as_float((uint32_t)(127 + e) << 23);   // 2^e, exact
   const float isc = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e, exact
-  uint4 *out = reinterpret_cast<uint4 *>(x16 + (size_t)warp * K);
-  for (int i = lane; i < n8; i += 32) {
+  uint4 *out = reinterpret_cast<uint4 *>(x16 + (size_t)m * K);
+#pragma unroll 4
+  for (int c = tid; c < n8; c += kPrepThreads) {
     float f[8];
-    load8<XDT>(row, i, f);
+    load8<XDT>(row, c, f);
     uint32_t o[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const __half2 h = __floats2half2_rn(f[2 * q] * sc, f[2 * q + 1] * sc);
       o[q] = *reinterpret_cast<const uint32_t *>(&h);
     }
-    out[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    out[c] = make_uint4(o[0], o[1], o[2], o[3]);
   }
-  if (lane == 0) inv_scale[warp] = isc;
+  if (tid == 0) inv_scale[m] = isc;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -387,6 +406,20 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
       "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
       "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
       "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+// 32 columns of this warp's 32 lanes; tcgen05.wait::ld before the values are used
+__device__ __forceinline__ void tmem_ld32_issue(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
+        "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]),
+        "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]),
+        "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr)
       : "memory");
 }
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
@@ -701,28 +734,52 @@ pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         // as soon as it is read, and one TMA store writes the CTA's 128 rows x
         // NT tokens (clipping rows and tokens beyond N and M)
         if (tl > 0 && !warp_wait(&sh->stg_free, (tl - 1) & 1u, sh, 0)) break;
+        // 64 columns per round: two loads, one wait; the accumulator is
+        // released right after the last round's loads, before its conversion
+        bool released = false;
 #pragma unroll 1
-        for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
-          const int m_l = m0 + c0 + lane;
-          const float rs_l = m_l < M ? inv_scale[m_l] : 0.f;
-          uint32_t v[32];
-          tmem_ld32(d_lane + (uint32_t)c0, v);
+        for (int c0 = c_lo; c0 < c_hi; c0 += 64) {
+          const int ma = m0 + c0 + lane, mb = ma + 32;
+          const float rs_a = ma < M ? inv_scale[ma] : 0.f, rs_b = mb < M ? inv_scale[mb] : 0.f;
+          uint32_t va[32], vb[32];
+          tmem_ld32_issue(d_lane + (uint32_t)c0, va);
+          tmem_ld32_issue(d_lane + (uint32_t)(c0 + 32), vb);
+          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+          if (c0 + 64 >= c_hi) {
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) {
+              if (h == 0) mbar_arrive(&sh->accum_empty[b]);
+              else mbar_arrive_remote(accum_empty_lead);
+            }
+            released = true;
+          }
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            const float f = __uint_as_float(v[e]) * __shfl_sync(0xffffffffu, rs_l, e);
+            const float f = __uint_as_float(va[e]) * __shfl_sync(0xffffffffu, rs_a, e);
             const uint16_t o = ydt == Q1_F16 ? __half_as_ushort(__float2half_rn(f))
                                              : __bfloat16_as_ushort(__float2bfloat16_rn(f));
             if (c0 + e < c_hi) stg[(c0 + e) * 128 + r] = o;
           }
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float f = __uint_as_float(vb[e]) * __shfl_sync(0xffffffffu, rs_b, e);
+            const uint16_t o = ydt == Q1_F16 ? __half_as_ushort(__float2half_rn(f))
+                                             : __bfloat16_as_ushort(__float2bfloat16_rn(f));
+            if (c0 + 32 + e < c_hi) stg[(c0 + 32 + e) * 128 + r] = o;
+          }
         }
-        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        if (!released) {  // no columns for this warp
+          asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) {
+            if (h == 0) mbar_arrive(&sh->accum_empty[b]);
+            else mbar_arrive_remote(accum_empty_lead);
+          }
+        }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
-        if (lane == 0) {
-          if (h == 0) mbar_arrive(&sh->accum_empty[b]);
-          else mbar_arrive_remote(accum_empty_lead);
-          mbar_arrive(&sh->stg_ready);
-        }
+        if (lane == 0) mbar_arrive(&sh->stg_ready);
         if (warp == (int)kPairEpiWarp0) {
           int okw = 1;
           if (lane == 0) {
@@ -994,10 +1051,10 @@ cudaError_t launch_wide(const WeightView &W, const void *x, int64_t M, void *y, 
                                                ((size_t)(M * W.K * 2) + 255) / 256 * 256);
   // 1. fp16 rows with per-row power-of-two scales
   {
-    const unsigned blocks = (unsigned)((M * 32 + 255) / 256);
-    if (dt == Q1_F32) x_to_f16_kernel<Q1_F32><<<blocks, 256, 0, st>>>(x, (int)M, (int)W.K, x16, inv_scale);
-    else if (dt == Q1_F16) x_to_f16_kernel<Q1_F16><<<blocks, 256, 0, st>>>(x, (int)M, (int)W.K, x16, inv_scale);
-    else x_to_f16_kernel<Q1_BF16><<<blocks, 256, 0, st>>>(x, (int)M, (int)W.K, x16, inv_scale);
+    const unsigned blocks = (unsigned)M;  // one block per row
+    if (dt == Q1_F32) x_to_f16_kernel<Q1_F32><<<blocks, kPrepThreads, 0, st>>>(x, (int)W.K, x16, inv_scale);
+    else if (dt == Q1_F16) x_to_f16_kernel<Q1_F16><<<blocks, kPrepThreads, 0, st>>>(x, (int)W.K, x16, inv_scale);
+    else x_to_f16_kernel<Q1_BF16><<<blocks, kPrepThreads, 0, st>>>(x, (int)W.K, x16, inv_scale);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
