@@ -140,9 +140,8 @@ q1_status q1_qmm_narrow(const q1_weight *W, const void *x, int64_t M, q1_dtype d
 }
 
 size_t q1_qmm_workspace_size(int64_t M, int64_t N, int64_t K) {
-  (void)N;
   if (M < 1 || K < 128 || K % 128) return 0;
-  return q1::wide_workspace_bytes(M, K);
+  return q1::wide_workspace_bytes(M, N, K);
 }
 
 q1_status q1_qmm(const q1_weight *W, const void *x, int64_t M, q1_dtype dtype, void *y,
@@ -151,9 +150,9 @@ q1_status q1_qmm(const q1_weight *W, const void *x, int64_t M, q1_dtype dtype, v
   if (s != Q1_OK) return s;
   if (M <= g_max_rows.load() && W->K <= q1::kNarrowMaxK)
     return cuda_status(q1::launch_narrow(q1::view(W), x, M, y, (cudaStream_t)stream, true, dtype, dtype));
-  s = check_ws(workspace, workspace_bytes, q1::wide_workspace_bytes(M, W->K));
+  s = check_ws(workspace, workspace_bytes, q1::wide_workspace_bytes(M, W->N, W->K));
   if (s != Q1_OK) return s;
-  return cuda_status(q1::launch_wide(q1::view(W), x, M, y, workspace, (cudaStream_t)stream, dtype));
+  return cuda_status(q1::launch_wide(q1::view(W), x, M, y, workspace, workspace_bytes, (cudaStream_t)stream, dtype));
 }
 
 q1_status q1_embed_gather(const q1_weight *E, const int32_t *ids, int64_t T, q1_dtype out_t,

@@ -82,10 +82,12 @@ cudaError_t launch_narrow_gate_up(const WeightView &G, const WeightView &U, cons
                                   int64_t M, void *h, cudaStream_t st, bool pdl, q1_dtype xdt = Q1_BF16);
 
 // ---- wide path (q1_wide.cu)
-// workspace: fp16 activation rows [M][K] and per-row scales [M]
-size_t wide_workspace_bytes(int64_t M, int64_t K);
-// x [M][K] and y [M][N] in dt (bf16, fp16 or fp32)
-cudaError_t launch_wide(const WeightView &W, const void *x, int64_t M, void *y, void *ws,
+// workspace: fp16 activation rows [M][K], per-row scales [M] and, when the
+// launch plan for this shape shares tiles between CTA pairs, partial-sum slots
+// and share counts
+size_t wide_workspace_bytes(int64_t M, int64_t N, int64_t K);
+// x [M][K] and y [M][N] in dt (bf16, fp16 or fp32); ws of ws_bytes >= wide_workspace_bytes
+cudaError_t launch_wide(const WeightView &W, const void *x, int64_t M, void *y, void *ws, size_t ws_bytes,
                         cudaStream_t st, q1_dtype dt = Q1_BF16);
 // fixed prefill tiling (token_tile, split), or the automatic choice when invalid
 void set_pair_plan(int token_tile, int split);

@@ -184,8 +184,11 @@ constexpr int kPrepThreads = 256;
 template <int XDT>
 __global__ void __launch_bounds__(kPrepThreads) x_to_f16_kernel(const void *__restrict__ x, int K,
                                                                 __half *__restrict__ x16,
-                                                                float *__restrict__ inv_scale) {
+                                                                float *__restrict__ inv_scale,
+                                                                int *__restrict__ cnt, int ncnt) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // the stream schedule's share counts start at zero
+  for (int i = blockIdx.x * kPrepThreads + threadIdx.x; i < ncnt; i += gridDim.x * kPrepThreads) cnt[i] = 0;
   __shared__ float wmax[kPrepThreads / 32];
   const int m = blockIdx.x, tid = threadIdx.x;
   const void *row = static_cast<const char *>(x) + (size_t)m * K * (XDT == Q1_F32 ? 4 : 2);
@@ -302,6 +305,9 @@ struct __align__(8) PairShared {
   uint64_t drain;                 // final commit before the allocation is released
   uint64_t stg_ready;             // the epilogue warps' rows of the output tile are staged (8 warps)
   uint64_t stg_free;              // the previous tile's TMA store has read the staging buffer
+  uint64_t part_done;             // stream: the epilogue warps' partial sums are written (8 warps)
+  uint64_t last_ready;            // stream: the share's count is taken and last_flag set
+  volatile int last_flag;         // stream: this CTA completed the tile's shares
   uint32_t tmem_base;
   volatile int abort_flag;
 };
@@ -456,6 +462,31 @@ __device__ __forceinline__ void deq_pair(uint32_t s16, uint32_t b16, bool affine
   hi2 = hi16 | (hi16 << 16);
 }
 
+// A pair's work as segments: tile t with k-steps [ka, kb).  Round robin:
+// whole tiles t, t + t_step, ... (k-steps [lo, hi) of a split).  Stream:
+// the contiguous units [u, u1) of the flattened (tile, k-step) space, so
+// that a tile at either end of the range may be shared with the neighbour
+// pairs.
+struct SegIter {
+  int stream, T, KS, t, t_step, lo, hi, u, u1;
+  __device__ __forceinline__ bool next(int &tt, int &ka, int &kb) {
+    if (stream) {
+      if (u >= u1) return false;
+      tt = u / KS;
+      ka = u - tt * KS;
+      kb = min(KS, ka + (u1 - u));
+      u += kb - ka;
+      return true;
+    }
+    if (t >= T) return false;
+    tt = t;
+    ka = lo;
+    kb = hi;
+    t += t_step;
+    return true;
+  }
+};
+
 // One 128-k stage of one weight row: four words and their metadata.
 struct PairStage {
   uint4 w;
@@ -467,7 +498,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_y,
             const uint32_t *__restrict__ W, const uint16_t *__restrict__ S, const uint16_t *__restrict__ Bv,
             int M, int N, int K, const float *__restrict__ inv_scale, void *__restrict__ y, int NT, int ksplit,
-            int mbf16, int ydt, int gshift, int ystage) {
+            int mbf16, int ydt, int gshift, int ystage, int stream, float *__restrict__ part,
+            int *__restrict__ cnt) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char *base = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -501,6 +533,12 @@ pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
   }
   const int T = mtiles * ntiles;
   const int nks = ks_hi - ks_lo;
+  // stream schedule: pair pidx of P takes units [b(pidx), b(pidx + 1)), b(p) = p W / P
+  const int P = (int)(gridDim.x >> 1), pidx = (int)(blockIdx.x >> 1);
+  const int64_t Wu = (int64_t)T * KS;
+  const int u0 = stream ? (int)((int64_t)pidx * Wu / P) : 0;
+  const int u1 = stream ? (int)((int64_t)(pidx + 1) * Wu / P) : 0;
+  const SegIter segs0{stream, T, KS, t_first, t_step, ks_lo, ks_hi, u0, u1};
 
   if (tid == 0) {
     for (int s = 0; s < xstages; ++s) {
@@ -518,6 +556,8 @@ pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
     mbar_init(&sh->drain, 1);
     mbar_init(&sh->stg_ready, 8);
     mbar_init(&sh->stg_free, 1);
+    mbar_init(&sh->part_done, 8);
+    mbar_init(&sh->last_ready, 1);
     sh->abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(&tmap_x) : "memory");
@@ -545,9 +585,11 @@ pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
       asm volatile("griddepcontrol.wait;" ::: "memory");  // x16 comes from the prep kernel
       uint32_t s = 0, ph = 0;
       bool ok = true;
-      for (int t = t_first; t < T && ok; t += t_step) {
+      SegIter segs = segs0;
+      int t, ka, kb;
+      while (ok && segs.next(t, ka, kb)) {
         const int m0 = (t % mtiles) * NT;
-        for (int ks = ks_lo; ks < ks_hi; ++ks) {
+        for (int ks = ka; ks < kb; ++ks) {
           if (!(ok = pair_wait(&sh->empty_x[s], ph ^ 1u, sh, 0))) break;
           unsigned char *dst = ring + s * XS;
           mbar_arrive_expect_tx(&sh->full_x[s], XS);
@@ -566,19 +608,21 @@ pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
       const uint32_t idesc = (1u << 4) | ((uint32_t)(NT >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
       uint32_t s = 0, ph = 0, tl = 0, sx = 0;
       bool ok = true;
-      for (int t = t_first; t < T && ok; t += t_step, ++tl) {
-        // accumulator b of this tile, used for the u-th time
+      SegIter segs = segs0;
+      int t, ka, kb;
+      for (; ok && segs.next(t, ka, kb); ++tl) {
+        // accumulator b of this segment, used for the u-th time
         const uint32_t b = tl % nbuf, u = tl / nbuf, d_tmem = tmem + 160u * b;
         if (u > 0 && !(ok = pair_wait(&sh->accum_empty[b], (u - 1) & 1u, sh, 0))) break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        for (int ks = 0; ks < nks; ++ks) {
+        for (int ks = ka; ks < kb; ++ks) {
           if (!(ok = pair_wait(&sh->full[s], ph, sh, 0))) break;
           asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
           const uint32_t xs = smem_u32(ring + sx * XS);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             umma_pair(d_tmem, tmem + a_col0 + 64u * s + 8u * kk,
-                      sw128_desc(xs + (kk >> 2) * (XS / 2) + (kk & 3) * 32), idesc, (ks > 0 || kk > 0) ? 1u : 0u);
+                      sw128_desc(xs + (kk >> 2) * (XS / 2) + (kk & 3) * 32), idesc, (ks > ka || kk > 0) ? 1u : 0u);
           umma_commit_pair(&sh->empty[s], pair_mask);
           umma_commit_pair(&sh->empty_x[sx], pair_mask);
           if (++sx == (uint32_t)xstages) sx = 0;
@@ -600,23 +644,26 @@ pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
     const int wpr = K / 32, G = wpr >> gshift;     // words and metadata groups per row
     const bool affine = Bv != nullptr, mb = mbf16 != 0;
     const uint32_t a_lane = tmem + ((uint32_t)(32 * q) << 16) + a_col0;
+    // this CTA's k-steps in order: tile t, k-step ks in [lo, hi); a tile move
+    // adds tstep to t and takes ks back by span (round robin: whole tiles of
+    // the split's k range; stream: consecutive tiles of the unit range)
     const int my_tiles = t_first < T ? (T - 1 - t_first) / t_step + 1 : 0;
-    const uint32_t total = (uint32_t)nks * (uint32_t)my_tiles;
-    // A cursor over this set's stages: tile iteration ti, k-step ks and this
-    // thread's weight row n (-1 past the last tile).  It moves two stages at a
-    // time; only a move to the next tile costs a division.
+    const uint32_t total = stream ? (uint32_t)(u1 - u0) : (uint32_t)nks * (uint32_t)my_tiles;
+    const int k_lo = stream ? 0 : ks_lo, k_hi = stream ? KS : ks_hi, k_span = k_hi - k_lo;
+    const int k_tstep = stream ? 1 : t_step;
+    // A cursor over this set's stages: tile t, k-step ks and this thread's
+    // weight row n (-1 past the last tile).  It moves two stages at a time;
+    // only a move to the next tile costs a division.
     struct Cursor {
-      int ti, ks, n;
+      int t, ks, n;
     };
-    auto set_row = [&](Cursor &c) {
-      c.n = c.ti < my_tiles ? ((t_first + c.ti * t_step) / mtiles) * 256 + 128 * h + r : -1;
-    };
-    auto step2 = [&](Cursor &c) {
-      c.ks += 2;
-      if (c.ks >= ks_hi) {
-        while (c.ks >= ks_hi) {
-          c.ks -= nks;
-          ++c.ti;
+    auto set_row = [&](Cursor &c) { c.n = c.t < T ? (c.t / mtiles) * 256 + 128 * h + r : -1; };
+    auto advance = [&](Cursor &c, int by) {
+      c.ks += by;
+      if (c.ks >= k_hi) {
+        while (c.ks >= k_hi) {
+          c.ks -= k_span;
+          if (c.t < T) c.t += k_tstep;
         }
         set_row(c);
       }
@@ -649,19 +696,13 @@ pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
     uint32_t j = (uint32_t)ds;
     uint32_t xj = (uint32_t)ds, xph = 0;           // x stage of step j and its phase (xstages >= 4)
     uint32_t s = (uint32_t)ds, ph = 0;             // weight stage of step j and its phase (SA >= 3)
-    Cursor pf{0, ks_lo, 0};
+    Cursor pf{stream ? u0 / KS : t_first, stream ? u0 % KS : ks_lo, 0};
     set_row(pf);
-    // stage ds may already lie in the second tile when a tile has one k-step
-    pf.ks += ds;
-    while (pf.ks >= ks_hi) {
-      pf.ks -= nks;
-      ++pf.ti;
-    }
-    set_row(pf);
+    advance(pf, ds);  // stage ds may already lie in the next tile
     if (j < total) load(pf, cur);
-    step2(pf);
+    advance(pf, 2);
     if (j + 2 < total) load(pf, nx1);
-    step2(pf);
+    advance(pf, 2);
     for (; j < total; j += 2) {
       if (!warp_wait(&sh->empty[s], ph ^ 1u, sh, 0)) break;
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");  // the MMAs that read the slot are done
@@ -694,7 +735,7 @@ pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         else mbar_arrive_remote(full_lead0 + 8u * s);
       }
       if (j + 4 < total) load(pf, nx2);
-      step2(pf);
+      advance(pf, 2);
       cur = nx1;
       nx1 = nx2;
       xj += 2;
@@ -712,9 +753,14 @@ pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
     // ---------------- epilogue: warp (q, eh) reads TMEM lanes 32q.. and half eh of the token columns
     const int q = warp & 3, eh = (warp - (int)kPairEpiWarp0) >> 2;
     const int r = 32 * q + lane;
-    uint32_t tl = 0;
+    uint32_t tl = 0, ts = 0, pc = 0;  // segments, staged tiles and partial shares so far
     bool deps = false;
-    for (int t = t_first; t < T; t += t_step, ++tl) {
+    SegIter segs = segs0;
+    int t, ka, kb;
+    // the pair holding unit v of the stream schedule, and the first unit of pair p
+    auto pair_of_unit = [&](int64_t v) { return (int)(((v + 1) * P + Wu - 1) / Wu) - 1; };
+    auto first_unit = [&](int p) { return (int64_t)p * Wu / P; };
+    for (; segs.next(t, ka, kb); ++tl) {
       const uint32_t b = tl % nbuf, u = tl / nbuf;
       const uint32_t d_lane = tmem + ((uint32_t)(32 * q) << 16) + 160u * b;
       const uint32_t accum_empty_lead = accum_empty_lead0 + 8u * b;
@@ -729,11 +775,118 @@ pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
       // the two warps of a lane quarter take halves of the NT columns (multiples of 16)
       const int chalf = ((NT >> 1) + 15) & ~15;
       const int c_lo = eh * chalf, c_hi = min(NT, c_lo + chalf);
+      if (stream && !(ka == 0 && kb == KS)) {
+        // A share of tile t (k-steps [ka, kb)): its fp32 partial sums go to
+        // this pair's workspace slot, token-major [NT][128] per CTA half; the
+        // share that completes the tile's count last adds all shares in k
+        // order (a fixed order: the result does not depend on which is last)
+        // and writes the outputs.  No CTA waits for another.
+        const int64_t tb = (int64_t)t * KS;
+        const int p0 = pair_of_unit(tb), p1 = pair_of_unit(tb + KS - 1);
+        const int which = (int64_t)u0 >= tb ? 0 : 1;  // this pair's first segment, or its last
+        float *mine = part + ((size_t)(2 * pidx + which) * 2 + h) * ((size_t)NT * 128);
+        bool released = false;
+#pragma unroll 1
+        for (int c0 = c_lo; c0 < c_hi; c0 += 64) {
+          uint32_t va[32], vb[32];
+          tmem_ld32_issue(d_lane + (uint32_t)c0, va);
+          tmem_ld32_issue(d_lane + (uint32_t)(c0 + 32), vb);
+          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+          if (c0 + 64 >= c_hi) {
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) {
+              if (h == 0) mbar_arrive(&sh->accum_empty[b]);
+              else mbar_arrive_remote(accum_empty_lead);
+            }
+            released = true;
+          }
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (c0 + e < c_hi) mine[(size_t)(c0 + e) * 128 + r] = __uint_as_float(va[e]);
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (c0 + 32 + e < c_hi) mine[(size_t)(c0 + 32 + e) * 128 + r] = __uint_as_float(vb[e]);
+        }
+        if (!released) {
+          asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) {
+            if (h == 0) mbar_arrive(&sh->accum_empty[b]);
+            else mbar_arrive_remote(accum_empty_lead);
+          }
+        }
+        __threadfence();  // the partial sums are visible device-wide before the count
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->part_done);
+        if (warp == (int)kPairEpiWarp0 && lane == 0) {
+          int last = 0;
+          if (pair_wait(&sh->part_done, pc & 1u, sh, 0)) {
+            const int old = atomicAdd(&cnt[2 * t + h], 1);
+            last = old == p1 - p0;
+            if (last) cnt[2 * t + h] = 0;  // every share has counted: ready for the next call
+            __threadfence();
+          }
+          sh->last_flag = last;
+          mbar_arrive(&sh->last_ready);
+        }
+        if (!warp_wait(&sh->last_ready, pc & 1u, sh, 0)) break;
+        ++pc;
+        if (sh->last_flag) {
+          __threadfence();
+          // token c by warp c mod 8; lane l adds rows 4l .. 4l+3 over the shares
+          const int m0 = (t % mtiles) * NT, nb = (t / mtiles) * 256 + 128 * h;
+          // four tokens per round, every share's loads issued before they
+          // are added (the shares sit in L2; one round trip per round)
+          const int n4 = nb + 4 * lane;
+          const int ctop = min(NT, M - m0);
+          constexpr int kTok = 4;
+          for (int c0 = (warp - (int)kPairEpiWarp0) * kTok; c0 < ctop; c0 += 8 * kTok) {
+            float4 acc[kTok];
+#pragma unroll
+            for (int q2 = 0; q2 < kTok; ++q2) acc[q2] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int i = 0; i <= p1 - p0; ++i) {
+              const int pi = p0 + i;
+              const int wi = (i == 0 && first_unit(pi) < tb) ? 1 : 0;
+              const float *src = part + ((size_t)(2 * pi + wi) * 2 + h) * ((size_t)NT * 128) + 4 * lane;
+              float4 v[kTok];
+#pragma unroll
+              for (int q2 = 0; q2 < kTok; ++q2)
+                v[q2] = c0 + q2 < ctop ? __ldcg(reinterpret_cast<const float4 *>(src + (size_t)(c0 + q2) * 128))
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+              for (int q2 = 0; q2 < kTok; ++q2) {
+                acc[q2].x += v[q2].x;
+                acc[q2].y += v[q2].y;
+                acc[q2].z += v[q2].z;
+                acc[q2].w += v[q2].w;
+              }
+            }
+            if (n4 < N) {
+#pragma unroll
+              for (int q2 = 0; q2 < kTok; ++q2) {
+                const int m = m0 + c0 + q2;
+                if (c0 + q2 < ctop) {
+                  const float rs = inv_scale[m];
+                  const float a4[4] = {acc[q2].x * rs, acc[q2].y * rs, acc[q2].z * rs, acc[q2].w * rs};
+                  const size_t i0 = (size_t)m * N + n4;
+                  if (n4 + 4 <= N && (N & 3) == 0) {
+                    store4(y, i0, a4, ydt);
+                  } else {
+                    for (int e = 0; e < 4 && n4 + e < N; ++e) store1(y, i0 + e, a4[e], ydt);
+                  }
+                }
+              }
+            }
+          }
+        }
+        continue;
+      }
       if (!SPLIT && ystage) {
         // 16-bit outputs through the staging tile: the accumulator is released
         // as soon as it is read, and one TMA store writes the CTA's 128 rows x
         // NT tokens (clipping rows and tokens beyond N and M)
-        if (tl > 0 && !warp_wait(&sh->stg_free, (tl - 1) & 1u, sh, 0)) break;
+        if (ts > 0 && !warp_wait(&sh->stg_free, (ts - 1) & 1u, sh, 0)) break;
         // 64 columns per round: two loads, one wait; the accumulator is
         // released right after the last round's loads, before its conversion
         bool released = false;
@@ -783,7 +936,7 @@ pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
         if (warp == (int)kPairEpiWarp0) {
           int okw = 1;
           if (lane == 0) {
-            okw = pair_wait(&sh->stg_ready, tl & 1u, sh, 0);
+            okw = pair_wait(&sh->stg_ready, ts & 1u, sh, 0);
             if (okw) {
               tma_store_2d(&tmap_y, stg, (t / mtiles) * 256 + 128 * h, m0);
               asm volatile("cp.async.bulk.commit_group;" ::: "memory");
@@ -793,6 +946,7 @@ pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
           }
           if (!__shfl_sync(0xffffffffu, okw, 0)) break;
         }
+        ++ts;
         continue;
       }
       for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
@@ -912,9 +1066,19 @@ int pair_clusters(int ksplit) {
   return n;
 }
 
+// A launch plan: token tile NT, S pairs per tile (S > 1: cluster split), the
+// stream schedule, and the grid (2 CTAs per pair).
+struct PairPlan {
+  int NT, S;
+  bool stream;
+  unsigned grid;
+};
+
 template <bool SPLIT, bool G128>
-cudaError_t launch_pair_g(const WeightView &W, const __half *x16, int64_t M, const float *inv_scale, void *y, int NT,
-                          int ksplit, unsigned grid, cudaStream_t st, q1_dtype dt) {
+cudaError_t launch_pair_g(const WeightView &W, const __half *x16, int64_t M, const float *inv_scale, void *y,
+                          const PairPlan &p, float *part, int *cnt, cudaStream_t st, q1_dtype dt) {
+  const int NT = p.NT, ksplit = p.S;
+  const unsigned grid = p.grid;
   auto encode = get_encode();
   if (!encode) return cudaErrorNotSupported;
   CUtensorMap map;
@@ -961,39 +1125,50 @@ cudaError_t launch_pair_g(const WeightView &W, const __half *x16, int64_t M, con
   cfg.attrs = attrs;
   cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, pair_kernel<SPLIT, G128>, map, ymap, W.w, W.s, W.b, (int)M, (int)W.N, (int)W.K,
-                            inv_scale, y, NT, ksplit, W.mbf16 ? 1 : 0, (int)dt, W.gshift, ystage);
+                            inv_scale, y, NT, ksplit, W.mbf16 ? 1 : 0, (int)dt, W.gshift, ystage,
+                            p.stream ? 1 : 0, part, cnt);
 }
 
-// Token-tile width NT (a multiple of 16, at most 256) and split factor S
-// (1 to 4 pairs per tile) from a cost model in SM clocks, fitted to forced
-// plans on GB300: a 128-k step of a pair takes about 1024 clocks for any NT up
-// to 256 (8 MMAs of K = 16; narrower N does not shorten them, so wide tiles
-// are cheaper per token), the tiles run in rounds over the resident pairs (or
-// clusters of S pairs), consecutive single-accumulator tiles are separated
-// by the epilogue stall (~24 NT) and a split tile adds its partial-tile
-// reduction (~48 NT).  Ties go to the narrowest tile.
-struct PairPlan {
-  int NT, S;
-  unsigned grid;
-};
+// Token-tile width NT (a multiple of 16, at most 256) and the schedule, from
+// a cost model in SM clocks fitted to forced plans on GB300: a 128-k step of
+// a pair takes about 1024 clocks for any NT up to 256 (8 MMAs of K = 16;
+// narrower N does not shorten them, so wide tiles are cheaper per token).
+//   round robin (S = 1): whole tiles in rounds over the resident pairs;
+//     consecutive single-accumulator tiles are separated by the epilogue
+//     stall (~24 NT);
+//   cluster split (S = 2..4): S pairs per tile, each a k range, partial
+//     tiles summed through distributed shared memory (~48 NT);
+//   stream: each pair an equal run of (tile, k-step) units, so the work is
+//     spread evenly whatever the tile count; a tile shared by neighbour
+//     pairs costs partial-sum writes (~48 NT) and a reduction (~24 NT per
+//     share).
+// Ties go to the simpler schedule and the narrower tile.
 std::atomic<int> g_plan_nt{0}, g_plan_s{0};
 
 PairPlan plan_pair(int64_t M, int64_t N, int64_t K) {
+  const int64_t KS = K / 128, ntn = (N + 255) / 256;
+  auto stream_plan = [&](int NT) {
+    const int pairs = pair_clusters(1);
+    const int64_t T = ntn * ((M + NT - 1) / NT), Wu = T * KS;
+    const int64_t P = pairs < Wu ? pairs : Wu;
+    return PairPlan{NT, 1, true, (unsigned)(2 * P)};
+  };
   {
     const int NT = g_plan_nt.load(std::memory_order_relaxed), S = g_plan_s.load(std::memory_order_relaxed);
-    if (NT > 0 && (S == 1 || K / 128 >= 2 * S)) {
+    if (NT > 0 && S == 0 && pair_clusters(1) > 0) return stream_plan(NT);
+    if (NT > 0 && S > 0 && (S == 1 || KS >= 2 * S)) {
       const int clusters = pair_clusters(S);
       if (clusters > 0) {
-        const int64_t T = ((N + 255) / 256) * ((M + NT - 1) / NT);
-        return PairPlan{NT, S, S > 1 ? (unsigned)(T * 2 * S) : (unsigned)(2 * (T < clusters ? T : clusters))};
+        const int64_t T = ntn * ((M + NT - 1) / NT);
+        return PairPlan{NT, S, false, S > 1 ? (unsigned)(T * 2 * S) : (unsigned)(2 * (T < clusters ? T : clusters))};
       }
     }
   }
   constexpr double kStep = 1024.0;      // clocks per 128-k step of a pair
   constexpr double kEpilogue = 24.0;    // x NT clocks per single-accumulator tile
-  constexpr double kReduce = 48.0;      // x NT clocks per split tile
-  const int64_t KS = K / 128, ntn = (N + 255) / 256;
-  PairPlan best{256, 1, 0};
+  constexpr double kReduce = 48.0;      // x NT clocks per split tile (and per share written)
+  constexpr double kShareRead = 24.0;   // x NT clocks per share a stream reduction reads
+  PairPlan best{256, 1, false, 0};
   double best_cost = 1e300;
   for (int S = 1; S <= 4; ++S) {
     if (S > 1 && KS < 2 * S) continue;
@@ -1007,9 +1182,24 @@ PairPlan plan_pair(int64_t M, int64_t N, int64_t K) {
                           (dbuf ? 0.0 : (double)(rounds - 1) * kEpilogue * NT);
       if (cost < best_cost * 0.999) {
         best_cost = cost;
-        best.NT = NT;
-        best.S = S;
-        best.grid = S > 1 ? (unsigned)(T * 2 * S) : (unsigned)(2 * (T < clusters ? T : clusters));
+        best = PairPlan{NT, S, false, S > 1 ? (unsigned)(T * 2 * S) : (unsigned)(2 * (T < clusters ? T : clusters))};
+      }
+    }
+  }
+  const int pairs = pair_clusters(1);
+  if (pairs > 0) {
+    for (int NT = 16; NT <= 256; NT += 16) {
+      const int64_t T = ntn * ((M + NT - 1) / NT), Wu = T * KS;
+      const int64_t P = pairs < Wu ? pairs : Wu;
+      const int64_t units = (Wu + P - 1) / P;                  // k-steps of the longest run
+      const int64_t segs = (units + KS - 1) / KS + 1;          // segments of a run, at most
+      const int64_t shares = (KS + units - 1) / units + 1;     // shares of a tile, at most
+      const bool dbuf = NT <= kPairDbufMaxNT;
+      const double cost = (double)units * kStep + (dbuf ? 0.0 : (double)(segs - 1) * kEpilogue * NT) +
+                          kReduce * NT + kShareRead * NT * (double)shares;
+      if (cost < best_cost * 0.97) {
+        best_cost = cost;
+        best = stream_plan(NT);
       }
     }
   }
@@ -1017,50 +1207,77 @@ PairPlan plan_pair(int64_t M, int64_t N, int64_t K) {
 }
 
 cudaError_t launch_pair(const WeightView &W, const __half *x16, int64_t M, const float *inv_scale, void *y,
-                        cudaStream_t st, q1_dtype dt) {
-  const PairPlan p = plan_pair(M, W.N, W.K);
+                        const PairPlan &p, float *part, int *cnt, cudaStream_t st, q1_dtype dt) {
   if (p.grid == 0) return cudaErrorInvalidConfiguration;
   const bool g128 = W.gshift == 2;
   if (p.S > 1) {
-    return g128 ? launch_pair_g<true, true>(W, x16, M, inv_scale, y, p.NT, p.S, p.grid, st, dt)
-                : launch_pair_g<true, false>(W, x16, M, inv_scale, y, p.NT, p.S, p.grid, st, dt);
+    return g128 ? launch_pair_g<true, true>(W, x16, M, inv_scale, y, p, part, cnt, st, dt)
+                : launch_pair_g<true, false>(W, x16, M, inv_scale, y, p, part, cnt, st, dt);
   }
-  return g128 ? launch_pair_g<false, true>(W, x16, M, inv_scale, y, p.NT, 1, p.grid, st, dt)
-              : launch_pair_g<false, false>(W, x16, M, inv_scale, y, p.NT, 1, p.grid, st, dt);
+  return g128 ? launch_pair_g<false, true>(W, x16, M, inv_scale, y, p, part, cnt, st, dt)
+              : launch_pair_g<false, false>(W, x16, M, inv_scale, y, p, part, cnt, st, dt);
+}
+
+// Workspace: fp16 rows [M][K], row scales [M], and for the stream schedule
+// the pairs' partial-sum slots (two per pair, NT x 256 fp32 each) and a share
+// count per tile half (zeroed by the prep kernel).
+struct WideWs {
+  size_t x16, scale, part, cnt, total;
+};
+WideWs wide_ws(int64_t M, int64_t K, const PairPlan &p, int64_t N) {
+  auto up = [](size_t b) { return (b + 255) / 256 * 256; };
+  WideWs w{};
+  w.x16 = up((size_t)(M * K * 2));
+  w.scale = up((size_t)(M * 4));
+  if (p.stream) {
+    const int64_t T = ((N + 255) / 256) * ((M + p.NT - 1) / p.NT);
+    w.part = up((size_t)(p.grid / 2) * 2 * 2 * (size_t)p.NT * 128 * 4);
+    w.cnt = up((size_t)T * 2 * 4);
+  }
+  w.total = w.x16 + w.scale + w.part + w.cnt;
+  return w;
 }
 
 }  // namespace
 
 void set_pair_plan(int token_tile, int split) {
-  const bool ok = token_tile >= 16 && token_tile <= 256 && token_tile % 16 == 0 && split >= 1 && split <= 4;
+  const bool ok = token_tile >= 16 && token_tile <= 256 && token_tile % 16 == 0 && split >= 0 && split <= 4;
   g_plan_s.store(ok ? split : 0, std::memory_order_relaxed);
   g_plan_nt.store(ok ? token_tile : 0, std::memory_order_relaxed);
 }
 
-size_t wide_workspace_bytes(int64_t M, int64_t K) {
-  const size_t x16 = ((size_t)(M * K * 2) + 255) / 256 * 256;
-  return x16 + ((size_t)(M * 4) + 255) / 256 * 256;
+size_t wide_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  return wide_ws(M, K, plan_pair(M, N, K), N).total;
 }
 
-cudaError_t launch_wide(const WeightView &W, const void *x, int64_t M, void *y, void *ws,
+cudaError_t launch_wide(const WeightView &W, const void *x, int64_t M, void *y, void *ws, size_t ws_bytes,
                         cudaStream_t st, q1_dtype dt) {
   auto encode = get_encode();
   if (!encode) return cudaErrorNotSupported;
-  __half *x16 = static_cast<__half *>(ws);
-  float *inv_scale = reinterpret_cast<float *>(static_cast<char *>(ws) +
-                                               ((size_t)(M * W.K * 2) + 255) / 256 * 256);
-  // 1. fp16 rows with per-row power-of-two scales
+  const PairPlan plan = plan_pair(M, W.N, W.K);
+  const WideWs w = wide_ws(M, W.K, plan, W.N);
+  if (ws_bytes < w.total) return cudaErrorInvalidValue;  // the plan changed since the workspace was sized
+  char *wb = static_cast<char *>(ws);
+  __half *x16 = reinterpret_cast<__half *>(wb);
+  float *inv_scale = reinterpret_cast<float *>(wb + w.x16);
+  float *part = plan.stream ? reinterpret_cast<float *>(wb + w.x16 + w.scale) : nullptr;
+  int *cnt = plan.stream ? reinterpret_cast<int *>(wb + w.x16 + w.scale + w.part) : nullptr;
+  const int ncnt = plan.stream ? (int)(w.cnt / 4) : 0;
+  // 1. fp16 rows with per-row power-of-two scales (and the share counts zeroed)
   {
     const unsigned blocks = (unsigned)M;  // one block per row
-    if (dt == Q1_F32) x_to_f16_kernel<Q1_F32><<<blocks, kPrepThreads, 0, st>>>(x, (int)W.K, x16, inv_scale);
-    else if (dt == Q1_F16) x_to_f16_kernel<Q1_F16><<<blocks, kPrepThreads, 0, st>>>(x, (int)W.K, x16, inv_scale);
-    else x_to_f16_kernel<Q1_BF16><<<blocks, kPrepThreads, 0, st>>>(x, (int)W.K, x16, inv_scale);
+    if (dt == Q1_F32)
+      x_to_f16_kernel<Q1_F32><<<blocks, kPrepThreads, 0, st>>>(x, (int)W.K, x16, inv_scale, cnt, ncnt);
+    else if (dt == Q1_F16)
+      x_to_f16_kernel<Q1_F16><<<blocks, kPrepThreads, 0, st>>>(x, (int)W.K, x16, inv_scale, cnt, ncnt);
+    else
+      x_to_f16_kernel<Q1_BF16><<<blocks, kPrepThreads, 0, st>>>(x, (int)W.K, x16, inv_scale, cnt, ncnt);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   // 2. the pair kernel, launched as a programmatic dependent of the prep:
   //    barrier set-up, TMEM allocation and the first weight stages overlap it
-  return launch_pair(W, x16, M, inv_scale, y, st, dt);
+  return launch_pair(W, x16, M, inv_scale, y, plan, part, cnt, st, dt);
 }
 
 unsigned int read_and_clear_wide_errors(cudaStream_t st, cudaError_t *err) {

@@ -298,8 +298,10 @@ def set_qmm_max_rows(rows: int):
 
 
 def set_prefill_plan(token_tile: int = 0, split: int = 0):
-    """Fixed prefill tiling (token_tile tokens x 256 weight rows per tile,
-    split CTA pairs per tile); (0, 0) restores the automatic choice."""
+    """Fixed prefill tiling: token_tile tokens x 256 weight rows per tile;
+    split 1 = whole tiles per CTA pair, 2..4 = pairs of a cluster per tile,
+    0 = equal runs of work per pair (tiles shared through the workspace);
+    (0, 0) restores the automatic choice."""
     lib().q1_set_prefill_plan(int(token_tile), int(split))
 
 

@@ -172,8 +172,12 @@ q1_status q1_qmv(const q1_weight *W, const void *x, q1_dtype dtype, void *y, q1_
 q1_status q1_qmm_narrow(const q1_weight *W, const void *x, int64_t M, q1_dtype dtype,
                         void *y, q1_stream stream);
 /* Workspace of q1_qmm: fp16 activation rows and per-row scales of the prefill
- * path, M*K*2 + M*4 bytes rounded up (256-byte aligned).  The call needs it
- * only when M > q1_get_qmm_max_rows(); workspace may be NULL otherwise. */
+ * path (M*K*2 + M*4 bytes, each part rounded up to 256), plus, when the
+ * prefill plan for this shape and device shares tiles between CTA pairs,
+ * their fp32 partial sums (two tiles of 256 rows per pair) and a count per
+ * tile.  The size depends on the current device and on q1_set_prefill_plan:
+ * take it after both are set.  The call needs the workspace only when
+ * M > q1_get_qmm_max_rows(); workspace may be NULL otherwise. */
 size_t q1_qmm_workspace_size(int64_t M, int64_t N, int64_t K);
 q1_status q1_qmm(const q1_weight *W, const void *x, int64_t M, q1_dtype dtype, void *y,
                  void *workspace, size_t workspace_bytes, q1_stream stream);
@@ -185,11 +189,15 @@ int q1_get_qmm_max_rows(void);
 /* Tiling of the prefill path (no counterpart on the pages; a tuning and test
  * control).  By default (0, 0) each call picks it from the shape: tiles of
  * 256 weight rows x token_tile tokens, token_tile a multiple of 16 in
- * [16, 256], each shared by `split` CTA pairs (1..4) that take contiguous k
- * ranges and sum their partial tiles in a fixed order.  A pair set here is
- * used by every later prefill call (with split > 1, by those whose K holds at
- * least 2 * split groups of 128; others fall back to the automatic choice);
- * values outside those ranges restore the automatic choice.  Results are the same for every tiling up to the fp32
+ * [16, 256], and a schedule: split = 1 gives each CTA pair whole tiles in
+ * turn; split = 2..4 shares each tile among that many pairs of a cluster,
+ * which take contiguous k ranges and sum their partial tiles in a fixed
+ * order; split = 0 gives each pair an equal run of (tile, k range) work, a
+ * tile shared by neighbouring runs being summed in k order through the
+ * workspace.  A pair set here is used by every later prefill call (with
+ * split > 1, by those whose K holds at least 2 * split groups of 128; others
+ * fall back to the automatic choice); values outside those ranges restore the
+ * automatic choice.  Results are the same for every tiling up to the fp32
  * summation order. */
 void q1_set_prefill_plan(int token_tile, int split);
 

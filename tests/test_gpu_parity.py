@@ -253,12 +253,15 @@ def prefill_plan(q1):
     q1.set_prefill_plan(0, 0)
 
 
-# every token-tile width class and split factor of the pair kernel, forced:
+# every token-tile width class and schedule of the pair kernel, forced:
 # persistent tiles (split 1) with the staged TMA-store epilogue (N % 8 == 0)
-# and the direct one (N % 8 != 0, fp32 outputs), and split-K clusters of 2..4
-# pairs summing partial tiles through distributed shared memory
+# and the direct one (N % 8 != 0, fp32 outputs), split-K clusters of 2..4
+# pairs summing partial tiles through distributed shared memory, and equal
+# runs of work per pair (split 0) whose shared tiles are summed through the
+# workspace (here a tile is shared by up to a dozen pairs)
 @pytest.mark.parametrize("affine", [False, True])
-@pytest.mark.parametrize("NT,S", [(16, 1), (48, 1), (128, 1), (208, 1), (256, 1), (128, 2), (64, 3), (256, 4)])
+@pytest.mark.parametrize("NT,S", [(16, 1), (48, 1), (128, 1), (208, 1), (256, 1), (128, 2), (64, 3), (256, 4),
+                                  (256, 0), (128, 0), (48, 0)])
 def test_prefill_forced_plans(q1, prefill_plan, NT, S, affine):
     M, N, K = 300, 768, 2048
     t, x = _case(N, K, M, affine, seed=NT + 7 * S + affine)
@@ -270,7 +273,7 @@ def test_prefill_forced_plans(q1, prefill_plan, NT, S, affine):
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-@pytest.mark.parametrize("NT,S", [(208, 1), (96, 2)])
+@pytest.mark.parametrize("NT,S", [(208, 1), (96, 2), (160, 0)])
 def test_prefill_forced_plans_ragged(q1, prefill_plan, dtype, NT, S):
     M, N, K = 250, 600, 1280
     t = synth.q1_tensor(N, K, seed=801 + NT, affine=True)
@@ -284,7 +287,7 @@ def test_prefill_forced_plans_ragged(q1, prefill_plan, dtype, NT, S):
 
 
 @pytest.mark.parametrize("group", [32, 64])
-@pytest.mark.parametrize("NT,S", [(144, 1), (80, 3)])
+@pytest.mark.parametrize("NT,S", [(144, 1), (80, 3), (224, 0)])
 def test_prefill_forced_plans_small_groups(q1, prefill_plan, group, NT, S):
     M, N, K = 200, 512, 1536
     t = synth.q1_tensor(N, K, seed=811 + group, affine=True, group=group)
@@ -294,6 +297,22 @@ def test_prefill_forced_plans_small_groups(q1, prefill_plan, group, NT, S):
     y = q1.qmm(W, x.to(DEV))
     check_matmul(y, O.qmm(x, t.words, t.scales, t.biases, K), x,
                  O.dequantize_f32(t.words, t.scales, t.biases, K), f"prefill g{group} NT={NT} S={S}")
+
+
+def test_prefill_stream_repeated_calls_same_result(q1, prefill_plan):
+    # the share counts return to zero after each tile, and the shares are
+    # summed in k order: repeated calls give identical bits
+    M, N, K = 700, 1024, 4096
+    t, x = _case(N, K, M, True, seed=821)
+    W = q1.Q1Weight.from_host(t)
+    prefill_plan(256, 0)
+    xd = x.to(DEV)
+    ws = q1.qmm_workspace(M, N, K, DEV)
+    y0 = q1.qmm(W, xd, workspace=ws)
+    for _ in range(3):
+        assert torch.equal(q1.qmm(W, xd, workspace=ws), y0)
+    check_matmul(y0, O.qmm(x, t.words, t.scales, t.biases, K), x,
+                 O.dequantize_f32(t.words, t.scales, t.biases, K), "prefill stream repeated")
 
 
 def test_wide_workspace_required(q1):
