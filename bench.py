@@ -356,9 +356,10 @@ def weight_bytes_g(N, K, affine, group):
 
 def narrow_sweep(q1, synth, torch, device, stream):
     """GB/s of single launches (graph of launches over 12 distinct matrices,
-    150-210 MB, more than the L2) on the two 27B-class FFN shapes: M = 1..9
-    (M = 9 crosses to the prefill path at the default threshold), symmetric
-    and affine; and M = 1 with metadata per 64 and per 32 weights."""
+    150-210 MB, more than the L2) on the two 27B-class FFN shapes: M = 1..9,
+    12, 16 and 17 (9..16 run as two narrow launches at the default
+    threshold, 17 on the prefill path), symmetric and affine; and M = 1 with
+    metadata per 64 and per 32 weights."""
     out = {}
     nl = 12
     for name, N, K in (SHAPES[0], SHAPES[2]):
@@ -367,8 +368,8 @@ def narrow_sweep(q1, synth, torch, device, stream):
                               synth.device_scales(N, K, 320 + i, device),
                               synth.device_biases(N, K, 340 + i, device) if affine else None, K)
                   for i in range(nl)]
-            ws = q1.qmm_workspace(9, N, K, device)
-            for M in range(1, 10):
+            ws = q1.qmm_workspace(17, N, K, device)
+            for M in list(range(1, 10)) + [12, 16, 17]:
                 x = torch.randn((M, K), device=device).to(torch.bfloat16)
                 y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
                 t = graph_time(torch, [lambda W=W: q1.qmm(W, x, workspace=ws, out=y) for W in Ws], stream, per=24)

@@ -148,8 +148,23 @@ q1_status q1_qmm(const q1_weight *W, const void *x, int64_t M, q1_dtype dtype, v
                  void *workspace, size_t workspace_bytes, q1_stream stream) {
   q1_status s = matmul_common(W, x, M, dtype, y);
   if (s != Q1_OK) return s;
-  if (M <= g_max_rows.load() && W->K <= q1::kNarrowMaxK)
+  const int rows = g_max_rows.load();
+  if (M <= rows && W->K <= q1::kNarrowMaxK)
     return cuda_status(q1::launch_narrow(q1::view(W), x, M, y, (cudaStream_t)stream, true, dtype, dtype));
+  if (rows == q1::kNarrowMaxM && M <= 2 * q1::kNarrowMaxM && W->K <= q1::kNarrowMaxK) {
+    // 9..16 rows at the default threshold: two narrow launches of 8 rows and
+    // M - 8 rows, the second chained with PDL (it streams its weights while
+    // the first drains).  Twice the weight traffic costs less than the
+    // prefill path here, whose MMAs take as long for 16 tokens as for 256.
+    const size_t es = dtype == Q1_F32 ? 4 : 2;
+    const int64_t m0 = q1::kNarrowMaxM;
+    cudaError_t e = q1::launch_narrow(q1::view(W), x, m0, y, (cudaStream_t)stream, true, dtype, dtype);
+    if (e == cudaSuccess)
+      e = q1::launch_narrow(q1::view(W), static_cast<const char *>(x) + (size_t)m0 * W->K * es, M - m0,
+                            static_cast<char *>(y) + (size_t)m0 * W->N * es, (cudaStream_t)stream, true, dtype,
+                            dtype);
+    return cuda_status(e);
+  }
   s = check_ws(workspace, workspace_bytes, q1::wide_workspace_bytes(M, W->N, W->K));
   if (s != Q1_OK) return s;
   return cuda_status(q1::launch_wide(q1::view(W), x, M, y, workspace, workspace_bytes, (cudaStream_t)stream, dtype));

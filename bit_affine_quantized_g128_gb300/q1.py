@@ -283,7 +283,9 @@ def qmm(W: Q1Weight, x: torch.Tensor, workspace: Optional[torch.Tensor] = None,
     M = x2.shape[0]
     y = _out(out, (M, W.N), x.dtype, x.device)
     ws = workspace
-    if ws is None and (M > get_qmm_max_rows() or W.K > NARROW_MAX_K):
+    rows = get_qmm_max_rows()
+    narrow = W.K <= NARROW_MAX_K and (M <= rows or (rows == 8 and M <= 16))
+    if ws is None and not narrow:
         ws = qmm_workspace(M, W.N, W.K, x.device)
     if ws is not None:
         _cuda(ws, "workspace", x.device)

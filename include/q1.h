@@ -156,8 +156,10 @@ q1_status q1_pack_from_dense(const void *dense, q1_dtype in_t, int64_t N, int64_
  *   kept packed and no dense temporary (higgs PR #212, "What": narrow Q1
  *   matrix multiplies of up to 8 flattened rows).  Leading dimensions are
  *   flattened by the caller: x [B][T][K] is passed as M = B*T.
- * q1_qmm: any M >= 1.  M <= q1_get_qmm_max_rows() runs the narrow path;
- *   wider M runs the prefill path, which dequantizes weight stages straight
+ * q1_qmm: any M >= 1.  M <= q1_get_qmm_max_rows() runs the narrow path.
+ *   At the default threshold (8), 9 <= M <= 16 also runs it, as two
+ *   launches of 8 and M - 8 rows (no workspace needed): at these sizes that
+ *   is faster than the prefill path.  Wider M runs the prefill path, which dequantizes weight stages straight
  *   into tensor memory and multiplies them on the tcgen05 tensor cores of CTA
  *   pairs (no dense weight temporary).  Its operands are fp16: symmetric
  *   weights are exact and affine ones rounded once at 2^-11; the activations
@@ -176,8 +178,9 @@ q1_status q1_qmm_narrow(const q1_weight *W, const void *x, int64_t M, q1_dtype d
  * prefill plan for this shape and device shares tiles between CTA pairs,
  * their fp32 partial sums (two tiles of 256 rows per pair) and a count per
  * tile.  The size depends on the current device and on q1_set_prefill_plan:
- * take it after both are set.  The call needs the workspace only when
- * M > q1_get_qmm_max_rows(); workspace may be NULL otherwise. */
+ * take it after both are set.  The call needs the workspace only on the
+ * prefill path (M > q1_get_qmm_max_rows(), except 9..16 rows at the default
+ * threshold, or K > 40960); workspace may be NULL otherwise. */
 size_t q1_qmm_workspace_size(int64_t M, int64_t N, int64_t K);
 q1_status q1_qmm(const q1_weight *W, const void *x, int64_t M, q1_dtype dtype, void *y,
                  void *workspace, size_t workspace_bytes, q1_stream stream);

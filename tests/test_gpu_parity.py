@@ -345,6 +345,28 @@ def test_threshold_dispatch(q1):
         q1.qmm_narrow(W, x.to(DEV))  # M = 9 is not narrow
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("M", [9, 13, 16, 17])
+def test_qmm_nine_to_sixteen_rows(q1, dtype, M):
+    # at the default threshold, 9..16 rows run as two narrow launches (8 and
+    # M - 8 rows; the second one's x and y start 8 rows in), 17 rows on the
+    # prefill path; N = 601 leaves the second chunk's y at an odd row offset
+    N, K = 601, 1280
+    t = synth.q1_tensor(N, K, seed=901 + M, affine=True)
+    x = _acts(M, K, 902 + M, dtype)
+    W = q1.Q1Weight.from_host(t)
+    assert q1.get_qmm_max_rows() == 8
+    y = q1.qmm(W, x.to(DEV))
+    assert y.dtype == dtype
+    check_matmul(y, O.qmm(x, t.words, t.scales, t.biases, K), x,
+                 O.dequantize_f32(t.words, t.scales, t.biases, K), f"qmm M={M} {dtype}")
+    if M <= 16:
+        # the same bits as the narrow kernel on each chunk
+        y0 = q1.qmm_narrow(W, x[:8].to(DEV))
+        y1 = q1.qmm_narrow(W, x[8:].to(DEV))
+        assert torch.equal(y, torch.cat([y0, y1]))
+
+
 # ------------------------------------------------------------------ gather / head
 @pytest.mark.parametrize("affine", [False, True])
 def test_embed_gather_bit_exact(q1, affine):
