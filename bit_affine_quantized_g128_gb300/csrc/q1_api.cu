@@ -300,6 +300,32 @@ q1_status q1_check_symmetric(const q1_weight *W, int32_t *d_is_symmetric, q1_str
   return cuda_status(q1::launch_check_symmetric(q1::view(W), d_is_symmetric, (cudaStream_t)stream));
 }
 
+namespace {
+std::atomic<unsigned long long> g_wait_ns{2000000000ull};
+std::atomic<int> g_stall{0};
+q1_status push_diagnostics() {
+  const unsigned long long ns = g_wait_ns.load();
+  const int stall = g_stall.load();
+  cudaError_t e = q1::set_narrow_diagnostics(ns, stall);
+  if (e == cudaSuccess) e = q1::set_wide_diagnostics(ns, stall);
+  return cuda_status(e);
+}
+}  // namespace
+
+q1_status q1_set_wait_limit_ns(uint64_t ns) {
+  q1_status s = check_device();
+  if (s != Q1_OK) return s;
+  g_wait_ns.store(ns ? (unsigned long long)ns : 2000000000ull);
+  return push_diagnostics();
+}
+
+q1_status q1_set_stalled_producers(int stall) {
+  q1_status s = check_device();
+  if (s != Q1_OK) return s;
+  g_stall.store(stall ? 1 : 0);
+  return push_diagnostics();
+}
+
 q1_status q1_device_errors(unsigned int *flags, q1_stream stream) {
   q1_status s = check_device();
   if (s != Q1_OK) return s;

@@ -93,6 +93,10 @@ cudaError_t launch_wide(const WeightView &W, const void *x, int64_t M, void *y, 
 void set_pair_plan(int token_tile, int split);
 
 // ---- device error words (each translation unit with bounded waits owns one)
+// and the diagnostics of the bounded waits: their limit, and producers that
+// issue nothing (every wait for their data then runs out)
+cudaError_t set_narrow_diagnostics(unsigned long long wait_ns, int stall);
+cudaError_t set_wide_diagnostics(unsigned long long wait_ns, int stall);
 unsigned int read_and_clear_wide_errors(cudaStream_t st, cudaError_t *err);
 unsigned int read_and_clear_narrow_errors(cudaStream_t st, cudaError_t *err);
 

@@ -71,6 +71,11 @@ namespace cg = cooperative_groups;
 namespace q1 {
 
 __device__ unsigned int g_narrow_err = 0;
+// Diagnostics (set from the host between launches): the limit of every
+// bounded wait, and a switch that makes the producers issue nothing, so that
+// every wait for their data runs out (no copy is then in flight).
+__constant__ unsigned long long c_narrow_wait_ns = 2000000000ull;
+__constant__ int c_narrow_stall = 0;
 
 namespace {
 
@@ -82,7 +87,6 @@ constexpr int kMaxKS = 8;                         // CTAs per cluster (K slices)
 constexpr int kTileBytes = 16 * 64;               // 16 rows x 16 words
 constexpr int kSmemMax = 227 * 1024;
 constexpr int kRingBytes = 24 * 1024;             // ring slots per SM, in bytes (about)
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
 // Consumer warps along K for a CTA of qs spans.  Each warp owns one span,
 // except that 9 or 10 spans go to 8 warps and 5 spans to 4 warps; the spans
@@ -238,16 +242,20 @@ __device__ __forceinline__ bool mbar_try(uint32_t addr, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait, all inline (no call in the tile loop): false when it ran out
-// (the device error word is set).
+// (the device error word is set), or at once once any wait has run out (the
+// word stays set until the host reads and clears it).
 __device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity) {
   if (mbar_try(addr, parity)) return true;
   const unsigned long long t0 = globaltimer();
 #pragma unroll 1
   for (uint32_t i = 1;; ++i) {
     if (mbar_try(addr, parity)) return true;
-    if ((i & 15u) == 0u && globaltimer() - t0 > kWaitLimitNs) {
-      atomicOr(&g_narrow_err, 1u);
-      return false;
+    if ((i & 15u) == 0u) {
+      if (*(volatile unsigned int *)&g_narrow_err) return false;
+      if (globaltimer() - t0 > c_narrow_wait_ns) {
+        atomicOr(&g_narrow_err, 1u);
+        return false;
+      }
     }
   }
 }
@@ -425,50 +433,54 @@ narrow_kernel(const __grid_constant__ Maps maps, NarrowArgs a) {
       const uint32_t fb = full_s + 8 * slot;
       // the slot's previous tile has been read by its consumer warps
       mbar_wait(empty_s + 8 * slot, ph ^ 1u);
-      const uint32_t mdst = meta_s + slot * L.slot_meta;
-      if (lane == 0) {
-        const uint32_t bytes =
-            QS * kTileBytes + (FASTMETA ? (uint32_t)(16 * MROW) * (has_b ? 2u : 1u) : 0u);
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb), "r"(bytes) : "memory");
-        const CUtensorMap *wm = mat ? &maps.w[1] : &maps.w[0];
-        const uint32_t wdst = ring_s + slot * L.slot_words;
-        if (a.w3) {
-          // one box: 16 words x 16 rows x QS spans, laid out span by span as
-          // the per-span boxes would be
-          const CUtensorMap *wm3 = &maps.w3[mat][QS == QM ? 0 : 1];
-          asm volatile(
-              "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
-              "[%5];" ::"r"(wdst),
-              "l"(wm3), "r"(0), "r"(rt * 16), "r"(q_lo), "r"(fb)
-              : "memory");
-        } else {
-          for (int qs = 0; qs < QS; ++qs) tma_2d(wdst + qs * kTileBytes, wm, (q_lo + qs) * 16, rt * 16, fb);
+      // (diagnostics) a stalled producer issues nothing: the slot's full
+      // barrier never completes and the consumers' waits run out
+      if (!c_narrow_stall) {
+        const uint32_t mdst = meta_s + slot * L.slot_meta;
+        if (lane == 0) {
+          const uint32_t bytes =
+              QS * kTileBytes + (FASTMETA ? (uint32_t)(16 * MROW) * (has_b ? 2u : 1u) : 0u);
+          asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb), "r"(bytes) : "memory");
+          const CUtensorMap *wm = mat ? &maps.w[1] : &maps.w[0];
+          const uint32_t wdst = ring_s + slot * L.slot_words;
+          if (a.w3) {
+            // one box: 16 words x 16 rows x QS spans, laid out span by span as
+            // the per-span boxes would be
+            const CUtensorMap *wm3 = &maps.w3[mat][QS == QM ? 0 : 1];
+            asm volatile(
+                "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+                "[%5];" ::"r"(wdst),
+                "l"(wm3), "r"(0), "r"(rt * 16), "r"(q_lo), "r"(fb)
+                : "memory");
+          } else {
+            for (int qs = 0; qs < QS; ++qs) tma_2d(wdst + qs * kTileBytes, wm, (q_lo + qs) * 16, rt * 16, fb);
+          }
+          if (FASTMETA) {
+            tma_2d(mdst, mat ? &maps.s[1] : &maps.s[0], q_base * GPS, rt * 16, fb);
+            if (has_b) tma_2d(mdst + 16 * MROW, mat ? &maps.b[1] : &maps.b[0], q_base * GPS, rt * 16, fb);
+          }
         }
-        if (FASTMETA) {
-          tma_2d(mdst, mat ? &maps.s[1] : &maps.s[0], q_base * GPS, rt * 16, fb);
-          if (has_b) tma_2d(mdst + 16 * MROW, mat ? &maps.b[1] : &maps.b[0], q_base * GPS, rt * 16, fb);
+        if (!FASTMETA) {
+          const uint16_t *sp = mat ? a.s[1] : a.s[0];
+          const uint16_t *bp = mat ? a.b[1] : a.b[0];
+          // runs of 4 metadata values: (row, span, run) per lane, GPS / 4 runs per span
+          constexpr int RUNS = GPS / 4;
+          for (int e = lane; e < 16 * QS * RUNS * (has_b ? 2 : 1); e += 32) {
+            const int r = e & 15, c = (e >> 4) % RUNS, qs = (e >> 4) / RUNS % QS, isb = (e >> 4) / RUNS / QS;
+            const int64_t row = (int64_t)rt * 16 + r;
+            const int s = q_lo + qs;
+            const int g0 = s * GPS + 4 * c;
+            const uint16_t *src = (isb ? bp : sp) + row * GM + g0;
+            uint32_t h[4];
+  #pragma unroll
+            for (int u = 0; u < 4; ++u) h[u] = (row < N && g0 + u < GM) ? (uint32_t)__ldg(src + u) : 0u;
+            asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(mdst + isb * 16 * MROW + r * MROW +
+                                                                ((s - q_base) * GPS + 4 * c) * 2),
+                         "r"(h[0] | (h[1] << 16)), "r"(h[2] | (h[3] << 16))
+                         : "memory");
+          }
+          asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(fb) : "memory");
         }
-      }
-      if (!FASTMETA) {
-        const uint16_t *sp = mat ? a.s[1] : a.s[0];
-        const uint16_t *bp = mat ? a.b[1] : a.b[0];
-        // runs of 4 metadata values: (row, span, run) per lane, GPS / 4 runs per span
-        constexpr int RUNS = GPS / 4;
-        for (int e = lane; e < 16 * QS * RUNS * (has_b ? 2 : 1); e += 32) {
-          const int r = e & 15, c = (e >> 4) % RUNS, qs = (e >> 4) / RUNS % QS, isb = (e >> 4) / RUNS / QS;
-          const int64_t row = (int64_t)rt * 16 + r;
-          const int s = q_lo + qs;
-          const int g0 = s * GPS + 4 * c;
-          const uint16_t *src = (isb ? bp : sp) + row * GM + g0;
-          uint32_t h[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) h[u] = (row < N && g0 + u < GM) ? (uint32_t)__ldg(src + u) : 0u;
-          asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(mdst + isb * 16 * MROW + r * MROW +
-                                                              ((s - q_base) * GPS + 4 * c) * 2),
-                       "r"(h[0] | (h[1] << 16)), "r"(h[2] | (h[3] << 16))
-                       : "memory");
-        }
-        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(fb) : "memory");
       }
       __syncwarp();
       ++j;
@@ -1216,6 +1228,12 @@ cudaError_t launch_narrow_gate_up(const WeightView &G, const WeightView &U, cons
   }
   if (G.b || U.b) return launch_meta<2, true, 0>(a, G.w, U.w, st, pdl);
   return launch_meta<2, false, 0>(a, G.w, U.w, st, pdl);
+}
+
+cudaError_t set_narrow_diagnostics(unsigned long long wait_ns, int stall) {
+  cudaError_t e = cudaMemcpyToSymbol(c_narrow_wait_ns, &wait_ns, sizeof(wait_ns));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(c_narrow_stall, &stall, sizeof(stall));
+  return e;
 }
 
 unsigned int read_and_clear_narrow_errors(cudaStream_t st, cudaError_t *err) {

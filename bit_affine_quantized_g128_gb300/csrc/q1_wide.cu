@@ -38,10 +38,14 @@
 namespace q1 {
 
 __device__ unsigned int g_wide_err = 0;
+// Diagnostics (set from the host between launches): the limit of every
+// bounded wait, and a switch that makes the x producer issue nothing, so that
+// every wait for its data runs out (no copy is then in flight).
+__constant__ unsigned long long c_wide_wait_ns = 2000000000ull;
+__constant__ int c_wide_stall = 0;
 
 namespace {
 
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s: every barrier wait is bounded
 
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -362,7 +366,7 @@ __device__ __noinline__ bool pair_wait_slow(uint32_t addr, uint32_t parity, Pair
         sh->abort_flag = 1;
         return false;
       }
-      if (globaltimer() - t0 > kWaitLimitNs) {
+      if (globaltimer() - t0 > c_wide_wait_ns) {
         sh->abort_flag = 1;
         atomicOr(&g_wide_err, 1u);
         return false;
@@ -581,7 +585,8 @@ pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
 
   if (warp == 0) {
     // ---------------- TMA producer: this CTA's token half, two 64-k boxes per stage
-    if (lane == 0) {
+    // ((diagnostics) a stalled producer issues nothing)
+    if (lane == 0 && !c_wide_stall) {
       asm volatile("griddepcontrol.wait;" ::: "memory");  // x16 comes from the prep kernel
       uint32_t s = 0, ph = 0;
       bool ok = true;
@@ -1278,6 +1283,12 @@ cudaError_t launch_wide(const WeightView &W, const void *x, int64_t M, void *y, 
   // 2. the pair kernel, launched as a programmatic dependent of the prep:
   //    barrier set-up, TMEM allocation and the first weight stages overlap it
   return launch_pair(W, x16, M, inv_scale, y, plan, part, cnt, st, dt);
+}
+
+cudaError_t set_wide_diagnostics(unsigned long long wait_ns, int stall) {
+  cudaError_t e = cudaMemcpyToSymbol(c_wide_wait_ns, &wait_ns, sizeof(wait_ns));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(c_wide_stall, &stall, sizeof(stall));
+  return e;
 }
 
 unsigned int read_and_clear_wide_errors(cudaStream_t st, cudaError_t *err) {

@@ -25,6 +25,7 @@ EXPORTED = [
     "q1_qmm_narrow", "q1_qmm", "q1_set_qmm_max_rows", "q1_get_qmm_max_rows", "q1_set_prefill_plan",
     "q1_embed_gather", "q1_ffn_workspace_size", "q1_ffn_fused", "q1_check_symmetric",
     "q1_device_errors", "q1_status_string", "q1_ffn_fused_noalloc",
+    "q1_set_wait_limit_ns", "q1_set_stalled_producers",
     "q1_decode_chain_workspace_size", "q1_decode_chain", "q1_pack_from_dense",
 ]
 
@@ -79,6 +80,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "q1_set_qmm_max_rows": ([ctypes.c_int], None),
         "q1_get_qmm_max_rows": ([], ctypes.c_int),
         "q1_set_prefill_plan": ([ctypes.c_int, ctypes.c_int], None),
+        "q1_set_wait_limit_ns": ([ctypes.c_uint64], I32),
+        "q1_set_stalled_producers": ([ctypes.c_int], I32),
         "q1_embed_gather": ([W, P, I64, I32, P, P, P], I32),
         "q1_ffn_workspace_size": ([I64, I64, I64], SZ),
         "q1_ffn_fused": ([W, W, W, P, I64, I32, P, P, SZ, P], I32),
@@ -447,6 +450,17 @@ def check_symmetric(W: Q1Weight) -> torch.Tensor:
     r = torch.empty((1,), dtype=torch.int32, device=W.words.device)
     _check("q1_check_symmetric", lib().q1_check_symmetric(W.cref(), r.data_ptr(), _stream()))
     return r
+
+
+def set_wait_limit_ns(ns: int = 0):
+    """Limit of the kernels' bounded waits in ns (0 restores 2 s); for tests."""
+    _check("q1_set_wait_limit_ns", lib().q1_set_wait_limit_ns(int(ns)))
+
+
+def set_stalled_producers(stall: bool):
+    """Producers of later launches issue no copies, so that every wait for
+    their data runs out (results undefined); for tests of the timeout path."""
+    _check("q1_set_stalled_producers", lib().q1_set_stalled_producers(1 if stall else 0))
 
 
 def device_errors() -> int:

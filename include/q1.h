@@ -288,6 +288,22 @@ q1_status q1_check_symmetric(const q1_weight *W, int32_t *d_is_symmetric, q1_str
  * Q1_ERR_TIMEOUT if any bounded wait ran out since the last call. */
 q1_status q1_device_errors(unsigned int *flags, q1_stream stream);
 const char *q1_status_string(q1_status s);
+/* Controls of the bounded waits (no counterpart on the pages; for tests of
+ * the timeout path).  Every wait of the narrow and prefill kernels on another
+ * role's progress is bounded; one that runs out sets the device error word
+ * (bit 0: prefill kernels, bit 1: narrow kernels), and later waits of those
+ * kernels then give up at once until q1_device_errors reads the word.
+ * q1_set_wait_limit_ns: the bound, in ns of the GPU's global timer (default
+ *   2 s; 0 restores it).
+ * q1_set_stalled_producers: nonzero makes the producers of later launches
+ *   issue no copies, so that every wait for their data runs out; no copy is
+ *   then in flight when the kernels give up.  The results of such launches
+ *   are undefined; 0 restores normal launches.
+ * Both apply to the current device, to launches made after the call, and
+ * synchronize with the device; they are not meant to race with launches on
+ * other threads. */
+q1_status q1_set_wait_limit_ns(uint64_t ns);
+q1_status q1_set_stalled_producers(int stall);
 
 #ifdef __cplusplus
 }
