@@ -441,6 +441,32 @@ def profile_case(args):
         y = torch.empty((M, N), dtype=torch.bfloat16, device=device)
         for r in range(args.steps):
             q1.qmm_narrow(Ws[r % nl], x, out=y)
+    elif case.startswith("ffn"):  # fused FFN: narrow_kernel<2> gate/up, then the down projection
+        M = int(case.split("M")[-1])
+        nl = 4  # 4 x 62.9 MB of FFN weights: more than the L2
+        ffns = [[q1.Q1Weight(synth.device_weight_words(N, K, 21 + 3 * i + j, device),
+                             synth.device_scales(N, K, 121 + 3 * i + j, device), None, K)
+                 for j, (_, N, K) in enumerate((SHAPES[0], SHAPES[1], SHAPES[2]))] for i in range(nl)]
+        x = torch.randn((M, D_MODEL), device=device).to(torch.bfloat16)
+        y = torch.empty((M, D_MODEL), dtype=torch.bfloat16, device=device)
+        ws = q1.ffn_workspace(M, D_MODEL, D_FF, device)
+        for r in range(args.steps):
+            g, u, d = ffns[r % nl]
+            q1.ffn_fused(g, u, d, x, workspace=ws, out=y)
+    elif case == "elementwise":  # dequantize, unpack, pack, gather, symmetric check, repack, once each
+        W1 = q1.Q1Weight(synth.device_weight_words(D_FF, D_MODEL, 31, device),
+                         synth.device_scales(D_FF, D_MODEL, 131, device), None, D_MODEL)
+        sc = synth.device_scales(D_FF, D_MODEL, 231, device).clamp(min=2.0 ** -13)
+        Wb = q1.Q1Weight(W1.words, sc, (sc.float() * -0.5).to(torch.float16), D_MODEL)
+        ids = torch.randint(0, D_FF, (64,), device=device, dtype=torch.int32)
+        for r in range(args.steps):
+            dense = q1.dequantize(W1, torch.bfloat16)
+            bits = q1.unpack(W1.words, D_MODEL)
+            q1.pack(bits)
+            q1.embed_gather(W1, ids)
+            q1.check_symmetric(Wb)
+            q1.pack_from_dense(dense, symmetric=True)
+            del dense, bits
     else:  # prefill
         M = int(case.split("M")[-1])
         _, N, K = {"gate": SHAPES[0], "down": SHAPES[2], "attn": SHAPES[3]}[args.shape]
@@ -722,7 +748,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-worker", type=float, default=None, help=argparse.SUPPRESS)
     ap.add_argument("--profile", default=None,
-                    help="run a few launches of one case for ncu: decode | narrowM<m> | prefillM<m>")
+                    help="run a few launches of one case for ncu: decode | narrowM<m> | prefillM<m> | ffnM<m> | elementwise")
     ap.add_argument("--shape", default="gate", choices=["gate", "down", "attn"])
     args = ap.parse_args()
     if args.cpu_worker is not None:
