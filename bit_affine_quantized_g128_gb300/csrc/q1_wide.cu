@@ -1152,6 +1152,8 @@ std::atomic<int> g_plan_nt{0}, g_plan_s{0};
 
 PairPlan plan_pair(int64_t M, int64_t N, int64_t K) {
   const int64_t KS = K / 128, ntn = (N + 255) / 256;
+  // the stream schedule indexes (tile, k-step) units with 32-bit integers
+  auto stream_fits = [&](int NT) { return ntn * ((M + NT - 1) / NT) * KS < ((int64_t)1 << 31); };
   auto stream_plan = [&](int NT) {
     const int pairs = pair_clusters(1);
     const int64_t T = ntn * ((M + NT - 1) / NT), Wu = T * KS;
@@ -1160,7 +1162,7 @@ PairPlan plan_pair(int64_t M, int64_t N, int64_t K) {
   };
   {
     const int NT = g_plan_nt.load(std::memory_order_relaxed), S = g_plan_s.load(std::memory_order_relaxed);
-    if (NT > 0 && S == 0 && pair_clusters(1) > 0) return stream_plan(NT);
+    if (NT > 0 && S == 0 && pair_clusters(1) > 0 && stream_fits(NT)) return stream_plan(NT);
     if (NT > 0 && S > 0 && (S == 1 || KS >= 2 * S)) {
       const int clusters = pair_clusters(S);
       if (clusters > 0) {
@@ -1194,6 +1196,7 @@ PairPlan plan_pair(int64_t M, int64_t N, int64_t K) {
   const int pairs = pair_clusters(1);
   if (pairs > 0) {
     for (int NT = 16; NT <= 256; NT += 16) {
+      if (!stream_fits(NT)) continue;
       const int64_t T = ntn * ((M + NT - 1) / NT), Wu = T * KS;
       const int64_t P = pairs < Wu ? pairs : Wu;
       const int64_t units = (Wu + P - 1) / P;                  // k-steps of the longest run

@@ -198,9 +198,10 @@ int q1_get_qmm_max_rows(void);
  * order; split = 0 gives each pair an equal run of (tile, k range) work, a
  * tile shared by neighbouring runs being summed in k order through the
  * workspace.  A pair set here is used by every later prefill call (with
- * split > 1, by those whose K holds at least 2 * split groups of 128; others
- * fall back to the automatic choice); values outside those ranges restore the
- * automatic choice.  Results are the same for every tiling up to the fp32
+ * split > 1, by those whose K holds at least 2 * split groups of 128, and
+ * with split = 0, by those with fewer than 2^31 (tile, 128-k step) units;
+ * others fall back to the automatic choice); values outside those ranges
+ * restore the automatic choice.  Results are the same for every tiling up to the fp32
  * summation order. */
 void q1_set_prefill_plan(int token_tile, int split);
 
