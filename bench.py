@@ -45,7 +45,7 @@ WORKLOAD = "q1 decode QMV M=1, 64 layers x {gate,up 17408x5120; down 5120x17408;
 # DRAM traffic per launch of the narrow kernel on the gate shape (17408 x 5120,
 # M = 1), from ncu (dram__bytes_read.sum + dram__bytes_write.sum), and the
 # sha256 of q1_narrow.cu it was taken on; reported as null once the source differs.
-NCU_TRAFFIC = {"bytes": 12595968, "source_sha256": "231e1f91cf357b8cb2d173ad316699017b0c0d3e7f3fd69c0d6250d15b437fad"}
+NCU_TRAFFIC = {"bytes": 12595968, "source_sha256": "0201254629d1d1b5ea93a42192705cbc0d0d9ed479514163062b1f3d6e07356e"}
 
 
 def weight_bytes(N, K, affine):

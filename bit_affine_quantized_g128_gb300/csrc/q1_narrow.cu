@@ -242,20 +242,17 @@ __device__ __forceinline__ bool mbar_try(uint32_t addr, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait, all inline (no call in the tile loop): false when it ran out
-// (the device error word is set), or at once once any wait has run out (the
-// word stays set until the host reads and clears it).
+// (the device error word is set).  Each wait runs out on its own limit: a
+// check of the error word in the polling loop cost 1.3 % on the decode step.
 __device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity) {
   if (mbar_try(addr, parity)) return true;
   const unsigned long long t0 = globaltimer();
 #pragma unroll 1
   for (uint32_t i = 1;; ++i) {
     if (mbar_try(addr, parity)) return true;
-    if ((i & 15u) == 0u) {
-      if (*(volatile unsigned int *)&g_narrow_err) return false;
-      if (globaltimer() - t0 > c_narrow_wait_ns) {
-        atomicOr(&g_narrow_err, 1u);
-        return false;
-      }
+    if ((i & 15u) == 0u && globaltimer() - t0 > c_narrow_wait_ns) {
+      atomicOr(&g_narrow_err, 1u);
+      return false;
     }
   }
 }

@@ -292,8 +292,9 @@ const char *q1_status_string(q1_status s);
 /* Controls of the bounded waits (no counterpart on the pages; for tests of
  * the timeout path).  Every wait of the narrow and prefill kernels on another
  * role's progress is bounded; one that runs out sets the device error word
- * (bit 0: prefill kernels, bit 1: narrow kernels), and later waits of those
- * kernels then give up at once until q1_device_errors reads the word.
+ * (bit 0: prefill kernels, bit 1: narrow kernels).  Later waits of the
+ * prefill kernels then give up at once until q1_device_errors reads the word;
+ * those of the narrow kernels each run out on their own limit.
  * q1_set_wait_limit_ns: the bound, in ns of the GPU's global timer (default
  *   2 s; 0 restores it).
  * q1_set_stalled_producers: nonzero makes the producers of later launches
