@@ -332,19 +332,20 @@ def time_prefill(q1, synth, torch, device, M, shape, affine, reps=20):
     e1.record()
     torch.cuda.synchronize()
     t = e0.elapsed_time(e1) / 1e3 / reps
-    # unfused comparator: dequantize to bf16, then a dense bf16 GEMM (cuBLAS via torch)
-    wd = [q1.dequantize(Ws[i], torch.bfloat16) for i in range(2)]
-    torch.matmul(xs[0], wd[0].T, out=ys[0])
+    # unfused comparator: dequantize to bf16, then a dense bf16 GEMM (cuBLAS via
+    # torch), over the same rotation of weights and activations (larger than L2)
+    for i in range(nl):
+        torch.matmul(xs[i], q1.dequantize(Ws[i], torch.bfloat16).T, out=ys[i])
     torch.cuda.synchronize()
     e0.record()
     for r in range(reps):
-        i = r % 2
+        i = r % nl
         tmp = q1.dequantize(Ws[i], torch.bfloat16)
         torch.matmul(xs[i], tmp.T, out=ys[i])
     e1.record()
     torch.cuda.synchronize()
     t_unfused = e0.elapsed_time(e1) / 1e3 / reps
-    del Ws, xs, ys, wd
+    del Ws, xs, ys
     return 2.0 * M * N * K / t / 1e12, 2.0 * M * N * K / t_unfused / 1e12
 
 
