@@ -65,6 +65,37 @@ def test_prefill_full_shapes(q1, M, N, K, affine):
     _check_rows(y, t, x, _rows(N, 48, M), f"prefill M={M} {N}x{K}")
 
 
+@pytest.mark.parametrize("M", [1000, 1024, 2048])
+@pytest.mark.parametrize("affine", [False, True])
+def test_prefill_attention_shape(q1, M, affine):
+    # the 5120 x 5120 projection at prefill sizes, in the plan each call picks
+    # (a ragged last token tile at M = 1000)
+    N = K = D_MODEL
+    t = synth.q1_tensor(N, K, seed=1011 + affine, affine=affine)
+    x = synth.activations(M, K, seed=1012)
+    W = q1.Q1Weight.from_host(t)
+    y = q1.qmm(W, x.to(DEV)).float().cpu().double().numpy()
+    _check_rows(y, t, x, _rows(N, 48, M + 7), f"prefill M={M} {N}x{K}")
+
+
+def test_prefill_attention_shape_stream_fp32_out(q1):
+    # the stream schedule forced, fp32 activations and outputs (its shared
+    # tiles' outputs are written by the share that completes them)
+    N = K = D_MODEL
+    M = 1000
+    t = synth.q1_tensor(N, K, seed=1013, affine=True)
+    x = synth.activations(M, K, seed=1014)
+    W = q1.Q1Weight.from_host(t)
+    q1.set_prefill_plan(256, 0)
+    try:
+        ws = q1.qmm_workspace(M, N, K, DEV)
+        y = q1.qmm(W, x.float().to(DEV), workspace=ws)
+    finally:
+        q1.set_prefill_plan(0, 0)
+    assert y.dtype == torch.float32
+    _check_rows(y.cpu().double().numpy(), t, x, _rows(N, 48, 17), "prefill stream fp32 M=1000")
+
+
 def test_dequantize_full_shape_bit_exact(q1):
     t = synth.q1_tensor(D_FF, D_MODEL, seed=1001, affine=True)
     W = q1.Q1Weight.from_host(t)
