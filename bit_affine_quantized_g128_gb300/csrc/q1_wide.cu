@@ -182,10 +182,14 @@ __device__ __forceinline__ void load8(const void *__restrict__ row, int i, float
 // [2^14, 2^15).  Multiplying by a power of two is exact; the fp16 rounding is
 // exact for every bf16 or fp16 activation whose scaled value is a normal fp16
 // number, and rounds fp32 activations once (2^-11).  One block of 256 threads
-// per row: the maximum pass keeps four independent loads in flight per
-// thread, and the conversion pass reads the row again (mostly from L2).
+// per row.  Rows of at most kPrepHeld chunks of 8 per thread are read once:
+// each thread keeps its chunks in registers between the maximum and the
+// conversion.  Longer rows take two passes: the maximum pass keeps four
+// independent loads in flight per thread, and the conversion pass reads the
+// row again (mostly from L2).
 constexpr int kPrepThreads = 256;
-template <int XDT>
+constexpr int kPrepHeld = 4;
+template <int XDT, bool HELD>
 __global__ void __launch_bounds__(kPrepThreads) x_to_f16_kernel(const void *__restrict__ x, int K,
                                                                 __half *__restrict__ x16,
                                                                 float *__restrict__ inv_scale,
@@ -198,7 +202,24 @@ __global__ void __launch_bounds__(kPrepThreads) x_to_f16_kernel(const void *__re
   const void *row = static_cast<const char *>(x) + (size_t)m * K * (XDT == Q1_F32 ? 4 : 2);
   const int n8 = K / 8;  // chunks of 8 activations
   float mx = 0.f;
-  int i = tid;
+  float fh[HELD ? kPrepHeld : 1][8];  // the held chunks tid + u * kPrepThreads
+  if constexpr (HELD) {
+#pragma unroll
+    for (int u = 0; u < kPrepHeld; ++u) {
+      const int c = tid + u * kPrepThreads;
+      if (c < n8) {
+        load8<XDT>(row, c, fh[u]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) fh[u][j] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kPrepHeld; ++u)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) mx = fmaxf(mx, fabsf(fh[u][j]));
+  }
+  int i = HELD ? n8 : tid;
   for (; i + 3 * kPrepThreads < n8; i += 4 * kPrepThreads) {
     float f[4][8];
 #pragma unroll
@@ -231,10 +252,7 @@ __global__ void __launch_bounds__(kPrepThreads) x_to_f16_kernel(const void *__re
   const float sc = __uint_as_float((uint32_t)(127 + e) << 23);   // 2^e, exact
   const float isc = __uint_as_float((uint32_t)(127 - e) << 23);  // 2^-e, exact
   uint4 *out = reinterpret_cast<uint4 *>(x16 + (size_t)m * K);
-#pragma unroll 4
-  for (int c = tid; c < n8; c += kPrepThreads) {
-    float f[8];
-    load8<XDT>(row, c, f);
+  auto convert = [&](const float (&f)[8], int c) {
     uint32_t o[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -242,6 +260,20 @@ __global__ void __launch_bounds__(kPrepThreads) x_to_f16_kernel(const void *__re
       o[q] = *reinterpret_cast<const uint32_t *>(&h);
     }
     out[c] = make_uint4(o[0], o[1], o[2], o[3]);
+  };
+  if constexpr (HELD) {
+#pragma unroll
+    for (int u = 0; u < kPrepHeld; ++u) {
+      const int c = tid + u * kPrepThreads;
+      if (c < n8) convert(fh[u], c);
+    }
+  } else {
+#pragma unroll 4
+    for (int c = tid; c < n8; c += kPrepThreads) {
+      float f[8];
+      load8<XDT>(row, c, f);
+      convert(f, c);
+    }
   }
   if (tid == 0) inv_scale[m] = isc;
 }
@@ -1268,12 +1300,17 @@ cudaError_t launch_wide(const WeightView &W, const void *x, int64_t M, void *y, 
   // 1. fp16 rows with per-row power-of-two scales (and the share counts zeroed)
   {
     const unsigned blocks = (unsigned)M;  // one block per row
-    if (dt == Q1_F32)
-      x_to_f16_kernel<Q1_F32><<<blocks, kPrepThreads, 0, st>>>(x, (int)W.K, x16, inv_scale, cnt, ncnt);
-    else if (dt == Q1_F16)
-      x_to_f16_kernel<Q1_F16><<<blocks, kPrepThreads, 0, st>>>(x, (int)W.K, x16, inv_scale, cnt, ncnt);
-    else
-      x_to_f16_kernel<Q1_BF16><<<blocks, kPrepThreads, 0, st>>>(x, (int)W.K, x16, inv_scale, cnt, ncnt);
+    const bool held = W.K / 8 <= kPrepHeld * kPrepThreads;
+    if (dt == Q1_F32) {
+      if (held) x_to_f16_kernel<Q1_F32, true><<<blocks, kPrepThreads, 0, st>>>(x, (int)W.K, x16, inv_scale, cnt, ncnt);
+      else x_to_f16_kernel<Q1_F32, false><<<blocks, kPrepThreads, 0, st>>>(x, (int)W.K, x16, inv_scale, cnt, ncnt);
+    } else if (dt == Q1_F16) {
+      if (held) x_to_f16_kernel<Q1_F16, true><<<blocks, kPrepThreads, 0, st>>>(x, (int)W.K, x16, inv_scale, cnt, ncnt);
+      else x_to_f16_kernel<Q1_F16, false><<<blocks, kPrepThreads, 0, st>>>(x, (int)W.K, x16, inv_scale, cnt, ncnt);
+    } else {
+      if (held) x_to_f16_kernel<Q1_BF16, true><<<blocks, kPrepThreads, 0, st>>>(x, (int)W.K, x16, inv_scale, cnt, ncnt);
+      else x_to_f16_kernel<Q1_BF16, false><<<blocks, kPrepThreads, 0, st>>>(x, (int)W.K, x16, inv_scale, cnt, ncnt);
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
