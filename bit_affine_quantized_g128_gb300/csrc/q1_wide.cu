@@ -28,6 +28,7 @@
 // as the shared-memory operand instead, every MMA re-read the weight tile
 // from shared memory and the dequantizers' stores drained slowly behind those
 // reads: the k-steps ran at about half the MMA rate.)
+#include <type_traits>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -934,19 +935,32 @@ pair_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ 
             }
             released = true;
           }
+          // the output type and whether all 64 columns exist are decided once
+          // per round, not per value
+          auto stage = [&](auto f16, auto full) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float f = __uint_as_float(va[e]) * __shfl_sync(0xffffffffu, rs_a, e);
-            const uint16_t o = ydt == Q1_F16 ? __half_as_ushort(__float2half_rn(f))
-                                             : __bfloat16_as_ushort(__float2bfloat16_rn(f));
-            if (c0 + e < c_hi) stg[(c0 + e) * 128 + r] = o;
-          }
+            for (int e = 0; e < 32; ++e) {
+              const float f = __uint_as_float(va[e]) * __shfl_sync(0xffffffffu, rs_a, e);
+              const uint16_t o = decltype(f16)::value ? __half_as_ushort(__float2half_rn(f))
+                                                      : __bfloat16_as_ushort(__float2bfloat16_rn(f));
+              if (decltype(full)::value || c0 + e < c_hi) stg[(c0 + e) * 128 + r] = o;
+            }
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float f = __uint_as_float(vb[e]) * __shfl_sync(0xffffffffu, rs_b, e);
-            const uint16_t o = ydt == Q1_F16 ? __half_as_ushort(__float2half_rn(f))
-                                             : __bfloat16_as_ushort(__float2bfloat16_rn(f));
-            if (c0 + 32 + e < c_hi) stg[(c0 + 32 + e) * 128 + r] = o;
+            for (int e = 0; e < 32; ++e) {
+              const float f = __uint_as_float(vb[e]) * __shfl_sync(0xffffffffu, rs_b, e);
+              const uint16_t o = decltype(f16)::value ? __half_as_ushort(__float2half_rn(f))
+                                                      : __bfloat16_as_ushort(__float2bfloat16_rn(f));
+              if (decltype(full)::value || c0 + 32 + e < c_hi) stg[(c0 + 32 + e) * 128 + r] = o;
+            }
+          };
+          using T_ = std::true_type;
+          using F_ = std::false_type;
+          if (c0 + 64 <= c_hi) {
+            if (ydt == Q1_F16) stage(T_{}, T_{});
+            else stage(F_{}, T_{});
+          } else {
+            if (ydt == Q1_F16) stage(T_{}, F_{});
+            else stage(F_{}, F_{});
           }
         }
         if (!released) {  // no columns for this warp
