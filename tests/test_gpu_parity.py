@@ -286,6 +286,21 @@ def test_prefill_forced_plans_ragged(q1, prefill_plan, dtype, NT, S):
                  O.dequantize_f32(t.words, t.scales, t.biases, K), f"prefill ragged NT={NT} S={S} {dtype}")
 
 
+@pytest.mark.parametrize("NT,S", [(256, 1), (256, 0), (128, 1)])
+def test_prefill_forced_plans_fp16_out(q1, prefill_plan, NT, S):
+    # fp16 activations and outputs through the staged epilogue: full rounds of
+    # 64 columns, a last token tile of 88 tokens (M = 600), N % 8 == 0
+    M, N, K = 600, 768, 1280
+    t = synth.q1_tensor(N, K, seed=806 + NT + S, affine=True)
+    x = _acts(M, K, 807, torch.float16)
+    W = q1.Q1Weight.from_host(t)
+    prefill_plan(NT, S)
+    y = q1.qmm(W, x.to(DEV))
+    assert y.dtype == torch.float16
+    check_matmul(y, O.qmm(x, t.words, t.scales, t.biases, K), x,
+                 O.dequantize_f32(t.words, t.scales, t.biases, K), f"prefill fp16 NT={NT} S={S}")
+
+
 @pytest.mark.parametrize("group", [32, 64])
 @pytest.mark.parametrize("NT,S", [(144, 1), (80, 3), (224, 0)])
 def test_prefill_forced_plans_small_groups(q1, prefill_plan, group, NT, S):
