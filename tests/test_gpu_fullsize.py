@@ -78,6 +78,18 @@ def test_prefill_attention_shape(q1, M, affine):
     _check_rows(y, t, x, _rows(N, 48, M + 7), f"prefill M={M} {N}x{K}")
 
 
+@pytest.mark.parametrize("M", [8192, 16384])
+def test_prefill_many_token_tiles(q1, M):
+    # 32 to 64 token tiles per weight-row tile: long runs of tiles per pair,
+    # in the plan each call picks; sampled rows, every token
+    N, K = 768, 1024
+    t = synth.q1_tensor(N, K, seed=1015, affine=True)
+    x = synth.activations(M, K, seed=1016)
+    W = q1.Q1Weight.from_host(t)
+    y = q1.qmm(W, x.to(DEV)).float().cpu().double().numpy()
+    _check_rows(y, t, x, _rows(N, 32, M), f"prefill M={M} {N}x{K}")
+
+
 def test_prefill_attention_shape_stream_fp32_out(q1):
     # the stream schedule forced, fp32 activations and outputs (its shared
     # tiles' outputs are written by the share that completes them)
